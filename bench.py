@@ -1,0 +1,423 @@
+"""Benchmark of the S4 layer forward pass (kernel generation + fused FFT
+convolution) on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one s4_layer_fwd over one batch of the workload N=64, r=1, H=256,
+L=1024, batch 16 (synthetic inputs resident in HBM).  Input/output buffer sets
+rotate so that the bytes touched between two uses of the same buffer exceed
+twice the L2 size.  `value` is channel-samples per second (batch*H*L per step,
+summed over ranks / max time over ranks).  `e2e` times the same call with the
+input copied from pinned host memory and the output copied back every step.
+Per-kernel durations come from the library's launch events (CUDA events on
+the launch stream) over a second pass of K steps.  The CPU baseline is the
+float64 oracle on the host cores.  `--impl reference` times that oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "S4 layer fwd channel-samples/s (B·H·L/s); Cauchy terms/s; % FP32 / HBM roofline"
+UNIT = "channel-samples/s"
+WORKLOAD_INDEX = 1
+SM_COUNT_NOMINAL = 152
+FP32_LANES_PER_SM = 128
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is busy."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception as e:  # no nvidia-smi
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.err or "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "structured_state_space_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_FILES = {
+    "conv": ["fft_rows.cu", "s4_dev.cuh", "s4_plan.cuh"],
+    "cauchy": ["cauchy.cu", "s4_dev.cuh"],
+    "spectrum": ["fft_rows.cu", "s4_dev.cuh", "s4_plan.cuh"],
+    "ifft": ["fft_rows.cu", "s4_dev.cuh", "s4_plan.cuh"],
+    "tau": ["cauchy.cu"],
+}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_hash") != kernel_source_hash(KERNEL_FILES[kernel]):
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm) -- run in spawned worker processes
+# ---------------------------------------------------------------------------
+
+def _oracle_init():
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["MKL_NUM_THREADS"] = "1"
+
+
+def _oracle_channel(args):
+    """Oracle on one channel: its kernel and every batch row's convolution.
+    Returns the channel-samples produced."""
+    h, = args
+    import numpy as np  # noqa: F401
+    import oracle.s4_oracle as O
+    from structured_state_space_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    p, u = _oracle_data()
+    K = O.s4_kernel(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["Ctilde"][h], p["dt"][h], w.L)
+    for b in range(w.batch):
+        O.causal_conv(K, u[b, h], p["D"][h])
+    return w.batch * w.L
+
+
+_DATA = None
+
+
+def _oracle_data():
+    global _DATA
+    if _DATA is None:
+        from structured_state_space_gb300 import workloads as W
+        w = W.WORKLOADS[WORKLOAD_INDEX]
+        p = W.make_params(w)
+        _DATA = (p, W.make_u(w, p))
+    return _DATA
+
+
+def _worker_start():
+    _oracle_init()
+    _oracle_data()
+
+
+def make_pool(procs):
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(procs, initializer=_worker_start)
+    pool.map(_oracle_channel, [(0,)] * procs)  # warm: imports, data, caches
+    return pool
+
+
+def oracle_rate(pool, procs, channels):
+    t0 = time.perf_counter()
+    samples = sum(pool.map(_oracle_channel, [(h,) for h in channels]))
+    dt = time.perf_counter() - t0
+    return samples / dt, dt, samples
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import structured_state_space_gb300 as s4
+    from structured_state_space_gb300 import build as s4build
+    from structured_state_space_gb300 import workloads as W
+
+    rank, local_rank, world = dist_env()
+    # CPU baseline pool first: spawned before any GPU work
+    pool, procs = None, 0
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        procs = max(1, os.cpu_count() or 1)
+        pool = make_pool(procs)
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        s4build.build()
+    if world > 1:
+        dist.barrier()
+    s4.load()
+
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    H, N, r, L, Bsz, M = w.H, w.N, w.r, w.L, w.batch, w.M
+    p = W.make_params(w)
+    u_host = W.make_u(w, p)
+    dev = torch.device("cuda", local_rank)
+    prm = {k: torch.from_numpy(np.ascontiguousarray(p[k])).to(dev) for k in ["Lambda", "P", "Q", "B", "Ctilde", "dt", "D"]}
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    set_bytes = Bsz * H * L * (4 + 8)
+    nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    u_d = [torch.from_numpy(u_host).to(dev) for _ in range(nsets)]
+    y_d = [torch.empty((Bsz, H, L), dtype=torch.complex64, device=dev) for _ in range(nsets)]
+    K_d = torch.empty((H, L), dtype=torch.complex64, device=dev)
+    ws = s4.workspace(H, N, r, L, Bsz, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s4.s4_layer_fwd(prm["Lambda"], prm["P"], prm["Q"], prm["B"], prm["Ctilde"], prm["dt"], prm["D"],
+                        u_d[i % nsets], K=K_d, y=y_d[i % nsets], ws=ws, stream=stream)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st = s4.s4_get_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {s4.s4_status_str(st)}")
+
+    def timed(fn, k):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(k):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            dist.barrier()
+        return ms
+
+    K = args.steps
+    ms_total = timed(step, K)
+    clocks = sampler.stop()
+
+    # per-kernel durations: the library's launch events over K more steps
+    s4.timing.reset()
+    s4.timing.enable(True)
+    ms_prof = timed(step, K)
+    s4.timing.enable(False)
+    kern = {}
+    for name in ["tau", "cauchy", "ifft", "spectrum", "conv"]:
+        n, t = s4.timing.read(name)
+        kern[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1), "share": 0.0}
+    s4.timing.reset()
+    tot = sum(v["avg_us"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["avg_us"] / tot if tot > 0 else 0.0
+
+    # end to end through the public call: pinned host input in, output back
+    u_pin = torch.from_numpy(u_host).pin_memory()
+    y_pin = torch.empty((Bsz, H, L), dtype=torch.complex64).pin_memory()
+
+    def e2e_step(i):
+        u_d[0].copy_(u_pin, non_blocking=True)
+        s4.s4_layer_fwd(prm["Lambda"], prm["P"], prm["Q"], prm["B"], prm["Ctilde"], prm["dt"], prm["D"],
+                        u_d[0], K=K_d, y=y_d[0], ws=ws, stream=stream)
+        y_pin.copy_(y_d[0], non_blocking=True)
+
+    e2e_steps = max(3, min(K, 200))
+    for i in range(3):
+        e2e_step(i)
+    ms_e2e = timed(e2e_step, e2e_steps)
+
+    samples_step = Bsz * H * L
+    value = samples_step * world * K / (ms_total / 1e3)
+    e2e_value = samples_step * world * e2e_steps / (ms_e2e / 1e3)
+
+    peaks, peak_src = read_peaks()
+    # roofline of the dominant kernel
+    dom = max(kern, key=lambda k: kern[k]["avg_us"])
+    fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    if dom == "cauchy":
+        flops = H * M * N * (8 * (r + 1) ** 2 + 6)
+        ach = flops / (kern[dom]["avg_us"] * 1e-6) / 1e12
+        roof = {"kernel": "cauchy_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": ach / fp32_peak, "traffic": profiled_traffic("cauchy"),
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
+                "algorithmic": f"{8 * (r + 1) ** 2 + 6} flop per (channel, root, pole)"}
+    else:
+        # algorithmic bytes of the named kernel per launch
+        if dom == "conv":
+            byts = Bsz * H * L * (4 + 8) + H * 2 * M * 8
+            desc = "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"
+        elif dom == "spectrum":
+            byts = H * L * 8 + H * 2 * M * 8
+            desc = "K 8 B per tap in, spectrum 8 B per 2M bin out"
+        elif dom == "ifft":
+            byts = H * M * 8 + H * L * 8
+            desc = "root values 8 B in, K 8 B out"
+        else:
+            byts = M * 8
+            desc = "table 8 B per root"
+        ach = byts / (kern[dom]["avg_us"] * 1e-6) / 1e9
+        roof = {"kernel": f"{dom}_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic(dom), "algorithmic": desc}
+    roof["peak_kind"] = f"of {peak_src}"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": w.name, "N": N, "r": r, "H": H, "L": L, "M": M, "batch": Bsz,
+                   "parallelism": f"replica x{world} (channels independent, no collective)",
+                   "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB (> 2x L2 {l2 / 2**20:.0f} MiB)"},
+        "cauchy_terms_per_s": H * M * N * (r + 1) ** 2 * world * K / (ms_total / 1e3),
+        "gpu_launches": 5 * K,
+        "kernels": kern,
+        "profiled_pass_ms_per_step": ms_prof / K,
+        "roofline": roof,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(u_host.nbytes),
+                "d2h_bytes_per_step": int(Bsz * H * L * 8), "steps": e2e_steps},
+    }
+    if pool is not None:
+        # bounded sample: every channel of the workload, each with all batch rows
+        chans = list(range(H))
+        rate, secs, samples = oracle_rate(pool, procs, chans)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": procs, "kind": "oracle",
+                                "sample": f"{len(chans)} channels x {Bsz} rows x L={L} ({samples} channel-samples, {secs:.1f} s wall)"}
+        pool.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from structured_state_space_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    procs = max(1, os.cpu_count() or 1)
+    pool = make_pool(procs)
+    # one step = one channel per worker process, each with every batch row
+    def step(i):
+        chans = [((i * procs) + j) % w.H for j in range(procs)]
+        return sum(pool.map(_oracle_channel, [(h,) for h in chans]))
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    samples = 0
+    for i in range(args.steps):
+        samples += step(args.warmup + i)
+    secs = time.perf_counter() - t0
+    pool.close()
+    value = samples / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": w.name, "N": w.N, "r": w.r, "H": w.H, "L": w.L, "M": w.M, "batch": w.batch},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
+                         "sample": f"per step {procs} channels x {w.batch} rows x L={w.L}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * s4.h -- C ABI of libs4: forward pass of the S4 structured state-space layer
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Model (page "Recurrent, LSTM, and structured state-space models", sections on
+ * the complex SISO state-space model and "DPLR structured state-space
+ * parameterization"):  per channel h,
+ *     A = Lambda - P Q^*          (Lambda diagonal N x N, P, Q in C^{N x r})
+ *     Abar = (I - Delta A/2)^{-1} (I + Delta A/2),  Bbar = (I - Delta A/2)^{-1} Delta B
+ *     K_j  = C^* Abar^j Bbar,  0 <= j < L          (length-L convolution kernel)
+ *     y_t  = sum_{j<=t} K_j u_{t-j} + D u_t         (causal convolution + skip term)
+ * The kernel is generated from the truncated output vector
+ *     C~ = (I - Abar^M)^* C,   M = least power of two >= L,
+ * which the filter procedure receives as given data.
+ *
+ * Conventions for every entry point
+ *  - Complex numbers are s4_c32 = {re, im} fp32 pairs (the memory layout of
+ *    torch.complex64 / std::complex<float>).  All arrays are dense row-major.
+ *  - Every array pointer is a DEVICE pointer owned by the caller.  The library
+ *    allocates no device memory and keeps no state between calls other than
+ *    per-device kernel attributes.  `ws` is caller-owned device scratch of at
+ *    least s4_workspace_bytes(...) bytes, 256-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *    enqueued asynchronously on it; no entry point synchronises the host
+ *    except s4_get_status.
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and returned synchronously.  Conditions that depend on device data
+ *    (resonances, non-finite values, a bad step size) are recorded in a
+ *    status word inside `ws` and read with s4_get_status; when one is
+ *    recorded, the affected output (K, or y) is written as all zeros.
+ *  - Concurrent calls that share one `ws` race; give each stream its own.
+ *
+ * Supported sizes: 1 <= H, 1 <= N <= 65536, 1 <= r <= 4, 1 <= L <= 65536,
+ * 1 <= batch.  Arrays u, y, K must be 16-byte aligned; others 8-byte aligned.
+ */
+#ifndef S4_H_
+#define S4_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct { float re, im; } s4_c32;
+
+typedef enum {
+    S4_OK = 0,
+    S4_ERR_INVALID_ARG = 1,          /* null pointer, size out of range, misaligned */
+    S4_ERR_WORKSPACE = 2,            /* ws missing, misaligned or too small */
+    S4_ERR_RESONANT_DIAGONAL = 3,    /* s(z_k) - lambda_j == 0 in fp32 at some root */
+    S4_ERR_RESONANT_CORRECTION = 4,  /* I_r + Q^* R(z_k) P singular at some root */
+    S4_ERR_NONFINITE = 5,            /* a root value or spectrum entry is inf/nan */
+    S4_ERR_INVALID_STEP = 6,         /* some Delta_h <= 0 or not finite */
+    S4_ERR_CUDA = 7                  /* a CUDA runtime call or launch failed */
+} s4_status;
+
+/* Bytes of scratch that s4_kernel_gen, s4_conv_fwd and s4_layer_fwd need for
+ * these sizes (the same number serves all three).  Returns 0 if the sizes are
+ * outside the supported range. */
+size_t s4_workspace_bytes(int H, int N, int r, int L, int batch);
+
+/*
+ * s4_kernel_gen -- the S4 filter: length-L kernel K from (Lambda, P, Q, B, C~, Delta).
+ * Page "Recurrent, LSTM, and structured state-space models", section "DPLR
+ * structured state-space parameterization", filter mode: with
+ * s(z) = (2/Delta)(1-z)/(1+z), R(z) = diag(1/(s(z) - lambda_j)),
+ * W(z) = I_r + Q^* R(z) P, the root values
+ *     H(z) = 2/(1+z) (C~^* R B - C~^* R P W^{-1} Q^* R B)
+ * at the M roots z_k = exp(-2 pi i k/M) (z = -1 by its finite value
+ * (Delta/2) C~^* B), followed by the inverse radix-two transform; K is its
+ * first L coefficients.  The resolvent sums are evaluated directly over the N
+ * poles in fp32 (the (r+1)^2 Cauchy sums of that section).
+ *   Lambda [H][N]    diagonal entries lambda_j per channel
+ *   P, Q   [H][N][r] low-rank factors (A = Lambda - P Q^*)
+ *   B      [H][N]    input vector
+ *   Ctilde [H][N]    truncated output vector C~_M
+ *   dt     [H]       step sizes Delta_h (fp32, must be > 0 and finite; checked on the device)
+ *   K      [H][L]    output kernel
+ * Device-detected statuses: S4_ERR_RESONANT_DIAGONAL, S4_ERR_RESONANT_CORRECTION,
+ * S4_ERR_NONFINITE, S4_ERR_INVALID_STEP (then K is all zeros).
+ */
+s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
+                        const s4_c32* B, const s4_c32* Ctilde, const float* dt,
+                        int H, int N, int r, int L, s4_c32* K,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * s4_conv_fwd -- causal convolution plus skip term for a batch of sequences.
+ * Page "Recurrent, LSTM, and structured state-space models": y_t = sum_{j<=t}
+ * K_j u_{t-j} + D u_t (direct term added separately); section "Roots-of-unity
+ * orthogonality and radix-two FFT cost": polynomial products by zero-padding
+ * to a radix-two length >= 2L-1.  Computed per row with FFTs of length 2M.
+ *   u [batch][H][L] real fp32 inputs
+ *   K [H][L]        kernel (complex)
+ *   D [H]           skip coefficients
+ *   y [batch][H][L] complex outputs
+ * Device-detected status: S4_ERR_NONFINITE (a non-finite kernel spectrum; y is zeros).
+ */
+s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D,
+                      int batch, int H, int L, s4_c32* y,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * s4_layer_fwd -- s4_kernel_gen followed by s4_conv_fwd on the same stream.
+ * K [H][L] receives the generated kernel (caller-owned; it is also an input of
+ * the convolution).  Statuses as for the two steps; a device-detected status
+ * from kernel generation makes both K and y all zeros.
+ */
+s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
+                       const s4_c32* B, const s4_c32* Ctilde, const float* dt,
+                       const float* D, const float* u,
+                       int batch, int H, int N, int r, int L,
+                       s4_c32* K, s4_c32* y,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then returns the device-detected status recorded in
+ * `ws` by the last entry point that used it (S4_OK if none), or
+ * S4_ERR_CUDA if the synchronisation or the read fails. */
+s4_status s4_get_status(const void* ws, void* stream);
+
+/* A static, human-readable name for a status value. */
+const char* s4_status_str(s4_status st);
+
+/* Optional per-kernel timing: when enabled, every kernel launch of the
+ * library is bracketed by CUDA events recorded on its launch stream.
+ * s4_timing_read syncs those events and returns, for the kernel family
+ * `name` ("cauchy", "ifft", "spectrum", "conv", "tau"), the number of
+ * launches and their summed duration in milliseconds since the last reset.
+ * Timing state is per process; it is meant for benchmarks, not for use
+ * from several host threads at once. */
+void s4_timing_enable(int on);
+void s4_timing_reset(void);
+int  s4_timing_read(const char* name, int* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* S4_H_ */

@@ -1,0 +1,214 @@
+"""S4 structured state-space layer, forward pass, on one NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``lib/libs4.so`` (declared in
+``include/s4.h``).  The functions here only marshal arguments: they check
+shapes and dtypes, take device pointers and the current CUDA stream from
+torch tensors, and call the library, whose kernels do all the work.  There is
+no fallback: if the library is missing or fails to load, these calls raise.
+
+Entry points (same names as the C ABI):
+    s4_kernel_gen(Lambda, P, Q, B, Ctilde, dt, L)      -> K [H][L] complex64
+    s4_conv_fwd(u, K, D)                               -> y [batch][H][L] complex64
+    s4_layer_fwd(Lambda, P, Q, B, Ctilde, dt, D, u)    -> (K, y)
+    s4_workspace_bytes(H, N, r, L, batch)
+    s4_get_status(ws), s4_status_str(code)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB as LIB_PATH
+
+__all__ = [
+    "S4Error", "load", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_workspace_bytes",
+    "s4_get_status", "s4_status_str", "workspace", "timing", "STATUS",
+]
+
+STATUS = {
+    0: "S4_OK", 1: "S4_ERR_INVALID_ARG", 2: "S4_ERR_WORKSPACE", 3: "S4_ERR_RESONANT_DIAGONAL",
+    4: "S4_ERR_RESONANT_CORRECTION", 5: "S4_ERR_NONFINITE", 6: "S4_ERR_INVALID_STEP", 7: "S4_ERR_CUDA",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+# Names of every function the C ABI exports (include/s4.h).
+ABI_FUNCTIONS = [
+    "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
+    "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
+]
+
+
+class S4Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        self.name = STATUS.get(self.code, f"status {code}")
+        super().__init__(f"{where}: {self.name} ({s4_status_str(self.code)})")
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libs4.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libs4 not built ({p} missing): run structured_state_space_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, sz, i32, f64p, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
+    lib.s4_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.s4_workspace_bytes.restype = sz
+    lib.s4_kernel_gen.argtypes = [vp] * 6 + [i32] * 4 + [vp, vp, sz, vp]
+    lib.s4_kernel_gen.restype = i32
+    lib.s4_conv_fwd.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]
+    lib.s4_conv_fwd.restype = i32
+    lib.s4_layer_fwd.argtypes = [vp] * 8 + [i32] * 5 + [vp, vp, vp, sz, vp]
+    lib.s4_layer_fwd.restype = i32
+    lib.s4_get_status.argtypes = [vp, vp]
+    lib.s4_get_status.restype = i32
+    lib.s4_status_str.argtypes = [i32]
+    lib.s4_status_str.restype = ctypes.c_char_p
+    lib.s4_timing_enable.argtypes = [i32]
+    lib.s4_timing_enable.restype = None
+    lib.s4_timing_reset.argtypes = []
+    lib.s4_timing_reset.restype = None
+    lib.s4_timing_read.argtypes = [ctypes.c_char_p, i32p, f64p]
+    lib.s4_timing_read.restype = i32
+    _lib = lib
+    return lib
+
+
+def s4_status_str(code: int) -> str:
+    return load().s4_status_str(int(code)).decode()
+
+
+def s4_workspace_bytes(H: int, N: int, r: int, L: int, batch: int) -> int:
+    return int(load().s4_workspace_bytes(H, N, r, L, batch))
+
+
+# ---------------------------------------------------------------------------
+# torch marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, dtype, shape, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(H, N, r, L, batch, device="cuda"):
+    """A device workspace of s4_workspace_bytes(...) bytes (a uint8 tensor)."""
+    torch = _torch()
+    n = s4_workspace_bytes(H, N, r, L, batch)
+    if n == 0:
+        raise S4Error(1, "s4_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _check(code, where):
+    if code != 0:
+        raise S4Error(code, where)
+
+
+def s4_kernel_gen(Lambda, P, Q, B, Ctilde, dt, L, K=None, ws=None, stream=None):
+    torch = _torch()
+    H, N = Lambda.shape
+    r = P.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+    if K is None:
+        K = torch.empty((H, L), dtype=c64, device=Lambda.device)
+    if ws is None:
+        ws = workspace(H, N, r, L, 1, Lambda.device)
+    code = load().s4_kernel_gen(
+        _ptr(Lambda, c64, (H, N), "Lambda"), _ptr(P, c64, (H, N, r), "P"), _ptr(Q, c64, (H, N, r), "Q"),
+        _ptr(B, c64, (H, N), "B"), _ptr(Ctilde, c64, (H, N), "Ctilde"), _ptr(dt, f32, (H,), "dt"),
+        H, N, r, L, _ptr(K, c64, (H, L), "K"), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _check(code, "s4_kernel_gen")
+    return K
+
+
+def s4_conv_fwd(u, K, D, y=None, ws=None, stream=None):
+    torch = _torch()
+    batch, H, L = u.shape
+    c64, f32 = torch.complex64, torch.float32
+    if y is None:
+        y = torch.empty((batch, H, L), dtype=c64, device=u.device)
+    if ws is None:
+        ws = workspace(H, 1, 1, L, batch, u.device)
+    code = load().s4_conv_fwd(
+        _ptr(u, f32, (batch, H, L), "u"), _ptr(K, c64, (H, L), "K"), _ptr(D, f32, (H,), "D"),
+        batch, H, L, _ptr(y, c64, (batch, H, L), "y"), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream(stream))
+    _check(code, "s4_conv_fwd")
+    return y
+
+
+def s4_layer_fwd(Lambda, P, Q, B, Ctilde, dt, D, u, K=None, y=None, ws=None, stream=None):
+    torch = _torch()
+    H, N = Lambda.shape
+    r = P.shape[-1]
+    batch, _, L = u.shape
+    c64, f32 = torch.complex64, torch.float32
+    if K is None:
+        K = torch.empty((H, L), dtype=c64, device=u.device)
+    if y is None:
+        y = torch.empty((batch, H, L), dtype=c64, device=u.device)
+    if ws is None:
+        ws = workspace(H, N, r, L, batch, u.device)
+    code = load().s4_layer_fwd(
+        _ptr(Lambda, c64, (H, N), "Lambda"), _ptr(P, c64, (H, N, r), "P"), _ptr(Q, c64, (H, N, r), "Q"),
+        _ptr(B, c64, (H, N), "B"), _ptr(Ctilde, c64, (H, N), "Ctilde"), _ptr(dt, f32, (H,), "dt"),
+        _ptr(D, f32, (H,), "D"), _ptr(u, f32, (batch, H, L), "u"), batch, H, N, r, L,
+        _ptr(K, c64, (H, L), "K"), _ptr(y, c64, (batch, H, L), "y"), ctypes.c_void_p(ws.data_ptr()),
+        ws.numel(), _stream(stream))
+    _check(code, "s4_layer_fwd")
+    return K, y
+
+
+def s4_get_status(ws, stream=None) -> int:
+    """Synchronise the stream and return the device-detected status code in ws."""
+    return int(load().s4_get_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
+
+
+class timing:
+    """Per-kernel launch timing recorded by the library (CUDA events on the
+    launch stream)."""
+
+    @staticmethod
+    def enable(on=True):
+        load().s4_timing_enable(1 if on else 0)
+
+    @staticmethod
+    def reset():
+        load().s4_timing_reset()
+
+    @staticmethod
+    def read(name):
+        n = ctypes.c_int(0)
+        ms = ctypes.c_double(0.0)
+        rc = load().s4_timing_read(name.encode(), ctypes.byref(n), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError("s4_timing_read failed")
+        return n.value, ms.value

@@ -1,0 +1,330 @@
+// Root values of the S4 filter on the radix-two root grid.
+//
+// "Recurrent, LSTM, and structured state-space models", section "DPLR
+// structured state-space parameterization", filter mode.  At the roots
+// z_k = exp(-2 pi i k/M), k != M/2,
+//     s(z_k) = (2/Delta)(1 - z_k)/(1 + z_k) = i a tan(pi k/M),   a = 2/Delta,
+//     R = diag(1/(s - lambda_j)),  W = I_r + Q^* R P,
+//     H(z_k) = 2/(1+z_k) (C~^* R B - C~^* R P W^{-1} Q^* R B),
+// and 2/(1 + z_k) = 1 + i tan(pi k/M).  The four resolvent families
+// C~^*RB, C~^*RP, Q^*RB, Q^*RP are the (r+1)^2 Cauchy sums of that section,
+// evaluated here directly over the N poles; the root z = -1 takes its finite
+// value (Delta/2) C~^* B.  Statuses: an fp32 denominator |s - lambda_j|^2 equal
+// to zero is 'resonant-diagonal'; an exactly singular W is 'resonant-correction'.
+//
+// Arithmetic: s is carried as an fp32 (hi, lo) pair (tan(pi k/M) from an fp64
+// table, a = 2/Delta split exactly), so that the difference s - lambda_j near a
+// resonance keeps full fp32 relative accuracy.  Each pole then costs one
+// reciprocal and 4 (r+1)^2 FMAs per root.
+#include <float.h>
+
+#include "s4_dev.cuh"
+#include "s4_internal.h"
+
+namespace s4dev {
+
+__global__ void tau_kernel(float2* __restrict__ tau, int M, int logC) {
+  const int pos = blockIdx.x * blockDim.x + threadIdx.x;
+  if (pos >= M) return;
+  const int Mc = M >> logC;
+  const int k = (pos % Mc) * (1 << logC) + pos / Mc;
+  double t = 0.0;
+  if (2 * k != M) {
+    const double x = (double)k / (double)M;
+    t = sinpi(x) / cospi(x);
+  }
+  const float hi = (float)t;
+  tau[pos] = make_float2(hi, (float)(t - (double)hi));
+}
+
+__device__ __forceinline__ float2 conj_mul(float2 a, float2 b) {  // conj(a) * b
+  return make_float2(fmaf(a.x, b.x, a.y * b.y), fmaf(a.x, b.y, -a.y * b.x));
+}
+
+__device__ __forceinline__ float2 crecip(float2 w) {
+  const float n = fmaf(w.x, w.x, w.y * w.y);
+  const float s = __fdiv_rn(1.f, n);
+  return make_float2(w.x * s, -w.y * s);
+}
+
+// Solve W z = v for an r x r complex system by Gaussian elimination with
+// partial pivoting; v is overwritten by z.  Returns false on an exactly zero pivot.
+template <int R>
+__device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
+#pragma unroll
+  for (int col = 0; col < R; ++col) {
+    int piv = col;
+    float best = fmaxf(fabsf(W[col][col].x), fabsf(W[col][col].y));
+#pragma unroll
+    for (int row = col + 1; row < R; ++row) {
+      const float m = fmaxf(fabsf(W[row][col].x), fabsf(W[row][col].y));
+      if (m > best) {
+        best = m;
+        piv = row;
+      }
+    }
+    if (!(best > 0.f)) return false;
+#pragma unroll
+    for (int row = col + 1; row < R; ++row) {
+      if (row == piv) {
+#pragma unroll
+        for (int c2 = 0; c2 < R; ++c2) {
+          const float2 t = W[col][c2];
+          W[col][c2] = W[row][c2];
+          W[row][c2] = t;
+        }
+        const float2 t = v[col];
+        v[col] = v[row];
+        v[row] = t;
+      }
+    }
+    const float2 inv = crecip(W[col][col]);
+#pragma unroll
+    for (int row = col + 1; row < R; ++row) {
+      const float2 f = cmul(W[row][col], inv);
+#pragma unroll
+      for (int c2 = col + 1; c2 < R; ++c2) W[row][c2] = csub(W[row][c2], cmul(f, W[col][c2]));
+      v[row] = csub(v[row], cmul(f, v[col]));
+    }
+  }
+#pragma unroll
+  for (int col = R - 1; col >= 0; --col) {
+    float2 acc = v[col];
+#pragma unroll
+    for (int c2 = col + 1; c2 < R; ++c2) acc = csub(acc, cmul(W[col][c2], v[c2]));
+    v[col] = cmul(acc, crecip(W[col][col]));
+  }
+  return true;
+}
+
+template <int RANK>
+struct CauchyLayout {
+  static constexpr int NW = (RANK + 1) * (RANK + 1);      // weight vectors
+  static constexpr int PS = (3 + 2 * NW + 3) / 4 * 4;     // floats per pole (float4-padded)
+  // weight order: 0: (C~,B); 1+l: (C~,P_l); 1+r+i: (Q_i,B); 1+2r+i r+l: (Q_i,P_l)
+};
+
+template <int RANK, int RPT, int T>
+__global__ void __launch_bounds__(T) cauchy_kernel(
+    const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
+    const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
+    const float2* __restrict__ tau, float2* __restrict__ Khat, int N, int M, int logC,
+    unsigned* __restrict__ status) {
+  using Lay = CauchyLayout<RANK>;
+  constexpr int NW = Lay::NW, PS = Lay::PS, JT = 128;
+  __shared__ __align__(16) float par[JT * PS];
+  __shared__ float2 red[T / 32 + 1];
+
+  const int h = blockIdx.x;
+  const float delta = dt[h];
+  const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
+  const int Mc = M >> logC;
+  // a = 2/Delta as an exact fp32 pair a_hi + a_lo
+  const float a_hi = bad ? 0.f : __fdiv_rn(2.f, delta);
+  const float a_lo = bad ? 0.f : __fdiv_rn(fmaf(-a_hi, delta, 2.f), delta);
+
+  int pos[RPT];
+  bool zm1[RPT];
+  float shi[RPT], slo[RPT], th[RPT];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    pos[rr] = (blockIdx.y * RPT + rr) * T + threadIdx.x;
+    const bool valid = pos[rr] < M;
+    const int k = valid ? (pos[rr] % Mc) * (1 << logC) + pos[rr] / Mc : 0;
+    const float2 tt = valid ? tau[pos[rr]] : make_float2(0.f, 0.f);
+    zm1[rr] = valid && M >= 2 && 2 * k == M;
+    const float p = a_hi * tt.x;
+    const float perr = fmaf(a_hi, tt.x, -p);
+    const float lo = perr + fmaf(a_hi, tt.y, a_lo * tt.x);
+    shi[rr] = zm1[rr] ? 0.f : p;
+    slo[rr] = zm1[rr] ? 0.f : lo;
+    th[rr] = tt.x;
+  }
+
+  float2 acc[RPT][NW];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr)
+#pragma unroll
+    for (int w = 0; w < NW; ++w) acc[rr][w] = make_float2(0.f, 0.f);
+  float2 cb = make_float2(0.f, 0.f);
+
+  for (int j0 = 0; j0 < N; j0 += JT) {
+    const int jn = min(JT, N - j0);
+    __syncthreads();
+    for (int jj = threadIdx.x; jj < jn; jj += T) {
+      const size_t j = (size_t)h * N + j0 + jj;
+      const float2 lam = Lambda[j], b = Bv[j], c = Ct[j];
+      float* pp = par + jj * PS;
+      pp[0] = lam.y;
+      pp[1] = lam.x * lam.x;
+      pp[2] = -lam.x;
+      float2 w = conj_mul(c, b);
+      cb = cadd(cb, w);
+      pp[3] = w.x;
+      pp[4] = w.y;
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) {
+        w = conj_mul(c, Pm[j * RANK + l]);
+        pp[3 + 2 * (1 + l)] = w.x;
+        pp[4 + 2 * (1 + l)] = w.y;
+      }
+#pragma unroll
+      for (int i = 0; i < RANK; ++i) {
+        const float2 qi = Qm[j * RANK + i];
+        w = conj_mul(qi, b);
+        pp[3 + 2 * (1 + RANK + i)] = w.x;
+        pp[4 + 2 * (1 + RANK + i)] = w.y;
+#pragma unroll
+        for (int l = 0; l < RANK; ++l) {
+          w = conj_mul(qi, Pm[j * RANK + l]);
+          pp[3 + 2 * (1 + 2 * RANK + i * RANK + l)] = w.x;
+          pp[4 + 2 * (1 + 2 * RANK + i * RANK + l)] = w.y;
+        }
+      }
+#pragma unroll
+      for (int f = 3 + 2 * NW; f < PS; ++f) pp[f] = 0.f;
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int jj = 0; jj < jn; ++jj) {
+      float pr[PS];
+      const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
+#pragma unroll
+      for (int v = 0; v < PS / 4; ++v) {
+        const float4 t = p4[v];
+        pr[4 * v] = t.x;
+        pr[4 * v + 1] = t.y;
+        pr[4 * v + 2] = t.z;
+        pr[4 * v + 3] = t.w;
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) {
+        const float dim = (shi[rr] - pr[0]) + slo[rr];
+        const float n2 = fmaf(dim, dim, pr[1]);
+        const float rn = rcp_approx(n2);
+        const float er = pr[2] * rn, ei = -dim * rn;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float wx = pr[3 + 2 * w], wy = pr[4 + 2 * w];
+          acc[rr][w].x = fmaf(wx, er, fmaf(-wy, ei, acc[rr][w].x));
+          acc[rr][w].y = fmaf(wx, ei, fmaf(wy, er, acc[rr][w].y));
+        }
+      }
+    }
+  }
+
+  // C~^* B over all poles, for the root z = -1
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cb.x += __shfl_xor_sync(0xffffffffu, cb.x, o);
+    cb.y += __shfl_xor_sync(0xffffffffu, cb.y, o);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cb;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float2 t = make_float2(0.f, 0.f);
+    for (int i = 0; i < T / 32; ++i) t = cadd(t, red[i]);
+    red[T / 32] = t;
+  }
+  __syncthreads();
+  const float2 cb_all = red[T / 32];
+
+  unsigned flags = bad ? ST_BAD_STEP : 0u;
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    if (pos[rr] >= M) continue;
+    float2 Hk = make_float2(0.f, 0.f);
+    if (!bad) {
+      if (zm1[rr]) {
+        Hk = cscale(cb_all, 0.5f * delta);
+      } else {
+        bool fin = true;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
+        if (!fin) {
+          // an exactly zero denominator gives inf/nan; tell it apart from overflow
+          bool res = false;
+          for (int j = 0; j < N; ++j) {
+            const float2 lam = Lambda[(size_t)h * N + j];
+            const float dim = (shi[rr] - lam.y) + slo[rr];
+            res = res || (fmaf(dim, dim, lam.x * lam.x) == 0.f);
+          }
+          flags |= res ? ST_RES_DIAG : ST_NONFINITE;
+          Khat[(size_t)h * M + pos[rr]] = Hk;
+          continue;
+        }
+        float2 Wm[RANK][RANK], z[RANK];
+#pragma unroll
+        for (int i = 0; i < RANK; ++i) {
+          z[i] = acc[rr][1 + RANK + i];
+#pragma unroll
+          for (int l = 0; l < RANK; ++l) {
+            Wm[i][l] = acc[rr][1 + 2 * RANK + i * RANK + l];
+            if (i == l) Wm[i][l].x += 1.f;
+          }
+        }
+        if (!solve_small<RANK>(Wm, z)) {
+          flags |= ST_RES_CORR;
+        } else {
+          float2 g = acc[rr][0];
+#pragma unroll
+          for (int l = 0; l < RANK; ++l) g = csub(g, cmul(acc[rr][1 + l], z[l]));
+          Hk = make_float2(fmaf(-th[rr], g.y, g.x), fmaf(th[rr], g.x, g.y));
+          if (!cfinite(Hk)) {
+            flags |= ST_NONFINITE;
+            Hk = make_float2(0.f, 0.f);
+          }
+        }
+      }
+    }
+    Khat[(size_t)h * M + pos[rr]] = Hk;
+  }
+  if (flags) atomicOr(status, flags);
+}
+
+}  // namespace s4dev
+
+namespace s4impl {
+using namespace s4dev;
+
+cudaError_t launch_tau(float2* tau, int M, int logC, cudaStream_t s) {
+  TimedLaunch tl("tau", s);
+  tau_kernel<<<(M + 255) / 256, 256, 0, s>>>(tau, M, logC);
+  return cudaGetLastError();
+}
+
+template <int RANK, int RPT>
+static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
+                                 const float2* B, const float2* Ct, const float* dt,
+                                 const float2* tau, float2* Khat, int H, int N, int M, int logC,
+                                 unsigned* status, cudaStream_t s) {
+  constexpr int T = 128;
+  const int tiles = (M + T * RPT - 1) / (T * RPT);
+  dim3 grid(H, tiles);
+  TimedLaunch tl("cauchy", s);
+  cauchy_kernel<RANK, RPT, T><<<grid, T, 0, s>>>(Lambda, P, Q, B, Ct, dt, tau, Khat, N, M, logC,
+                                                 status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
+                          const float2* Ct, const float* dt, const float2* tau, float2* Khat, int H,
+                          int N, int r, int M, int logC, unsigned* status, cudaStream_t s) {
+  // roots per thread: enough CTAs to fill the GPU for small M, more ILP for large M
+  const bool small = (long long)H * M < 4LL * 128 * 4 * num_sms() * 8;
+  switch (r) {
+    case 1:
+      return small ? cauchy_launch<1, 2>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s)
+                   : cauchy_launch<1, 4>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+    case 2:
+      return cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+    case 3:
+      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+    case 4:
+      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace s4impl

@@ -1,0 +1,346 @@
+// Row FFT kernels for rows longer than one CTA's shared memory holds
+// (length 2^15 .. 2^17).  A row of n = C m points is split over a thread-block
+// cluster of C CTAs by the four-step factorisation n = C x m:
+//   forward:  b_c[i] = w_n^{i c} * sum_q x[i + q m] w_C^{q c}     (cross-CTA, through DSMEM)
+//             X[c + C k] = sum_i b_c[i] w_m^{i k}                (local m-point FFT in CTA c)
+//   inverse:  g_c[i] = sum_k Y[c + C k] w_m^{-i k}               (local inverse in CTA c)
+//             y[i + q m] = (1/n) sum_c g_c[i] w_n^{-i c} w_C^{-q c} (cross-CTA)
+// Spectra therefore live in "blocked" order: CTA c owns bins c, c + C, ...
+// stored contiguously; the kernel spectrum and the root values of kernel
+// generation use the same layout, so no reordering pass is needed.
+// Remote shared-memory traffic uses plain DSMEM loads and stores.
+#include <cooperative_groups.h>
+
+#include "s4_internal.h"
+#include "s4_plan.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace s4dev {
+
+template <int LOGN>
+struct ClusterCfg {
+  static constexpr int LOGC = s4impl::cluster_log(LOGN);
+  static constexpr int C = 1 << LOGC;
+  static constexpr int LOGM = LOGN - LOGC;
+  static constexpr int n = 1 << LOGN, m = 1 << LOGM;
+  static constexpr int T = row_threads(LOGM);
+  static constexpr int NP = plan_npass(LOGM);
+  static constexpr int MI = m / C;   // cross-step indices owned by one CTA
+  static constexpr int PI = MI / T;  // ... per thread
+  static constexpr int TWF = plan_tw_size(LOGM, false);
+  static constexpr int TWI = plan_tw_size(LOGM, true);
+  static constexpr int PADM = padded_len(m);
+  static_assert(PI >= 1 && MI % T == 0, "cluster split");
+};
+
+// w_n^i for the indices i = c MI + il owned by CTA c.
+__device__ __forceinline__ void fill_cross_twiddles(float2* tw1, int c, int MI, int n, int tid, int nth) {
+  for (int il = tid; il < MI; il += nth) {
+    float s, co;
+    sincospif(2.0f * (float)(c * MI + il) / (float)n, &s, &co);
+    tw1[il] = make_float2(co, -s);
+  }
+}
+
+// Forward cross step for one row: x[i + q m] (q < C/2 from `load`, the rest zero
+// padding) -> radix-C DFT -> twiddle -> CTA q'.
+template <int LOGN, typename LoadF>
+__device__ __forceinline__ void cross_forward(cg::cluster_group& cl, float2* buf, const float2* tw1,
+                                              int c, int lt, LoadF load) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int C = Cf::C, MI = Cf::MI, T = Cf::T, m = Cf::m;
+#pragma unroll
+  for (int s = 0; s < Cf::PI; ++s) {
+    const int il = lt + s * T;
+    const int i = c * MI + il;
+    float2 x[C];
+#pragma unroll
+    for (int q = 0; q < C / 2; ++q) x[q] = load(s, q, i + q * m);
+    dft<C, false, true>(x);
+    apply_twiddles<C>(x, tw1[il]);
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      float2* dst = cl.map_shared_rank(buf, q);
+      dst[pad(i)] = x[q];
+    }
+  }
+}
+
+// Inverse cross step: gather g_c[i] from every CTA, twiddle, inverse radix-C DFT.
+template <int LOGN, bool HALF, typename StoreF>
+__device__ __forceinline__ void cross_inverse(cg::cluster_group& cl, float2* buf, const float2* tw1,
+                                              int c, int lt, StoreF store) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int C = Cf::C, MI = Cf::MI, T = Cf::T, m = Cf::m;
+#pragma unroll
+  for (int s = 0; s < Cf::PI; ++s) {
+    const int il = lt + s * T;
+    const int i = c * MI + il;
+    float2 x[C];
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      const float2* src = cl.map_shared_rank(buf, q);
+      x[q] = src[pad(i)];
+    }
+    float2 w = tw1[il];
+    w.y = -w.y;
+    apply_twiddles<C>(x, w);
+    dft<C, true, false, HALF>(x);
+#pragma unroll
+    for (int q = 0; q < (HALF ? C / 2 : C); ++q) store(s, q, i + q * m, x[q]);
+  }
+}
+
+// Kernel spectrum of n = 2M points per channel, blocked output order.
+template <int LOGN>
+__global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
+    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, unsigned* __restrict__ status) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
+  constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
+  cg::cluster_group cl = cg::this_cluster();
+  const int c = (int)cl.block_rank();
+  extern __shared__ float2 smem[];
+  float2* twf = smem;
+  float2* tw1 = twf + Cf::TWF;
+  float2* buf = tw1 + Cf::MI;
+  const int lt = threadIdx.x;
+  fill_plan_twiddles<LOGM, false>(twf, lt, T);
+  fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
+  __syncthreads();
+  cl.sync();
+  bool fin = true;
+  const int ncl = gridDim.x / Cf::C;
+  for (int h = blockIdx.x / Cf::C; h < H; h += ncl) {
+    cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int, int, int t) {
+      return t < L ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+    });
+    cl.sync();
+    run_passes<LOGM, false, 0, NP - 2, T>(buf, twf, lt);
+    const float2* twl = twf + plan_tw_off(LOGM, NP - 1, false);
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+      float2 a[RB];
+#pragma unroll
+      for (int q = 0; q < RB; ++q) a[q] = buf[pad(i + q * NBL)];
+      apply_twiddles<RB>(a, twl[i]);
+      dft<RB, false>(a);
+#pragma unroll
+      for (int q = 0; q < RB; ++q) {
+        fin = fin && cfinite(a[q]);
+        K2[(size_t)h * n + (size_t)c * m + i + q * NBL] = a[q];
+      }
+    }
+    cl.sync();
+  }
+  if (!fin) atomicOr(status, ST_NONFINITE);
+}
+
+// Inverse transform of M = n root values per channel (blocked input order),
+// first L outputs scaled by 1/M.
+template <int LOGN>
+__global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
+    const float2* __restrict__ Khat, float2* __restrict__ K, int H, int L,
+    const unsigned* __restrict__ status) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
+  constexpr int R0 = plan_radix(LOGM, 0, true), NB0 = m / R0, PER0 = NB0 / T;
+  cg::cluster_group cl = cg::this_cluster();
+  const int c = (int)cl.block_rank();
+  extern __shared__ float2 smem[];
+  float2* twi = smem;
+  float2* tw1 = twi + Cf::TWI;
+  float2* buf = tw1 + Cf::MI;
+  const int lt = threadIdx.x;
+  fill_plan_twiddles<LOGM, true>(twi, lt, T);
+  fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  __syncthreads();
+  cl.sync();
+  const float sc = 1.f / n;
+  const int ncl = gridDim.x / Cf::C;
+  for (int h = blockIdx.x / Cf::C; h < H; h += ncl) {
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {
+      const int i = lt + s * T;
+      float2 a[R0];
+#pragma unroll
+      for (int q = 0; q < R0; ++q) a[q] = Khat[(size_t)h * n + (size_t)c * m + i + q * NB0];
+      dft<R0, true>(a);
+#pragma unroll
+      for (int q = 0; q < R0; ++q) buf[pad(i * R0 + q)] = a[q];
+    }
+    __syncthreads();
+    run_passes<LOGM, true, 1, NP - 1, T>(buf, twi, lt);
+    cl.sync();
+    cross_inverse<LOGN, false>(cl, buf, tw1, c, lt, [&](int, int, int t, float2 v) {
+      if (t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(v, sc);
+    });
+    cl.sync();
+  }
+}
+
+// Fused causal convolution for rows of n = 2M > 16384 points.
+template <int LOGN>
+__global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
+    const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
+    float2* __restrict__ y, int rows, int H, int L, const unsigned* __restrict__ status) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
+  constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
+  cg::cluster_group cl = cg::this_cluster();
+  const int c = (int)cl.block_rank();
+  extern __shared__ float2 smem[];
+  float2* twf = smem;
+  float2* twi = twf + Cf::TWF;
+  float2* tw1 = twi + Cf::TWI;
+  float2* buf = tw1 + Cf::MI;
+  const int lt = threadIdx.x;
+  fill_plan_twiddles<LOGM, false>(twf, lt, T);
+  fill_plan_twiddles<LOGM, true>(twi, lt, T);
+  fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  __syncthreads();
+  cl.sync();
+  const float sc = 1.f / n;
+  const int ncl = gridDim.x / C;
+  for (int row = blockIdx.x / C; row < rows; row += ncl) {
+    const int h = row % H;
+    const float d = D[h];
+    float uv[Cf::PI][C / 2];
+    cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int s, int q, int t) {
+      const float v = t < L ? u[(size_t)row * L + t] : 0.f;
+      uv[s][q] = v;
+      return make_float2(v, 0.f);
+    });
+    cl.sync();
+    run_passes<LOGM, false, 0, NP - 2, T>(buf, twf, lt);
+    {
+      const float2* twl = twf + plan_tw_off(LOGM, NP - 1, false);
+      float2 a[PERL][RB];
+#pragma unroll
+      for (int s = 0; s < PERL; ++s) {
+        const int i = lt + s * T;
+        float2 kv[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) kv[q] = K2[(size_t)h * n + (size_t)c * m + i + q * NBL];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) a[s][q] = buf[pad(i + q * NBL)];
+        apply_twiddles<RB>(a[s], twl[i]);
+        dft<RB, false>(a[s]);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], kv[q]);
+        dft<RB, true>(a[s]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < PERL; ++s) {
+        const int i = lt + s * T;
+#pragma unroll
+        for (int q = 0; q < RB; ++q) buf[pad(i * RB + q)] = a[s][q];
+      }
+      __syncthreads();
+    }
+    run_passes<LOGM, true, 1, NP - 1, T>(buf, twi, lt);
+    cl.sync();
+    cross_inverse<LOGN, true>(cl, buf, tw1, c, lt, [&](int s, int q, int t, float2 v) {
+      if (t < L)
+        y[(size_t)row * L + t] =
+            zero ? make_float2(0.f, 0.f) : make_float2(fmaf(v.x, sc, d * uv[s][q]), v.y * sc);
+    });
+    cl.sync();
+  }
+}
+
+}  // namespace s4dev
+
+namespace s4impl {
+using namespace s4dev;
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_clustered(void (*kern)(KArgs...), int C, int threads, size_t smem,
+                                    int rows, const char* name, cudaStream_t s, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(C * rows);
+  int maxc = 0;
+  if (cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg) != cudaSuccess || maxc < 1) {
+    (void)cudaGetLastError();
+    maxc = 1;
+  }
+  const int ncl = rows < maxc ? rows : maxc;
+  cfg.gridDim = dim3(C * ncl);
+  TimedLaunch tl(name, s);
+  e = cudaLaunchKernelEx(&cfg, kern, args...);
+  return e;
+}
+
+template <int LOGN>
+static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, const unsigned* st,
+                           cudaStream_t s) {
+  using Cf = ClusterCfg<LOGN>;
+  const size_t smem = sizeof(float2) * (Cf::TWI + Cf::MI + (size_t)Cf::PADM);
+  return launch_clustered(ifft_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "ifft", s, Khat, K, H, L, st);
+}
+
+template <int LOGN>
+static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsigned* st, cudaStream_t s) {
+  using Cf = ClusterCfg<LOGN>;
+  const size_t smem = sizeof(float2) * (Cf::TWF + Cf::MI + (size_t)Cf::PADM);
+  return launch_clustered(spectrum_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "spectrum", s, K, K2,
+                          H, L, st);
+}
+
+template <int LOGN>
+static cudaError_t conv_cl(const float* u, const float2* K2, const float* D, float2* y, int rows, int H,
+                           int L, const unsigned* st, cudaStream_t s) {
+  using Cf = ClusterCfg<LOGN>;
+  const size_t smem = sizeof(float2) * (Cf::TWF + Cf::TWI + Cf::MI + (size_t)Cf::PADM);
+  return launch_clustered(conv_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, rows, "conv", s, u, K2, D, y,
+                          rows, H, L, st);
+}
+
+cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
+                                const unsigned* st, cudaStream_t s) {
+  switch (logM) {
+    case 15: return ifft_cl<15>(Khat, K, H, L, st, s);
+    case 16: return ifft_cl<16>(Khat, K, H, L, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
+                                    unsigned* st, cudaStream_t s) {
+  switch (logn) {
+    case 15: return spectrum_cl<15>(K, K2, H, L, st, s);
+    case 16: return spectrum_cl<16>(K, K2, H, L, st, s);
+    case 17: return spectrum_cl<17>(K, K2, H, L, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, const float* D,
+                                float2* y, int rows, int H, int L, const unsigned* st,
+                                cudaStream_t s) {
+  switch (logn) {
+    case 15: return conv_cl<15>(u, K2, D, y, rows, H, L, st, s);
+    case 16: return conv_cl<16>(u, K2, D, y, rows, H, L, st, s);
+    case 17: return conv_cl<17>(u, K2, D, y, rows, H, L, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace s4impl

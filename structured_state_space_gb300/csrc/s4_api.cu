@@ -1,0 +1,272 @@
+// C ABI of libs4 (declared in include/s4.h): argument checks, workspace
+// layout, the order of kernel launches on the caller's stream, the device
+// status word and optional launch timing.
+#include <limits.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "s4.h"
+#include "s4_dev.cuh"
+#include "s4_internal.h"
+
+namespace {
+
+constexpr int kMaxL = 65536;
+constexpr int kMaxN = 65536;
+constexpr int kMaxR = 4;
+
+int ilog2_ceil(int v) {
+  int lg = 0;
+  while ((1 << lg) < v) ++lg;
+  return lg;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Workspace: [status word | tan table (M) | root values (H M) | kernel spectra (H 2M)]
+struct Layout {
+  size_t tau, khat, k2, total;
+};
+
+Layout layout_for(int H, int L) {
+  const size_t M = (size_t)1 << ilog2_ceil(L);
+  Layout l;
+  l.tau = 256;
+  l.khat = l.tau + round256(sizeof(float2) * M);
+  l.k2 = l.khat + round256(sizeof(float2) * M * (size_t)H);
+  l.total = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
+  return l;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool sizes_ok(int H, int N, int r, int L, int batch) {
+  if (H < 1 || N < 1 || N > kMaxN || r < 1 || r > kMaxR || L < 1 || L > kMaxL || batch < 1)
+    return false;
+  if ((long long)batch * H > INT_MAX) return false;
+  if ((long long)H * N > INT_MAX / kMaxR) return false;
+  return true;
+}
+
+s4_status check_ws(const void* ws, size_t ws_bytes, int H, int L) {
+  if (ws == nullptr || !aligned(ws, 256)) return S4_ERR_WORKSPACE;
+  if (ws_bytes < layout_for(H, L).total) return S4_ERR_WORKSPACE;
+  return S4_OK;
+}
+
+s4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? S4_OK : S4_ERR_CUDA; }
+
+s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
+                   const s4_c32* Ct, const float* dt, int H, int N, int r, int L, s4_c32* K,
+                   void* ws, cudaStream_t s) {
+  using namespace s4impl;
+  const int logM = ilog2_ceil(L);
+  const int M = 1 << logM;
+  const int logC = cluster_log(logM);
+  const Layout lay = layout_for(H, L);
+  char* w = static_cast<char*>(ws);
+  unsigned* st = reinterpret_cast<unsigned*>(w);
+  float2* tau = reinterpret_cast<float2*>(w + lay.tau);
+  float2* khat = reinterpret_cast<float2*>(w + lay.khat);
+  cudaError_t e = launch_tau(tau, M, logC, s);
+  if (e == cudaSuccess)
+    e = launch_cauchy(reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
+                      reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
+                      reinterpret_cast<const float2*>(Ct), dt, tau, khat, H, N, r, M, logC, st, s);
+  if (e == cudaSuccess)
+    e = logM <= kMaxLogRowCta
+            ? launch_ifft_rows(logM, khat, reinterpret_cast<float2*>(K), H, L, st, s)
+            : launch_ifft_cluster(logM, khat, reinterpret_cast<float2*>(K), H, L, st, s);
+  return cuda_status(e);
+}
+
+s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
+                    s4_c32* y, void* ws, cudaStream_t s) {
+  using namespace s4impl;
+  const int logn = ilog2_ceil(L) + 1;
+  const Layout lay = layout_for(H, L);
+  char* w = static_cast<char*>(ws);
+  unsigned* st = reinterpret_cast<unsigned*>(w);
+  float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
+  const float2* Kf = reinterpret_cast<const float2*>(K);
+  float2* yf = reinterpret_cast<float2*>(y);
+  const int rows = batch * H;
+  cudaError_t e;
+  if (logn <= kMaxLogRowCta) {
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s);
+    if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, rows, H, L, st, s);
+  } else {
+    e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
+    if (e == cudaSuccess) e = launch_conv_cluster(logn, u, k2, D, yf, rows, H, L, st, s);
+  }
+  return cuda_status(e);
+}
+
+// ---- launch timing --------------------------------------------------------------
+struct TimingRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_tmu;
+bool g_timing = false;
+std::vector<TimingRec> g_recs;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_pool;
+size_t g_used = 0;
+
+}  // namespace
+
+namespace s4impl {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) v = 148;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+TimedLaunch::TimedLaunch(const char* name, cudaStream_t s) : slot_(-1), s_(s) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (!g_timing) return;
+  if (g_used == g_pool.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return;
+    }
+    g_pool.push_back({a, b});
+  }
+  const auto pr = g_pool[g_used];
+  slot_ = (int)g_recs.size();
+  g_recs.push_back({name, pr.first, pr.second});
+  ++g_used;
+  cudaEventRecord(pr.first, s);
+}
+
+TimedLaunch::~TimedLaunch() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  cudaEventRecord(g_recs[slot_].stop, s_);
+}
+
+}  // namespace s4impl
+
+extern "C" {
+
+size_t s4_workspace_bytes(int H, int N, int r, int L, int batch) {
+  if (!sizes_ok(H, N, r, L, batch)) return 0;
+  return layout_for(H, L).total;
+}
+
+s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
+                        const s4_c32* Ctilde, const float* dt, int H, int N, int r, int L,
+                        s4_c32* K, void* ws, size_t ws_bytes, void* stream) {
+  if (!Lambda || !P || !Q || !B || !Ctilde || !dt || !K) return S4_ERR_INVALID_ARG;
+  if (!sizes_ok(H, N, r, L, 1)) return S4_ERR_INVALID_ARG;
+  if (!aligned(Lambda, 8) || !aligned(P, 8) || !aligned(Q, 8) || !aligned(B, 8) ||
+      !aligned(Ctilde, 8) || !aligned(dt, 4) || !aligned(K, 16))
+    return S4_ERR_INVALID_ARG;
+  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  if (wst != S4_OK) return wst;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);
+}
+
+s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
+                      s4_c32* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!u || !K || !D || !y) return S4_ERR_INVALID_ARG;
+  if (!sizes_ok(H, 1, 1, L, batch)) return S4_ERR_INVALID_ARG;
+  if (!aligned(u, 16) || !aligned(K, 16) || !aligned(D, 4) || !aligned(y, 16))
+    return S4_ERR_INVALID_ARG;
+  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  if (wst != S4_OK) return wst;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  return conv_impl(u, K, D, batch, H, L, y, ws, s);
+}
+
+s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
+                       const s4_c32* Ctilde, const float* dt, const float* D, const float* u,
+                       int batch, int H, int N, int r, int L, s4_c32* K, s4_c32* y, void* ws,
+                       size_t ws_bytes, void* stream) {
+  if (!Lambda || !P || !Q || !B || !Ctilde || !dt || !D || !u || !K || !y)
+    return S4_ERR_INVALID_ARG;
+  if (!sizes_ok(H, N, r, L, batch)) return S4_ERR_INVALID_ARG;
+  if (!aligned(Lambda, 8) || !aligned(P, 8) || !aligned(Q, 8) || !aligned(B, 8) ||
+      !aligned(Ctilde, 8) || !aligned(dt, 4) || !aligned(D, 4) || !aligned(u, 16) ||
+      !aligned(K, 16) || !aligned(y, 16))
+    return S4_ERR_INVALID_ARG;
+  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  if (wst != S4_OK) return wst;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);
+  if (g != S4_OK) return g;
+  return conv_impl(u, K, D, batch, H, L, y, ws, s);
+}
+
+s4_status s4_get_status(const void* ws, void* stream) {
+  if (ws == nullptr) return S4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return S4_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return S4_ERR_CUDA;
+  if (word & s4dev::ST_BAD_STEP) return S4_ERR_INVALID_STEP;
+  if (word & s4dev::ST_RES_DIAG) return S4_ERR_RESONANT_DIAGONAL;
+  if (word & s4dev::ST_RES_CORR) return S4_ERR_RESONANT_CORRECTION;
+  if (word & s4dev::ST_NONFINITE) return S4_ERR_NONFINITE;
+  return S4_OK;
+}
+
+const char* s4_status_str(s4_status st) {
+  switch (st) {
+    case S4_OK: return "ok";
+    case S4_ERR_INVALID_ARG: return "invalid argument";
+    case S4_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case S4_ERR_RESONANT_DIAGONAL: return "resonant-diagonal";
+    case S4_ERR_RESONANT_CORRECTION: return "resonant-correction";
+    case S4_ERR_NONFINITE: return "non-finite value";
+    case S4_ERR_INVALID_STEP: return "step size not positive and finite";
+    case S4_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+void s4_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  g_timing = on != 0;
+}
+
+void s4_timing_reset(void) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  g_recs.clear();
+  g_used = 0;
+}
+
+int s4_timing_read(const char* name, int* launches, double* total_ms) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  int n = 0;
+  double ms = 0.0;
+  for (const TimingRec& r : g_recs) {
+    if (name && strcmp(name, r.name) != 0) continue;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) return -1;
+    ms += t;
+    ++n;
+  }
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = ms;
+  return 0;
+}
+
+}  // extern "C"

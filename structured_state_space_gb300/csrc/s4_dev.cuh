@@ -1,0 +1,195 @@
+// Device building blocks shared by the libs4 kernels: complex helpers,
+// device status bits, register-resident small DFTs and Stockham FFT passes
+// over a row held in (padded) shared memory.
+//
+// Transform conventions follow "Recurrent, LSTM, and structured state-space
+// models", section "Radix-two discrete Fourier transform": forward
+// ahat_k = sum_j a_j w^{jk} with w = exp(-2 pi i/M); the inverse uses conj(w)
+// and the 1/M factor, which the callers apply.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace s4dev {
+
+// ---- device status bits (kept in the first word of the workspace) ----------
+constexpr unsigned ST_RES_DIAG = 1u;   // s(z_k) - lambda_j == 0 (fp32)
+constexpr unsigned ST_RES_CORR = 2u;   // W(z_k) singular
+constexpr unsigned ST_NONFINITE = 4u;  // non-finite root value or spectrum
+constexpr unsigned ST_BAD_STEP = 8u;   // Delta <= 0 or not finite
+
+// ---- complex helpers ----------------------------------------------------------
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+  return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+__device__ __forceinline__ float2 cscale(float2 a, float s) { return make_float2(a.x * s, a.y * s); }
+__device__ __forceinline__ bool cfinite(float2 a) { return isfinite(a.x) && isfinite(a.y); }
+
+// Approximate reciprocal (PTX rcp.approx.ftz.f32, relative error ~2^-23).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// ---- padded shared-memory index: one spare slot per 16 entries ------------------
+// Keeps the Stockham read (stride n/R) and write (stride p) patterns free of
+// shared-memory bank conflicts for the radix plans used here.
+__device__ __forceinline__ int pad(int w) { return w + (w >> 4); }
+__host__ __device__ constexpr int padded_len(int n) { return n + (n >> 4) + 1; }
+
+// ---- cos/sin of 2 pi e / 16 ----------------------------------------------------------
+__host__ __device__ constexpr float cos16(int e) {
+  constexpr float c1 = 0.92387953251128674f, s1 = 0.38268343236508978f, h = 0.70710678118654752f;
+  e &= 15;
+  return e == 0 ? 1.f : e == 1 ? c1 : e == 2 ? h : e == 3 ? s1 : e == 4 ? 0.f : e == 5 ? -s1
+       : e == 6 ? -h : e == 7 ? -c1 : e == 8 ? -1.f : e == 9 ? -c1 : e == 10 ? -h : e == 11 ? -s1
+       : e == 12 ? 0.f : e == 13 ? s1 : e == 14 ? h : c1;
+}
+__host__ __device__ constexpr float sin16(int e) { return cos16(e - 4); }  // sin x = cos(x - pi/2)
+
+// a <- a + w b, b <- a - w b, with w = exp(-+ 2 pi i e/16) (forward / inverse).
+template <bool INV>
+__device__ __forceinline__ void bfly(float2& a, float2& b, int e) {
+  if (e == 0) {
+    const float2 t = b;
+    b = csub(a, t);
+    a = cadd(a, t);
+  } else if (e == 4) {  // w = -i (forward) or +i (inverse)
+    const float2 t = INV ? make_float2(-b.y, b.x) : make_float2(b.y, -b.x);
+    b = csub(a, t);
+    a = cadd(a, t);
+  } else {
+    const float c = cos16(e);
+    const float s = INV ? sin16(e) : -sin16(e);  // w = c + i s
+    const float yx = fmaf(b.x, c, fmaf(-b.y, s, a.x));
+    const float yy = fmaf(b.x, s, fmaf(b.y, c, a.y));
+    b = make_float2(fmaf(2.f, a.x, -yx), fmaf(2.f, a.y, -yy));
+    a = make_float2(yx, yy);
+  }
+}
+
+// Same butterfly when only a + w b is wanted.
+template <bool INV>
+__device__ __forceinline__ void bfly_top(float2& a, const float2 b, int e) {
+  if (e == 0) {
+    a = cadd(a, b);
+  } else if (e == 4) {
+    a = cadd(a, INV ? make_float2(-b.y, b.x) : make_float2(b.y, -b.x));
+  } else {
+    const float c = cos16(e);
+    const float s = INV ? sin16(e) : -sin16(e);
+    a = make_float2(fmaf(b.x, c, fmaf(-b.y, s, a.x)), fmaf(b.x, s, fmaf(b.y, c, a.y)));
+  }
+}
+
+// In-register DFT of length R (1, 2, 4, 8, 16) by the even/odd split of the
+// radix-two recursion.  HALFZERO: inputs R/2..R-1 are known zero.  HALFOUT:
+// only outputs 0..R/2-1 are needed.
+template <int R, bool INV, bool HALFZERO = false, bool HALFOUT = false>
+__device__ __forceinline__ void dft(float2* a) {
+  if constexpr (R == 1) {
+    return;
+  } else if constexpr (R == 2) {
+    if constexpr (HALFZERO) {
+      a[1] = a[0];
+    } else if constexpr (HALFOUT) {
+      a[0] = cadd(a[0], a[1]);
+    } else {
+      bfly<INV>(a[0], a[1], 0);
+    }
+  } else {
+    float2 ev[R / 2], od[R / 2];
+#pragma unroll
+    for (int j = 0; j < R / 2; ++j) {
+      ev[j] = a[2 * j];
+      od[j] = a[2 * j + 1];
+    }
+    dft<R / 2, INV, HALFZERO>(ev);
+    dft<R / 2, INV, HALFZERO>(od);
+#pragma unroll
+    for (int k = 0; k < R / 2; ++k) {
+      if constexpr (HALFOUT) {
+        bfly_top<INV>(ev[k], od[k], (16 / R) * k);
+        a[k] = ev[k];
+      } else {
+        bfly<INV>(ev[k], od[k], (16 / R) * k);
+        a[k] = ev[k];
+        a[k + R / 2] = od[k];
+      }
+    }
+  }
+}
+
+__host__ __device__ constexpr int highbit(int q) {
+  int h = 1;
+  while (h * 2 <= q) h *= 2;
+  return h;
+}
+
+// a[q] *= w^q, q = 1..R-1 (w already conjugated for an inverse pass).
+template <int R>
+__device__ __forceinline__ void apply_twiddles(float2* a, float2 w) {
+  if constexpr (R > 1) {
+    float2 pw[R];
+    pw[1] = w;
+#pragma unroll
+    for (int q = 2; q < R; ++q) {
+      const int hb = highbit(q);
+      pw[q] = (hb == q) ? cmul(pw[q / 2], pw[q / 2]) : cmul(pw[hb], pw[q - hb]);
+    }
+#pragma unroll
+    for (int q = 1; q < R; ++q) a[q] = cmul(a[q], pw[q]);
+  }
+}
+
+// Twiddle base table of one Stockham pass: tw[k] = exp(-2 pi i k / (P R)), k < P.
+__device__ __forceinline__ void fill_twiddles(float2* tw, int P, int PR, int tid, int nthreads) {
+  for (int k = tid; k < P; k += nthreads) {
+    float s, c;
+    sincospif(2.0f * (float)k / (float)PR, &s, &c);
+    tw[k] = make_float2(c, -s);
+  }
+}
+
+// One Stockham radix-R pass (Bainville's auto-sort form) over a row of N
+// points in padded shared memory.  P = product of the radices of the
+// earlier passes.  Butterfly i reads x[i + q N/R], multiplies by
+// w_{PR}^{q (i mod P)}, transforms, and writes to (i - k) R + k + q P.
+// `lt` is this thread's index in the row's T-thread group.
+template <int N, int R, int P, bool INV, int T>
+__device__ __forceinline__ void pass_smem(float2* buf, const float2* tw, int lt) {
+  constexpr int NB = N / R;
+  constexpr int PER = (NB + T - 1) / T;
+  float2 a[PER][R];
+#pragma unroll
+  for (int s = 0; s < PER; ++s) {
+    const int i = lt + s * T;
+    if (NB % T == 0 || i < NB) {
+#pragma unroll
+      for (int q = 0; q < R; ++q) a[s][q] = buf[pad(i + q * NB)];
+      if constexpr (P > 1) {
+        float2 w = tw[i & (P - 1)];
+        if (INV) w.y = -w.y;
+        apply_twiddles<R>(a[s], w);
+      }
+      dft<R, INV>(a[s]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int s = 0; s < PER; ++s) {
+    const int i = lt + s * T;
+    if (NB % T == 0 || i < NB) {
+      const int k = i & (P - 1);
+      const int j0 = (i - k) * R + k;
+#pragma unroll
+      for (int q = 0; q < R; ++q) buf[pad(j0 + q * P)] = a[s][q];
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace s4dev

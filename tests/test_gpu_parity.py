@@ -1,0 +1,222 @@
+"""CUDA path vs the float64 oracle, element by element, on the same seeded inputs.
+
+Tolerances (fp32 arithmetic against float64): relative L2 error <= 1e-4 on K
+and on y, and max |y_gpu - y_ref| <= 1e-3 * max|y_ref|.  Large workloads are
+compared on sampled channels (full kernels) and sampled rows (full rows, or
+sampled output positions where the direct O(L^2) sum is too slow).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle.s4_oracle as O  # noqa: E402
+import structured_state_space_gb300 as s4  # noqa: E402
+from structured_state_space_gb300 import build as s4build  # noqa: E402
+from structured_state_space_gb300 import workloads as W  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+REL_K = 1e-4
+REL_Y = 1e-4
+MAXABS_Y = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    s4build.build()
+    return s4.load()
+
+
+def dev(params, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt", "D")):
+    return {k: torch.from_numpy(np.ascontiguousarray(params[k])).cuda() for k in keys}
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def check_y(y_gpu, y_ref, what):
+    e = rel_l2(y_gpu, y_ref)
+    m = float(np.max(np.abs(y_gpu - y_ref)))
+    scale = float(np.max(np.abs(y_ref)))
+    assert e <= REL_Y, f"{what}: rel-L2 {e:.3e}"
+    assert m <= MAXABS_Y * scale, f"{what}: max abs {m:.3e} vs {scale:.3e}"
+    return e
+
+
+def run_layer(p, u):
+    d = dev(p)
+    ut = torch.from_numpy(u).cuda()
+    K, y = s4.s4_layer_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], d["D"], ut)
+    torch.cuda.synchronize()
+    return K.cpu().numpy(), y.cpu().numpy()
+
+
+# sampled channels per workload (all of them for the small ones)
+def _channels(w, count):
+    if w.H <= count:
+        return list(range(w.H))
+    rng = np.random.default_rng(77)
+    extra = rng.choice(np.arange(2, w.H - 2), size=count - 4, replace=False)
+    return sorted(set([0, 1, w.H // 2, w.H - 1] + [int(x) for x in extra]))
+
+
+@pytest.mark.parametrize("wi,nch,full_rows", [(0, 2, True), (1, 256, True), (2, 16, True), (3, 6, True), (4, 4, False)])
+def test_layer_matches_oracle(wi, nch, full_rows):
+    w = W.WORKLOADS[wi]
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+    K_gpu, y_gpu = run_layer(p, u)
+    chans = _channels(w, nch)
+    K_ref = O.s4_kernel_channels(p, w.L, chans)
+    assert rel_l2(K_gpu[chans], K_ref) <= REL_K, rel_l2(K_gpu[chans], K_ref)
+    ys_gpu, ys_ref = [], []
+    rng = np.random.default_rng(5)
+    for ci, h in enumerate(chans):
+        for b in range(w.batch):
+            if full_rows:
+                ys_ref.append(O.causal_conv(K_ref[ci], u[b, h], p["D"][h]))
+                ys_gpu.append(y_gpu[b, h])
+            else:
+                ts = sorted(set([0, 1, 2, w.L - 1, w.L // 2] + list(rng.integers(0, w.L, 60))))
+                ys_ref.append(O.causal_conv_at(K_ref[ci], u[b, h], p["D"][h], ts))
+                ys_gpu.append(y_gpu[b, h, ts])
+    check_y(np.concatenate(ys_gpu), np.concatenate(ys_ref), w.name)
+    assert np.all(np.isfinite(y_gpu))
+
+
+@pytest.mark.parametrize("N,r,H,L,batch", [
+    (4, 1, 3, 1, 2), (4, 1, 3, 2, 2), (5, 2, 2, 3, 1), (6, 1, 5, 16, 3), (8, 2, 4, 100, 2),
+    (7, 3, 2, 33, 2), (4, 4, 2, 64, 1), (300, 1, 2, 200, 2), (16, 1, 9, 1000, 3),
+    (16, 2, 3, 5000, 2), (12, 1, 2, 16384, 1), (8, 1, 2, 20000, 2), (8, 2, 2, 40000, 1),
+])
+def test_edge_sizes(N, r, H, L, batch):
+    w = W.custom(N, r, H, L, batch, seed=N * 1000 + L)
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+    K_gpu, y_gpu = run_layer(p, u)
+    K_ref = O.s4_kernel_channels(p, L)
+    assert rel_l2(K_gpu, K_ref) <= REL_K, rel_l2(K_gpu, K_ref)
+    if L <= 20000:
+        y_ref = np.stack([[O.causal_conv(K_ref[h], u[b, h], p["D"][h]) for h in range(H)] for b in range(batch)])
+        check_y(y_gpu, y_ref, f"edge N{N} r{r} L{L}")
+    else:
+        ts = [0, 1, L // 3, L // 2, L - 2, L - 1]
+        y_ref = np.array([[O.causal_conv_at(K_ref[h], u[b, h], p["D"][h], ts) for h in range(H)] for b in range(batch)])
+        check_y(y_gpu[:, :, ts], y_ref, f"edge N{N} r{r} L{L}")
+
+
+def test_kernel_gen_and_conv_separately():
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+    d = dev(p)
+    K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L)
+    chans = [0, 7, 200]
+    K_ref = O.s4_kernel_channels(p, w.L, chans)
+    assert rel_l2(K.cpu().numpy()[chans], K_ref) <= REL_K
+    # the convolution alone, fed a kernel given in complex64
+    Kin = (np.random.default_rng(3).standard_normal((w.H, w.L)) * 0.05 + 1j * 0.02).astype(np.complex64)
+    y = s4.s4_conv_fwd(torch.from_numpy(u).cuda(), torch.from_numpy(Kin).cuda(), d["D"]).cpu().numpy()
+    rows = [(0, 0), (3, 17), (15, 255)]
+    y_ref = np.stack([O.causal_conv(Kin[h], u[b, h], p["D"][h]) for b, h in rows])
+    check_y(np.stack([y[b, h] for b, h in rows]), y_ref, "conv only")
+
+
+def test_scalar_example_conv_gives_prefix_sums():
+    # Page example: K = (1, ..., 1), D = 0  =>  y_t = sum_{s<=t} u_s.
+    L = 8
+    g = W.scalar_example(L, u=[3, -1, 4, 1, -5, 9, 2, -6])
+    K = torch.ones((1, L), dtype=torch.complex64, device="cuda")
+    y = s4.s4_conv_fwd(torch.from_numpy(g["u"]).cuda(), K, torch.zeros(1, device="cuda")).cpu().numpy()
+    np.testing.assert_allclose(y[0, 0].real, [3, 2, 6, 7, 2, 11, 13, 7], atol=1e-5)
+    np.testing.assert_allclose(y[0, 0].imag, 0, atol=1e-5)
+
+
+def test_scalar_example_kernel_gen_is_resonant():
+    # Through the filter, A = 0 resonates at z = 1 (s(1) = 0 = lambda).
+    g = W.scalar_example(8)
+    d = {k: torch.from_numpy(g[k]).cuda() for k in ["Lambda", "P", "Q", "B", "dt"]}
+    ws = s4.workspace(1, 1, 1, 8, 1)
+    K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["B"], d["dt"], 8, ws=ws)
+    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_RESONANT_DIAGONAL"]
+    assert torch.count_nonzero(K).item() == 0
+
+
+def test_resonant_correction_status():
+    # lambda = -1/2, p = 1/2, q = -1: W(1) = 1 + conj(q) p / (0 - lambda) = 0 exactly.
+    c = lambda v: torch.tensor(v, dtype=torch.complex64, device="cuda")
+    ws = s4.workspace(1, 1, 1, 4, 1)
+    K = s4.s4_kernel_gen(c([[-0.5]]), c([[[0.5]]]), c([[[-1.0]]]), c([[1.0]]), c([[1.0]]),
+                         torch.tensor([0.3], device="cuda"), 4, ws=ws)
+    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_RESONANT_CORRECTION"]
+    assert torch.count_nonzero(K).item() == 0
+
+
+@pytest.mark.parametrize("bad", [0.0, -1e-3, float("nan"), float("inf")])
+def test_invalid_step_status(bad):
+    w = W.WORKLOADS[0]
+    p = W.make_params(w)
+    p["dt"][1] = bad
+    d = dev(p)
+    ws = s4.workspace(w.H, w.N, w.r, w.L, 1)
+    K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=ws)
+    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_INVALID_STEP"]
+    assert torch.count_nonzero(K).item() == 0
+
+
+def test_status_clears_on_next_call():
+    w = W.WORKLOADS[0]
+    p = W.make_params(w)
+    d = dev(p)
+    ws = s4.workspace(w.H, w.N, w.r, w.L, 1)
+    bad = d["dt"].clone()
+    bad[0] = -1.0
+    s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], bad, w.L, ws=ws)
+    assert s4.s4_get_status(ws) != 0
+    s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=ws)
+    assert s4.s4_get_status(ws) == 0
+
+
+def test_host_errors_raise():
+    w = W.WORKLOADS[0]
+    p = W.make_params(w)
+    d = dev(p)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(s4.S4Error) as e:
+        s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=small)
+    assert e.value.code == 2
+    with pytest.raises(TypeError):
+        s4.s4_kernel_gen(d["Lambda"].to(torch.complex128), d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L)
+
+
+def test_deterministic():
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+    K1, y1 = run_layer(p, u)
+    K2, y2 = run_layer(p, u)
+    assert np.array_equal(K1, K2) and np.array_equal(y1, y2)
+
+
+def test_timing_hooks_count_launches():
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+    d = dev(p)
+    ut = torch.from_numpy(u).cuda()
+    s4.timing.reset()
+    s4.timing.enable(True)
+    try:
+        for _ in range(3):
+            s4.s4_layer_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], d["D"], ut)
+        torch.cuda.synchronize()
+        for name in ["tau", "cauchy", "ifft", "spectrum", "conv"]:
+            n, ms = s4.timing.read(name)
+            assert n == 3 and ms > 0.0, (name, n, ms)
+    finally:
+        s4.timing.enable(False)
+        s4.timing.reset()
