@@ -23,18 +23,24 @@
 
 namespace s4dev {
 
+// One thread per root k <= M/2; tan(pi (M - k)/M) = -tan(pi k/M) fills the
+// other half.  Small blocks spread the fp64 work over all SMs.
 __global__ void tau_kernel(float2* __restrict__ tau, int M, int logC) {
-  const int pos = blockIdx.x * blockDim.x + threadIdx.x;
-  if (pos >= M) return;
-  const int Mc = M >> logC;
-  const int k = (pos % Mc) * (1 << logC) + pos / Mc;
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k > M / 2) return;
+  const int Mc = M >> logC, Cm = (1 << logC) - 1;
   double t = 0.0;
   if (2 * k != M) {
     const double x = (double)k / (double)M;
     t = sinpi(x) / cospi(x);
   }
   const float hi = (float)t;
-  tau[pos] = make_float2(hi, (float)(t - (double)hi));
+  const float lo = (float)(t - (double)hi);
+  tau[(k & Cm) * Mc + (k >> logC)] = make_float2(hi, lo);
+  if (k > 0 && 2 * k < M) {
+    const int k2 = M - k;
+    tau[(k2 & Cm) * Mc + (k2 >> logC)] = make_float2(-hi, -lo);
+  }
 }
 
 __device__ __forceinline__ float2 conj_mul(float2 a, float2 b) {  // conj(a) * b
@@ -289,7 +295,8 @@ using namespace s4dev;
 
 cudaError_t launch_tau(float2* tau, int M, int logC, cudaStream_t s) {
   TimedLaunch tl("tau", s);
-  tau_kernel<<<(M + 255) / 256, 256, 0, s>>>(tau, M, logC);
+  const int roots = M / 2 + 1;
+  tau_kernel<<<(roots + 31) / 32, 32, 0, s>>>(tau, M, logC);
   return cudaGetLastError();
 }
 
