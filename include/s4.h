@@ -18,7 +18,8 @@
  *    torch.complex64 / std::complex<float>).  All arrays are dense row-major.
  *  - Every array pointer is a DEVICE pointer owned by the caller.  The library
  *    allocates no device memory and keeps no state between calls other than
- *    per-device kernel attributes.  `ws` is caller-owned device scratch of at
+ *    per-device kernel attributes (and the fixed scratch array of
+ *    s4_conv_fwd_noalloc).  `ws` is caller-owned device scratch of at
  *    least s4_workspace_bytes(...) bytes, 256-byte aligned.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *    enqueued asynchronously on it; no entry point synchronises the host
@@ -113,6 +114,32 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
                        int batch, int H, int N, int r, int L,
                        s4_c32* K, s4_c32* y,
                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * s4_conv_fwd_noalloc -- s4_conv_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a service entry point of the library.
+ * Some callers cannot call cudaMalloc: a host program that owns all device
+ * memory through its own pool and forbids allocations by the libraries it
+ * loads, or a latency-critical loop where an allocation (which can
+ * synchronise the device) is not acceptable.  They cannot provide `ws`, so
+ * this variant keeps its scratch (the status word and the kernel spectrum)
+ * in a fixed array of S4_NOALLOC_SCRATCH_BYTES compiled into the library;
+ * every device that loads the library holds that array until the process exits.
+ *   Arguments, layouts and results as for s4_conv_fwd; no ws, no ws_bytes.
+ *   Limit: 256 + 16 * H * M bytes of scratch (M = least power of two >= L)
+ *   must fit S4_NOALLOC_SCRATCH_BYTES (8 MiB; e.g. H * M <= 524272), else
+ *   S4_ERR_WORKSPACE is returned before anything is enqueued.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   All calls share the one array: calls that can overlap on the GPU (work
+ *   on streams not ordered with each other) race and must not be issued.
+ *   A non-finite kernel spectrum writes y as zeros; no status word is exposed.
+ *   Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
+ */
+#define S4_NOALLOC_SCRATCH_BYTES (8u << 20)
+s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const float* D,
+                              int batch, int H, int L, s4_c32* y, void* stream);
 
 /* Synchronises `stream`, then returns the device-detected status recorded in
  * `ws` by the last entry point that used it (S4_OK if none), or

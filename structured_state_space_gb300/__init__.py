@@ -35,6 +35,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
+    "s4_conv_fwd_noalloc",
 ]
 
 
