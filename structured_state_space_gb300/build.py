@@ -21,8 +21,9 @@ LIB = os.path.join(LIBDIR, "libs4.so")
 SOURCES = ["s4_api.cu", "cauchy.cu", "fft_rows.cu", "fft_cluster.cu", "s4_noalloc.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+GENDIR = os.path.join(OBJDIR, "gen")
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-         "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+         "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, "-I", GENDIR]
 
 
 def nvcc() -> str:
@@ -42,11 +43,16 @@ def _stale(extra_deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if needed) and return the path of libs4.so."""
-    deps = [os.path.join(INCLUDE, "s4.h"), os.path.abspath(__file__)]
+    deps = [os.path.join(INCLUDE, "s4.h"), os.path.abspath(__file__),
+            os.path.join(PKG, "gen_twiddles.py")]
     if not force and not _stale(deps):
         return LIB
     os.makedirs(LIBDIR, exist_ok=True)
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(GENDIR, exist_ok=True)
+    sys.path.insert(0, PKG)
+    import gen_twiddles
+    gen_twiddles.generate(os.path.join(GENDIR, "s4_twiddles.cuh"))
+    gen_twiddles.generate_tan(os.path.join(GENDIR, "s4_tan.cuh"))
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 

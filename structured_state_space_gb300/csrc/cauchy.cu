@@ -12,36 +12,17 @@
 // value (Delta/2) C~^* B.  Statuses: an fp32 denominator |s - lambda_j|^2 equal
 // to zero is 'resonant-diagonal'; an exactly singular W is 'resonant-correction'.
 //
-// Arithmetic: s is carried as an fp32 (hi, lo) pair (tan(pi k/M) from an fp64
-// table, a = 2/Delta split exactly), so that the difference s - lambda_j near a
-// resonance keeps full fp32 relative accuracy.  Each pole then costs one
+// Arithmetic: s is carried as an fp32 (hi, lo) pair (tan(pi k/M) from a table
+// computed in float64 at build time, a = 2/Delta split exactly), so that the
+// difference s - lambda_j near a resonance keeps full fp32 relative accuracy.  Each pole then costs one
 // reciprocal and 4 (r+1)^2 FMAs per root.
 #include <float.h>
 
 #include "s4_dev.cuh"
 #include "s4_internal.h"
+#include "s4_tan.cuh"
 
 namespace s4dev {
-
-// One thread per root k <= M/2; tan(pi (M - k)/M) = -tan(pi k/M) fills the
-// other half.  Small blocks spread the fp64 work over all SMs.
-__global__ void tau_kernel(float2* __restrict__ tau, int M, int logC) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k > M / 2) return;
-  const int Mc = M >> logC, Cm = (1 << logC) - 1;
-  double t = 0.0;
-  if (2 * k != M) {
-    const double x = (double)k / (double)M;
-    t = sinpi(x) / cospi(x);
-  }
-  const float hi = (float)t;
-  const float lo = (float)(t - (double)hi);
-  tau[(k & Cm) * Mc + (k >> logC)] = make_float2(hi, lo);
-  if (k > 0 && 2 * k < M) {
-    const int k2 = M - k;
-    tau[(k2 & Cm) * Mc + (k2 >> logC)] = make_float2(-hi, -lo);
-  }
-}
 
 __device__ __forceinline__ float2 conj_mul(float2 a, float2 b) {  // conj(a) * b
   return make_float2(fmaf(a.x, b.x, a.y * b.y), fmaf(a.x, b.y, -a.y * b.x));
@@ -114,14 +95,14 @@ template <int RANK, int RPT, int T>
 __global__ void __launch_bounds__(T) cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
-    const float2* __restrict__ tau, float2* __restrict__ Khat, int N, int M, int logC,
-    unsigned* __restrict__ status) {
+    float2* __restrict__ Khat, int N, int logM, int logC, unsigned* __restrict__ status) {
   using Lay = CauchyLayout<RANK>;
   constexpr int NW = Lay::NW, PS = Lay::PS, JT = 128;
   __shared__ __align__(16) float par[JT * PS];
   __shared__ float2 red[T / 32 + 1];
 
   const int h = blockIdx.x;
+  const int M = 1 << logM;
   const float delta = dt[h];
   const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
   const int Mc = M >> logC;
@@ -137,7 +118,7 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
     pos[rr] = (blockIdx.y * RPT + rr) * T + threadIdx.x;
     const bool valid = pos[rr] < M;
     const int k = valid ? (pos[rr] % Mc) * (1 << logC) + pos[rr] / Mc : 0;
-    const float2 tt = valid ? tau[pos[rr]] : make_float2(0.f, 0.f);
+    const float2 tt = valid ? __ldg(g_tan + (k << (16 - logM))) : make_float2(0.f, 0.f);
     zm1[rr] = valid && M >= 2 && 2 * k == M;
     const float p = a_hi * tt.x;
     const float perr = fmaf(a_hi, tt.x, -p);
@@ -293,42 +274,43 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
 namespace s4impl {
 using namespace s4dev;
 
-cudaError_t launch_tau(float2* tau, int M, int logC, cudaStream_t s) {
-  TimedLaunch tl("tau", s);
-  const int roots = M / 2 + 1;
-  tau_kernel<<<(roots + 31) / 32, 32, 0, s>>>(tau, M, logC);
-  return cudaGetLastError();
-}
+#ifndef S4_CAUCHY_T
+#define S4_CAUCHY_T 128
+#endif
+#ifndef S4_CAUCHY_RPT1
+#define S4_CAUCHY_RPT1 2
+#endif
 
 template <int RANK, int RPT>
 static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
                                  const float2* B, const float2* Ct, const float* dt,
-                                 const float2* tau, float2* Khat, int H, int N, int M, int logC,
-                                 unsigned* status, cudaStream_t s) {
-  constexpr int T = 128;
+                                 float2* Khat, int H, int N, int M, int logC, unsigned* status,
+                                 cudaStream_t s) {
+  constexpr int T = S4_CAUCHY_T;
   const int tiles = (M + T * RPT - 1) / (T * RPT);
   dim3 grid(H, tiles);
   TimedLaunch tl("cauchy", s);
-  cauchy_kernel<RANK, RPT, T><<<grid, T, 0, s>>>(Lambda, P, Q, B, Ct, dt, tau, Khat, N, M, logC,
-                                                 status);
+  int logM = 0;
+  while ((1 << logM) < M) ++logM;
+  cauchy_kernel<RANK, RPT, T><<<grid, T, 0, s>>>(Lambda, P, Q, B, Ct, dt, Khat, N, logM, logC, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
-                          const float2* Ct, const float* dt, const float2* tau, float2* Khat, int H,
-                          int N, int r, int M, int logC, unsigned* status, cudaStream_t s) {
+                          const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
+                          int M, int logC, unsigned* status, cudaStream_t s) {
   // roots per thread: enough CTAs to fill the GPU for small M, more ILP for large M
   const bool small = (long long)H * M < 4LL * 128 * 4 * num_sms() * 8;
   switch (r) {
     case 1:
-      return small ? cauchy_launch<1, 2>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s)
-                   : cauchy_launch<1, 4>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
+                   : cauchy_launch<1, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     case 2:
-      return cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+      return cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     case 3:
-      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     case 4:
-      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, tau, Khat, H, N, M, logC, status, s);
+      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     default:
       return cudaErrorInvalidValue;
   }

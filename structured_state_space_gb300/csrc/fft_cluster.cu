@@ -11,8 +11,8 @@
 // Remote shared-memory traffic uses plain DSMEM loads and stores.
 #include <cooperative_groups.h>
 
+#include "s4_fft.cuh"
 #include "s4_internal.h"
-#include "s4_plan.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -28,8 +28,6 @@ struct ClusterCfg {
   static constexpr int NP = plan_npass(LOGM);
   static constexpr int MI = m / C;   // cross-step indices owned by one CTA
   static constexpr int PI = MI / T;  // ... per thread
-  static constexpr int TWF = plan_tw_size(LOGM, false);
-  static constexpr int TWI = plan_tw_size(LOGM, true);
   static constexpr int PADM = padded_len(m);
   static_assert(PI >= 1 && MI % T == 0, "cluster split");
 };
@@ -99,14 +97,15 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
+  using IXL = PassIdx<m, RB, m / RB>;
+  using TWL = PassTw<LOGM, NP - 1, false>;
   cg::cluster_group cl = cg::this_cluster();
   const int c = (int)cl.block_rank();
   extern __shared__ float2 smem[];
-  float2* twf = smem;
-  float2* tw1 = twf + Cf::TWF;
+  float2* tw1 = smem;
   float2* buf = tw1 + Cf::MI;
+  float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
-  fill_plan_twiddles<LOGM, false>(twf, lt, T);
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
   __syncthreads();
   cl.sync();
@@ -117,15 +116,15 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
       return t < L ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
     });
     cl.sync();
-    run_passes<LOGM, false, 0, NP - 2, T>(buf, twf, lt);
-    const float2* twl = twf + plan_tw_off(LOGM, NP - 1, false);
+    passes_rows<LOGM, false, 0, NP - 2, T, 1>(bufs, lt);
 #pragma unroll
     for (int s = 0; s < PERL; ++s) {
       const int i = lt + s * T;
-      float2 a[RB];
+      float2 a[RB], w[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) a[q] = buf[pad(i + q * NBL)];
-      apply_twiddles<RB>(a, twl[i]);
+      for (int q = 0; q < RB; ++q) a[q] = buf[IXL::rd(i, q)];
+      TWL::load(w, i);
+      TWL::apply(a, w);
       dft<RB, false>(a);
 #pragma unroll
       for (int q = 0; q < RB; ++q) {
@@ -147,14 +146,14 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
   constexpr int R0 = plan_radix(LOGM, 0, true), NB0 = m / R0, PER0 = NB0 / T;
+  using IX0 = PassIdx<m, R0, 1>;
   cg::cluster_group cl = cg::this_cluster();
   const int c = (int)cl.block_rank();
   extern __shared__ float2 smem[];
-  float2* twi = smem;
-  float2* tw1 = twi + Cf::TWI;
+  float2* tw1 = smem;
   float2* buf = tw1 + Cf::MI;
+  float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
-  fill_plan_twiddles<LOGM, true>(twi, lt, T);
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
   const bool zero = *((volatile const unsigned*)status) != 0u;
   __syncthreads();
@@ -170,10 +169,10 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
       for (int q = 0; q < R0; ++q) a[q] = Khat[(size_t)h * n + (size_t)c * m + i + q * NB0];
       dft<R0, true>(a);
 #pragma unroll
-      for (int q = 0; q < R0; ++q) buf[pad(i * R0 + q)] = a[q];
+      for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
     }
     __syncthreads();
-    run_passes<LOGM, true, 1, NP - 1, T>(buf, twi, lt);
+    passes_rows<LOGM, true, 1, NP - 1, T, 1>(bufs, lt);
     cl.sync();
     cross_inverse<LOGN, false>(cl, buf, tw1, c, lt, [&](int, int, int t, float2 v) {
       if (t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(v, sc);
@@ -190,16 +189,16 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
+  using IXL = PassIdx<m, RB, m / RB>;
+  using IXI0 = PassIdx<m, RB, 1>;
+  using TWL = PassTw<LOGM, NP - 1, false>;
   cg::cluster_group cl = cg::this_cluster();
   const int c = (int)cl.block_rank();
   extern __shared__ float2 smem[];
-  float2* twf = smem;
-  float2* twi = twf + Cf::TWF;
-  float2* tw1 = twi + Cf::TWI;
+  float2* tw1 = smem;
   float2* buf = tw1 + Cf::MI;
+  float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
-  fill_plan_twiddles<LOGM, false>(twf, lt, T);
-  fill_plan_twiddles<LOGM, true>(twi, lt, T);
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
   const bool zero = *((volatile const unsigned*)status) != 0u;
   __syncthreads();
@@ -216,9 +215,8 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
       return make_float2(v, 0.f);
     });
     cl.sync();
-    run_passes<LOGM, false, 0, NP - 2, T>(buf, twf, lt);
+    passes_rows<LOGM, false, 0, NP - 2, T, 1>(bufs, lt);
     {
-      const float2* twl = twf + plan_tw_off(LOGM, NP - 1, false);
       float2 a[PERL][RB];
 #pragma unroll
       for (int s = 0; s < PERL; ++s) {
@@ -226,9 +224,11 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
         float2 kv[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) kv[q] = K2[(size_t)h * n + (size_t)c * m + i + q * NBL];
+        float2 w[RB];
 #pragma unroll
-        for (int q = 0; q < RB; ++q) a[s][q] = buf[pad(i + q * NBL)];
-        apply_twiddles<RB>(a[s], twl[i]);
+        for (int q = 0; q < RB; ++q) a[s][q] = buf[IXL::rd(i, q)];
+        TWL::load(w, i);
+        TWL::apply(a[s], w);
         dft<RB, false>(a[s]);
 #pragma unroll
         for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], kv[q]);
@@ -239,11 +239,11 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
       for (int s = 0; s < PERL; ++s) {
         const int i = lt + s * T;
 #pragma unroll
-        for (int q = 0; q < RB; ++q) buf[pad(i * RB + q)] = a[s][q];
+        for (int q = 0; q < RB; ++q) buf[IXI0::wr(i, q)] = a[s][q];
       }
       __syncthreads();
     }
-    run_passes<LOGM, true, 1, NP - 1, T>(buf, twi, lt);
+    passes_rows<LOGM, true, 1, NP - 1, T, 1>(bufs, lt);
     cl.sync();
     cross_inverse<LOGN, true>(cl, buf, tw1, c, lt, [&](int s, int q, int t, float2 v) {
       if (t < L)
@@ -292,14 +292,14 @@ template <int LOGN>
 static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, const unsigned* st,
                            cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
-  const size_t smem = sizeof(float2) * (Cf::TWI + Cf::MI + (size_t)Cf::PADM);
+  const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(ifft_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "ifft", s, Khat, K, H, L, st);
 }
 
 template <int LOGN>
 static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsigned* st, cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
-  const size_t smem = sizeof(float2) * (Cf::TWF + Cf::MI + (size_t)Cf::PADM);
+  const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(spectrum_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "spectrum", s, K, K2,
                           H, L, st);
 }
@@ -308,7 +308,7 @@ template <int LOGN>
 static cudaError_t conv_cl(const float* u, const float2* K2, const float* D, float2* y, int rows, int H,
                            int L, const unsigned* st, cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
-  const size_t smem = sizeof(float2) * (Cf::TWF + Cf::TWI + Cf::MI + (size_t)Cf::PADM);
+  const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(conv_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, rows, "conv", s, u, K2, D, y,
                           rows, H, L, st);
 }
@@ -325,6 +325,7 @@ cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, 
 cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
                                     unsigned* st, cudaStream_t s) {
   switch (logn) {
+    case 14: return spectrum_cl<14>(K, K2, H, L, st, s);
     case 15: return spectrum_cl<15>(K, K2, H, L, st, s);
     case 16: return spectrum_cl<16>(K, K2, H, L, st, s);
     case 17: return spectrum_cl<17>(K, K2, H, L, st, s);
@@ -336,6 +337,7 @@ cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, cons
                                 float2* y, int rows, int H, int L, const unsigned* st,
                                 cudaStream_t s) {
   switch (logn) {
+    case 14: return conv_cl<14>(u, K2, D, y, rows, H, L, st, s);
     case 15: return conv_cl<15>(u, K2, D, y, rows, H, L, st, s);
     case 16: return conv_cl<16>(u, K2, D, y, rows, H, L, st, s);
     case 17: return conv_cl<17>(u, K2, D, y, rows, H, L, st, s);

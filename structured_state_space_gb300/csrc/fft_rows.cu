@@ -1,15 +1,21 @@
 // Row FFT kernels whose rows fit one CTA's shared memory (length <= 16384):
-//   ifft_kernel      K = first L of (1/M) iFFT_M(Khat)             (kernel generation)
-//   spectrum_kernel  K2 = FFT_{2M}(K zero-padded to 2M)            (kernel spectrum)
-//   conv_kernel      y = first L of iFFT_{2M}(FFT_{2M}(u) * K2) + D u (fused convolution)
+//   ifft_kernel      K = first L of (1/M) iFFT_M(Khat)                (kernel generation)
+//   spectrum_kernel  K2 = s FFT_{2M}(K zero-padded to 2M), s = 1/(4M)  (kernel spectrum)
+//   conv_pair_kernel y = first L of iFFT_{2M}(FFT_{2M}(u) K2) + D u    (fused convolution)
 //
 // "Recurrent, LSTM, and structured state-space models": filter mode returns
 // the first L coefficients of the inverse radix-two transform of the root
 // values; "Roots-of-unity orthogonality and radix-two FFT cost": a product of
 // two length-n polynomials by zero-padding to a radix-two length >= 2n - 1.
-// Here both factors have length L <= M and the transforms have length 2M.
+// Here both factors have length L <= M and the transforms have length n = 2M.
+//
+// The convolution takes two batch rows b, b+1 of one channel at a time and
+// transforms them together as the real and imaginary parts of one complex
+// row z = u_b + i u_{b+1}; the two spectra follow from Z and its mirror:
+//   U_b[k] = (Z[k] + conj Z[n-k]) / 2,   U_{b+1}[k] = (Z[k] - conj Z[n-k]) / (2i).
+// The factor 1/2 and the inverse transform's 1/n are folded into K2.
+#include "s4_fft.cuh"
 #include "s4_internal.h"
-#include "s4_plan.cuh"
 
 namespace s4dev {
 
@@ -37,7 +43,7 @@ __global__ void __launch_bounds__(128) ifft_small_kernel(const float2* __restric
 template <int LOGN>
 __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __restrict__ K,
                                                              float2* __restrict__ K2, int H, int L,
-                                                             unsigned* __restrict__ status) {
+                                                             float scale, unsigned* __restrict__ status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
   const int h = blockIdx.x * 128 + threadIdx.x;
   if (h >= H) return;
@@ -49,39 +55,53 @@ __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __res
 #pragma unroll
   for (int q = 0; q < n; ++q) {
     fin = fin && cfinite(a[q]);
-    K2[(size_t)h * n + q] = a[q];
+    K2[(size_t)h * n + q] = cscale(a[q], scale);
   }
   if (!fin) atomicOr(status, ST_NONFINITE);
 }
 
+// rows of length n <= 16 with K2 scaled by 1/(2n): two rows per thread
 template <int LOGN>
 __global__ void __launch_bounds__(128) conv_small_kernel(const float* __restrict__ u,
                                                          const float2* __restrict__ K2,
                                                          const float* __restrict__ D,
-                                                         float2* __restrict__ y, int rows, int H,
+                                                         float2* __restrict__ y, int batch, int H,
                                                          int L, const unsigned* __restrict__ status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
-  const int row = blockIdx.x * 128 + threadIdx.x;
-  if (row >= rows) return;
-  const int h = row % H;
+  const int pairs = ((batch + 1) / 2) * H;
+  const int p = blockIdx.x * 128 + threadIdx.x;
+  if (p >= pairs) return;
+  const int h = p % H, b0 = 2 * (p / H);
+  const bool has1 = b0 + 1 < batch;
+  const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
   const bool zero = *((volatile const unsigned*)status) != 0u;
-  float uv[n / 2];
-  float2 a[n];
+  float u0[n / 2], u1[n / 2];
+  float2 z[n];
 #pragma unroll
   for (int q = 0; q < n / 2; ++q) {
-    uv[q] = q < L ? u[(size_t)row * L + q] : 0.f;
-    a[q] = make_float2(uv[q], 0.f);
+    u0[q] = q < L ? u[row0 * L + q] : 0.f;
+    u1[q] = (has1 && q < L) ? u[row1 * L + q] : 0.f;
+    z[q] = make_float2(u0[q], u1[q]);
   }
-  dft<n, false, true>(a);
+  dft<n, false, true>(z);
+  float2 a0[n], a1[n];
 #pragma unroll
-  for (int q = 0; q < n; ++q) a[q] = cmul(a[q], K2[(size_t)h * n + q]);
-  dft<n, true, false, true>(a);
-  const float sc = 1.f / n, d = D[h];
+  for (int k = 0; k < n; ++k) {
+    const float2 zp = z[(n - k) & (n - 1)];
+    const float2 kv = K2[(size_t)h * n + k];
+    a0[k] = cmul(make_float2(z[k].x + zp.x, z[k].y - zp.y), kv);
+    a1[k] = cmul(make_float2(z[k].y + zp.y, zp.x - z[k].x), kv);
+  }
+  dft<n, true, false, true>(a0);
+  dft<n, true, false, true>(a1);
+  const float d = D[h];
 #pragma unroll
-  for (int q = 0; q < n / 2; ++q)
-    if (q < L)
-      y[(size_t)row * L + q] =
-          zero ? make_float2(0.f, 0.f) : make_float2(fmaf(a[q].x, sc, d * uv[q]), a[q].y * sc);
+  for (int q = 0; q < n / 2; ++q) {
+    if (q < L) {
+      y[row0 * L + q] = zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, u0[q], a0[q].x), a0[q].y);
+      if (has1) y[row1 * L + q] = zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, u1[q], a1[q].x), a1[q].y);
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -96,8 +116,6 @@ struct RowCfg {
   static constexpr int NP = plan_npass(LOGN);
   static constexpr int RA = plan_radix(LOGN, 0, false);       // first forward radix
   static constexpr int RB = plan_radix(LOGN, NP - 1, false);  // last forward radix
-  static constexpr int TWF = plan_tw_size(LOGN, false);
-  static constexpr int TWI = plan_tw_size(LOGN, true);
   static constexpr int PADN = padded_len(n);
 };
 
@@ -110,209 +128,360 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
   constexpr int n = C::n, T = C::T, NP = C::NP;
   constexpr int R0 = plan_radix(LOGN, 0, true), RL = plan_radix(LOGN, NP - 1, true);
   constexpr int NB0 = n / R0, PER0 = NB0 / T, NBL = n / RL, PERL = NBL / T;
+  using IX0 = PassIdx<n, R0, 1>;
+  using IXL = PassIdx<n, RL, n / RL>;
+  using TWL = PassTw<LOGN, NP - 1, true>;
   extern __shared__ float2 smem[];
-  float2* tw = smem;
-  float2* data = smem + C::TWI;
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
-  float2* buf = data + slot * C::PADN;
-  fill_plan_twiddles<LOGN, true>(tw, threadIdx.x, C::THREADS);
+  float2* buf = smem + slot * C::PADN;
+  float2* const bufs[1] = {buf};
   const bool zero = *((volatile const unsigned*)status) != 0u;
-  __syncthreads();
   const float sc = 1.f / n;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
     const bool act = h < H;
-    {  // inverse pass 0 (P = 1): global -> registers -> shared
-      float2 a[PER0][R0];
 #pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
+    for (int s = 0; s < PER0; ++s) {  // inverse pass 0 (P = 1): global -> shared
+      const int i = lt + s * T;
+      float2 a[R0];
 #pragma unroll
-        for (int q = 0; q < R0; ++q)
-          a[s][q] = act ? Khat[(size_t)h * n + i + q * NB0] : make_float2(0.f, 0.f);
-        dft<R0, true>(a[s]);
+      for (int q = 0; q < R0; ++q)
+        a[q] = act ? Khat[(size_t)h * n + i + q * NB0] : make_float2(0.f, 0.f);
+      dft<R0, true>(a);
 #pragma unroll
-        for (int q = 0; q < R0; ++q) buf[pad(i * R0 + q)] = a[s][q];
-      }
-      __syncthreads();
+      for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
     }
-    run_passes<LOGN, true, 1, NP - 2, T>(buf, tw, lt);
-    {  // last inverse pass (P = n / RL): shared -> registers -> global
-      const float2* twl = tw + plan_tw_off(LOGN, NP - 1, true);
+    __syncthreads();
+    passes_rows<LOGN, true, 1, NP - 2, T, 1>(bufs, lt);
 #pragma unroll
-      for (int s = 0; s < PERL; ++s) {
-        const int i = lt + s * T;
-        float2 a[RL];
+    for (int s = 0; s < PERL; ++s) {  // last inverse pass: shared -> global
+      const int i = lt + s * T;
+      float2 a[RL], w[RL];
 #pragma unroll
-        for (int q = 0; q < RL; ++q) a[q] = buf[pad(i + q * NBL)];
-        float2 w = twl[i];
-        w.y = -w.y;
-        apply_twiddles<RL>(a, w);
-        dft<RL, true>(a);
+      for (int q = 0; q < RL; ++q) a[q] = buf[IXL::rd(i, q)];
+      TWL::load(w, i);
+      TWL::apply(a, w);
+      dft<RL, true>(a);
 #pragma unroll
-        for (int q = 0; q < RL; ++q) {
-          const int t = i + q * NBL;
-          if (act && t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(a[q], sc);
-        }
+      for (int q = 0; q < RL; ++q) {
+        const int t = i + q * NBL;
+        if (act && t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(a[q], sc);
       }
-      __syncthreads();
     }
+    __syncthreads();
   }
 }
 
-// Spectrum of each channel's kernel zero-padded to n = 2M (natural order).
+// Spectrum of each channel's kernel zero-padded to n = 2M, natural order, times `scale`.
 template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
-    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
+    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale,
     unsigned* __restrict__ status) {
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
+  using IX0 = PassIdx<n, RA, 1>;
+  using IXL = PassIdx<n, RB, n / RB>;
+  using TWL = PassTw<LOGN, NP - 1, false>;
   extern __shared__ float2 smem[];
-  float2* tw = smem;
-  float2* data = smem + C::TWF;
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
-  float2* buf = data + slot * C::PADN;
-  fill_plan_twiddles<LOGN, false>(tw, threadIdx.x, C::THREADS);
-  __syncthreads();
+  float2* buf = smem + slot * C::PADN;
+  float2* const bufs[1] = {buf};
   bool fin = true;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
     const bool act = h < H;
-    {  // forward pass 0 (P = 1), upper half of the input is the zero padding
 #pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
-        float2 a[RA];
+    for (int s = 0; s < PER0; ++s) {  // forward pass 0; the upper half is the zero padding
+      const int i = lt + s * T;
+      float2 a[RA];
 #pragma unroll
-        for (int q = 0; q < RA / 2; ++q) {
-          const int t = i + q * NB0;
-          a[q] = (act && t < L) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
-        }
-        dft<RA, false, true>(a);
-#pragma unroll
-        for (int q = 0; q < RA; ++q) buf[pad(i * RA + q)] = a[q];
+      for (int q = 0; q < RA / 2; ++q) {
+        const int t = i + q * NB0;
+        a[q] = (act && t < L) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
       }
-      __syncthreads();
+      dft<RA, false, true>(a);
+#pragma unroll
+      for (int q = 0; q < RA; ++q) buf[IX0::wr(i, q)] = a[q];
     }
-    run_passes<LOGN, false, 1, NP - 2, T>(buf, tw, lt);
-    {  // last forward pass: shared -> registers -> global
-      const float2* twl = tw + plan_tw_off(LOGN, NP - 1, false);
+    __syncthreads();
+    passes_rows<LOGN, false, 1, NP - 2, T, 1>(bufs, lt);
 #pragma unroll
-      for (int s = 0; s < PERL; ++s) {
-        const int i = lt + s * T;
-        float2 a[RB];
+    for (int s = 0; s < PERL; ++s) {  // last forward pass: shared -> global
+      const int i = lt + s * T;
+      float2 a[RB], w[RB];
 #pragma unroll
-        for (int q = 0; q < RB; ++q) a[q] = buf[pad(i + q * NBL)];
-        apply_twiddles<RB>(a, twl[i]);
-        dft<RB, false>(a);
-        if (act) {
+      for (int q = 0; q < RB; ++q) a[q] = buf[IXL::rd(i, q)];
+      TWL::load(w, i);
+      TWL::apply(a, w);
+      dft<RB, false>(a);
+      if (act) {
 #pragma unroll
-          for (int q = 0; q < RB; ++q) {
-            fin = fin && cfinite(a[q]);
-            K2[(size_t)h * n + i + q * NBL] = a[q];
-          }
+        for (int q = 0; q < RB; ++q) {
+          fin = fin && cfinite(a[q]);
+          K2[(size_t)h * n + i + q * NBL] = cscale(a[q], scale);
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
   }
   if (!fin) atomicOr(status, ST_NONFINITE);
 }
 
-// Fused causal convolution of real rows u[row] (row = b H + h) with the
-// channel spectrum K2[h]: pad -> FFT -> product -> iFFT -> first L -> + D u.
+// Layer path: for each channel, K = first L of (1/M) iFFT_M(Khat) (written
+// out) and, from the same shared-memory row, K2 = scale FFT_2M(K zero-padded).
+// One launch instead of two, and K is not read back.  Rows of 2M <= 2^13
+// points (LOGM = 5..12).
+template <int LOGM>
+__global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
+    const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
+    float scale, unsigned* __restrict__ status) {
+  constexpr int LOGN = LOGM + 1;
+  using C = RowCfg<LOGN>;
+  constexpr int M = 1 << LOGM, n = C::n, T = C::T;
+  constexpr int TI = row_threads(LOGM);
+  static_assert(TI <= T, "thread split");
+  // inverse, length M
+  constexpr int NPI = plan_npass(LOGM);
+  constexpr int RI0 = plan_radix(LOGM, 0, true), RIL = plan_radix(LOGM, NPI - 1, true);
+  constexpr int NBI0 = M / RI0, PERI0 = NBI0 / TI, NBIL = M / RIL, PERIL = NBIL / TI;
+  using IXI0 = PassIdx<M, RI0, 1>;
+  using IXIL = PassIdx<M, RIL, M / RIL>;
+  using TWIL = PassTw<LOGM, NPI - 1, true>;
+  // forward, length n = 2M
+  constexpr int NPF = C::NP, RA = C::RA, RB = C::RB;
+  constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
+  using IXF0 = PassIdx<n, RA, 1>;
+  using IXFL = PassIdx<n, RB, n / RB>;
+  using TWFL = PassTw<LOGN, NPF - 1, false>;
+  static_assert(NPI >= 2 && NPF >= 2, "sizes");
+  extern __shared__ float2 smem[];
+  const int slot = threadIdx.x / T, lt = threadIdx.x % T;
+  float2* buf = smem + slot * C::PADN;
+  float2* const bufs[1] = {buf};
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const float sc = 1.f / M;
+  bool fin = true;
+  for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
+    const int h = h0 + slot;
+    const bool act = h < H;
+    if (lt < TI) {  // inverse pass 0 (P = 1): root values -> shared
+#pragma unroll
+      for (int s = 0; s < PERI0; ++s) {
+        const int i = lt + s * TI;
+        float2 a[RI0];
+#pragma unroll
+        for (int q = 0; q < RI0; ++q)
+          a[q] = act ? Khat[(size_t)h * M + i + q * NBI0] : make_float2(0.f, 0.f);
+        dft<RI0, true>(a);
+#pragma unroll
+        for (int q = 0; q < RI0; ++q) buf[IXI0::wr(i, q)] = a[q];
+      }
+    }
+    __syncthreads();
+    passes_rows<LOGM, true, 1, NPI - 2, TI, 1>(bufs, lt);
+    float2 kv[PERIL][RIL];
+    if (lt < TI) {  // last inverse pass: K in registers
+#pragma unroll
+      for (int s = 0; s < PERIL; ++s) {
+        const int i = lt + s * TI;
+        float2 w[RIL];
+#pragma unroll
+        for (int q = 0; q < RIL; ++q) kv[s][q] = buf[IXIL::rd(i, q)];
+        TWIL::load(w, i);
+        TWIL::apply(kv[s], w);
+        dft<RIL, true>(kv[s]);
+      }
+    }
+    __syncthreads();
+    if (lt < TI) {  // K out (first L, scaled) and into shared memory, natural order
+#pragma unroll
+      for (int s = 0; s < PERIL; ++s) {
+        const int i = lt + s * TI;
+#pragma unroll
+        for (int q = 0; q < RIL; ++q) {
+          const int t = i + q * NBIL;
+          const float2 v = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(kv[s][q], sc);
+          if (act && t < L) K[(size_t)h * L + t] = v;
+          buf[pad(t)] = v;
+        }
+      }
+    }
+    __syncthreads();
+    {  // forward pass 0 of the spectrum (upper half is the zero padding)
+      float2 a[PER0][RA];
+#pragma unroll
+      for (int s = 0; s < PER0; ++s) {
+        const int i = lt + s * T;
+#pragma unroll
+        for (int q = 0; q < RA / 2; ++q) a[s][q] = buf[pad(i + q * NB0)];
+        dft<RA, false, true>(a[s]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < PER0; ++s) {
+        const int i = lt + s * T;
+#pragma unroll
+        for (int q = 0; q < RA; ++q) buf[IXF0::wr(i, q)] = a[s][q];
+      }
+      __syncthreads();
+    }
+    passes_rows<LOGN, false, 1, NPF - 2, T, 1>(bufs, lt);
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {  // last forward pass -> K2
+      const int i = lt + s * T;
+      float2 a[RB], w[RB];
+#pragma unroll
+      for (int q = 0; q < RB; ++q) a[q] = buf[IXFL::rd(i, q)];
+      TWFL::load(w, i);
+      TWFL::apply(a, w);
+      dft<RB, false>(a);
+      if (act) {
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          fin = fin && cfinite(a[q]);
+          K2[(size_t)h * n + i + q * NBL] = cscale(a[q], scale);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (!fin) atomicOr(status, ST_NONFINITE);
+}
+
+// Resident CTAs per SM the convolution is compiled for: 512 threads per SM
+// (4 CTAs of 128 threads, 128 registers each) measured fastest at 2M = 2048 --
+// the kernel is latency-bound and occupancy beats the extra registers.  Rows
+// of 8192 points (256 threads) keep their registers (128 would spill).
+__host__ __device__ constexpr int conv_min_blocks(int logn, int threads) {
+  return (logn >= 13 || threads >= 512) ? 1 : 512 / threads;
+}
+
+// Fused causal convolution, two batch rows (b, b+1) of one channel per row
+// group; K2 is the channel spectrum scaled by 1/(2n).
 template <int LOGN>
-__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) conv_kernel(
+__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN>::THREADS))
+conv_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int rows, int H, int L, const unsigned* __restrict__ status) {
+    float2* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
+  using IXF0 = PassIdx<n, RA, 1>;        // forward pass 0 writes
+  using IXFL = PassIdx<n, RB, n / RB>;   // forward last pass reads
+  using IXI0 = PassIdx<n, RB, 1>;        // inverse pass 0 writes
+  using IXIL = PassIdx<n, RA, n / RA>;   // inverse last pass reads
+  using TWFL = PassTw<LOGN, NP - 1, false>;
+  using TWIL = PassTw<LOGN, NP - 1, true>;
   extern __shared__ float2 smem[];
-  float2* twf = smem;
-  float2* twi = smem + C::TWF;
-  float2* data = twi + C::TWI;
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
-  float2* buf = data + slot * C::PADN;
-  fill_plan_twiddles<LOGN, false>(twf, threadIdx.x, C::THREADS);
-  fill_plan_twiddles<LOGN, true>(twi, threadIdx.x, C::THREADS);
+  float2* bufA = smem + slot * 2 * C::PADN;
+  float2* bufB = bufA + C::PADN;
+  float2* const buf1[1] = {bufA};
+  float2* const buf2[2] = {bufA, bufB};
   const bool zero = *((volatile const unsigned*)status) != 0u;
-  __syncthreads();
-  const float sc = 1.f / n;
-  for (int r0 = blockIdx.x * C::ROWS; r0 < rows; r0 += gridDim.x * C::ROWS) {
-    const int row = r0 + slot;
-    const bool act = row < rows;
-    const int h = act ? row % H : 0;
+  const int pairs = ((batch + 1) / 2) * H;
+  for (int p0 = blockIdx.x * C::ROWS; p0 < pairs; p0 += gridDim.x * C::ROWS) {
+    const int p = p0 + slot;
+    const bool act = p < pairs;
+    const int h = act ? p % H : 0;
+    const int b0 = act ? 2 * (p / H) : 0;
+    const bool has1 = act && b0 + 1 < batch;
+    const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
     const float d = act ? D[h] : 0.f;
-    float uv[PER0][RA / 2];
-    {  // forward pass 0: u (real, zero-padded) -> registers -> shared
+    float u0[PER0][RA / 2], u1[PER0][RA / 2];
+    // forward pass 0: z = u_b + i u_{b+1}, zero-padded, global -> shared
 #pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
-        float2 a[RA];
+    for (int s = 0; s < PER0; ++s) {
+      const int i = lt + s * T;
+      float2 a[RA];
 #pragma unroll
-        for (int q = 0; q < RA / 2; ++q) {
-          const int t = i + q * NB0;
-          uv[s][q] = (act && t < L) ? u[(size_t)row * L + t] : 0.f;
-          a[q] = make_float2(uv[s][q], 0.f);
+      for (int q = 0; q < RA / 2; ++q) {
+        const int t = i + q * NB0;
+        const float x0 = (act && t < L) ? u[row0 * L + t] : 0.f;
+        const float x1 = (has1 && t < L) ? u[row1 * L + t] : 0.f;
+        u0[s][q] = x0;
+        u1[s][q] = x1;
+        a[q] = make_float2(x0, x1);
+      }
+      dft<RA, false, true>(a);
+#pragma unroll
+      for (int q = 0; q < RA; ++q) bufA[IXF0::wr(i, q)] = a[q];
+    }
+    __syncthreads();
+    passes_rows<LOGN, false, 1, NP - 2, T, 1>(buf1, lt);
+    // forward last pass; Z in natural order k = i + q NBL goes to bufB
+    float2 z[PERL][RB];
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+      float2 w[RB];
+#pragma unroll
+      for (int q = 0; q < RB; ++q) z[s][q] = bufA[IXFL::rd(i, q)];
+      TWFL::load(w, i);
+      TWFL::apply(z[s], w);
+      dft<RB, false>(z[s]);
+#pragma unroll
+      for (int q = 0; q < RB; ++q) bufB[IXFL::rd(i, q)] = z[s][q];
+    }
+    __syncthreads();
+    // split the two spectra, multiply by K2, first inverse pass (P = 1) in registers
+    float2 a0[PERL][RB], a1[PERL][RB];
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+#pragma unroll
+      for (int q = 0; q < RB; ++q) {
+        const int k = i + q * NBL;
+        const float2 zp = bufB[pad((n - k) & (n - 1))];
+        const float2 kv = __ldg(K2 + (size_t)h * n + k);
+        const float2 zk = z[s][q];
+        a0[s][q] = cmul(make_float2(zk.x + zp.x, zk.y - zp.y), kv);
+        a1[s][q] = cmul(make_float2(zk.y + zp.y, zp.x - zk.x), kv);
+      }
+      dft<RB, true>(a0[s]);
+      dft<RB, true>(a1[s]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+#pragma unroll
+      for (int q = 0; q < RB; ++q) {
+        bufA[IXI0::wr(i, q)] = a0[s][q];
+        bufB[IXI0::wr(i, q)] = a1[s][q];
+      }
+    }
+    __syncthreads();
+    passes_rows<LOGN, true, 1, NP - 2, T, 2>(buf2, lt);
+    // last inverse pass: first L outputs of both rows + D u
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {
+      const int i = lt + s * T;
+      float2 c0[RA], c1[RA], w[RA];
+#pragma unroll
+      for (int q = 0; q < RA; ++q) {
+        c0[q] = bufA[IXIL::rd(i, q)];
+        c1[q] = bufB[IXIL::rd(i, q)];
+      }
+      TWIL::load(w, i);
+      TWIL::apply(c0, w);
+      TWIL::apply(c1, w);
+      dft<RA, true, false, true>(c0);
+      dft<RA, true, false, true>(c1);
+#pragma unroll
+      for (int q = 0; q < RA / 2; ++q) {
+        const int t = i + q * NB0;
+        if (t < L) {
+          const float x0 = u0[s][q], x1 = u1[s][q];
+          if (act)
+            __stcs(y + row0 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, x0, c0[q].x), c0[q].y));
+          if (has1)
+            __stcs(y + row1 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, x1, c1[q].x), c1[q].y));
         }
-        dft<RA, false, true>(a);
-#pragma unroll
-        for (int q = 0; q < RA; ++q) buf[pad(i * RA + q)] = a[q];
       }
-      __syncthreads();
     }
-    run_passes<LOGN, false, 1, NP - 2, T>(buf, twf, lt);
-    {  // last forward pass, product with K2, first inverse pass: all in registers
-      const float2* twl = twf + plan_tw_off(LOGN, NP - 1, false);
-      float2 a[PERL][RB];
-#pragma unroll
-      for (int s = 0; s < PERL; ++s) {
-        const int i = lt + s * T;
-        float2 kv[RB];
-#pragma unroll
-        for (int q = 0; q < RB; ++q) kv[q] = K2[(size_t)h * n + i + q * NBL];
-#pragma unroll
-        for (int q = 0; q < RB; ++q) a[s][q] = buf[pad(i + q * NBL)];
-        apply_twiddles<RB>(a[s], twl[i]);
-        dft<RB, false>(a[s]);
-#pragma unroll
-        for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], kv[q]);
-        dft<RB, true>(a[s]);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int s = 0; s < PERL; ++s) {
-        const int i = lt + s * T;
-#pragma unroll
-        for (int q = 0; q < RB; ++q) buf[pad(i * RB + q)] = a[s][q];
-      }
-      __syncthreads();
-    }
-    run_passes<LOGN, true, 1, NP - 2, T>(buf, twi, lt);
-    {  // last inverse pass: shared -> registers -> first L outputs + D u
-      const float2* twl = twi + plan_tw_off(LOGN, NP - 1, true);
-#pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
-        float2 a[RA];
-#pragma unroll
-        for (int q = 0; q < RA; ++q) a[q] = buf[pad(i + q * NB0)];
-        float2 w = twl[i];
-        w.y = -w.y;
-        apply_twiddles<RA>(a, w);
-        dft<RA, true, false, true>(a);
-#pragma unroll
-        for (int q = 0; q < RA / 2; ++q) {
-          const int t = i + q * NB0;
-          if (act && t < L)
-            y[(size_t)row * L + t] = zero ? make_float2(0.f, 0.f)
-                                          : make_float2(fmaf(a[q].x, sc, d * uv[s][q]), a[q].y * sc);
-        }
-      }
-      __syncthreads();
-    }
+    __syncthreads();
   }
 }
 
@@ -348,7 +517,7 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, cons
     ifft_small_kernel<LOGN><<<(H + 127) / 128, 128, 0, s>>>(Khat, K, H, L, st);
   } else {
     using C = RowCfg<LOGN>;
-    const size_t smem = sizeof(float2) * (C::TWI + (size_t)C::ROWS * C::PADN);
+    const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
     auto k = ifft_kernel<LOGN>;
     cudaError_t e = prepare(k, smem);
     if (e != cudaSuccess) return e;
@@ -362,39 +531,73 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, cons
 template <int LOGN>
 static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, unsigned* st,
                                    cudaStream_t s) {
+  const float scale = 1.f / (float)(2 << LOGN);  // 1/(2n): pair split and inverse scaling
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("spectrum", s);
-    spectrum_small_kernel<LOGN><<<(H + 127) / 128, 128, 0, s>>>(K, K2, H, L, st);
+    spectrum_small_kernel<LOGN><<<(H + 127) / 128, 128, 0, s>>>(K, K2, H, L, scale, st);
   } else {
     using C = RowCfg<LOGN>;
-    const size_t smem = sizeof(float2) * (C::TWF + (size_t)C::ROWS * C::PADN);
+    const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
     auto k = spectrum_kernel<LOGN>;
     cudaError_t e = prepare(k, smem);
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("spectrum", s);
-    k<<<grid, C::THREADS, smem, s>>>(K, K2, H, L, st);
+    k<<<grid, C::THREADS, smem, s>>>(K, K2, H, L, scale, st);
   }
   return cudaGetLastError();
 }
 
 template <int LOGN>
-static cudaError_t conv_launch(const float* u, const float2* K2, const float* D, float2* y, int rows,
+static cudaError_t conv_launch(const float* u, const float2* K2, const float* D, float2* y, int batch,
                                int H, int L, const unsigned* st, cudaStream_t s) {
+  const int pairs = ((batch + 1) / 2) * H;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("conv", s);
-    conv_small_kernel<LOGN><<<(rows + 127) / 128, 128, 0, s>>>(u, K2, D, y, rows, H, L, st);
+    conv_small_kernel<LOGN><<<(pairs + 127) / 128, 128, 0, s>>>(u, K2, D, y, batch, H, L, st);
   } else {
     using C = RowCfg<LOGN>;
-    const size_t smem = sizeof(float2) * (C::TWF + C::TWI + (size_t)C::ROWS * C::PADN);
-    auto k = conv_kernel<LOGN>;
+    const size_t smem = sizeof(float2) * 2 * (size_t)C::ROWS * C::PADN;
+    auto k = conv_pair_kernel<LOGN>;
     cudaError_t e = prepare(k, smem);
     if (e != cudaSuccess) return e;
-    const int grid = grid_for(k, C::THREADS, smem, (rows + C::ROWS - 1) / C::ROWS);
+    const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv", s);
-    k<<<grid, C::THREADS, smem, s>>>(u, K2, D, y, rows, H, L, st);
+    k<<<grid, C::THREADS, smem, s>>>(u, K2, D, y, batch, H, L, st);
   }
   return cudaGetLastError();
+}
+
+template <int LOGM>
+static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H, int L, unsigned* st,
+                                cudaStream_t s) {
+  using C = RowCfg<LOGM + 1>;
+  const float scale = 1.f / (float)(4 << LOGM);  // 1/(2n), n = 2M
+  const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
+  auto k = kspec_kernel<LOGM>;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
+  TimedLaunch tl("kspec", s);
+  k<<<grid, C::THREADS, smem, s>>>(Khat, K, K2, H, L, scale, st);
+  return cudaGetLastError();
+}
+
+bool kspec_supported(int logM) { return logM >= 5 && logM <= 12; }
+
+cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
+                              unsigned* st, cudaStream_t s) {
+  switch (logM) {
+    case 5: return kspec_launch<5>(Khat, K, K2, H, L, st, s);
+    case 6: return kspec_launch<6>(Khat, K, K2, H, L, st, s);
+    case 7: return kspec_launch<7>(Khat, K, K2, H, L, st, s);
+    case 8: return kspec_launch<8>(Khat, K, K2, H, L, st, s);
+    case 9: return kspec_launch<9>(Khat, K, K2, H, L, st, s);
+    case 10: return kspec_launch<10>(Khat, K, K2, H, L, st, s);
+    case 11: return kspec_launch<11>(Khat, K, K2, H, L, st, s);
+    case 12: return kspec_launch<12>(Khat, K, K2, H, L, st, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
@@ -418,7 +621,7 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
   case X:          \
     return spectrum_launch<X>(K, K2, H, L, st, s);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
-    S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13) S4_CASE(14)
+    S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE
     default:
       return cudaErrorInvalidValue;
@@ -426,13 +629,13 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
 }
 
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int rows, int H, int L, const unsigned* st, cudaStream_t s) {
+                             int batch, int H, int L, const unsigned* st, cudaStream_t s) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
-    return conv_launch<X>(u, K2, D, y, rows, H, L, st, s);
+    return conv_launch<X>(u, K2, D, y, batch, H, L, st, s);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
-    S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13) S4_CASE(14)
+    S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE
     default:
       return cudaErrorInvalidValue;

@@ -26,16 +26,15 @@ int ilog2_ceil(int v) {
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Workspace: [status word | tan table (M) | root values (H M) | kernel spectra (H 2M)]
+// Workspace: [status word | root values (H M) | kernel spectra (H 2M)]
 struct Layout {
-  size_t tau, khat, k2, total;
+  size_t khat, k2, total;
 };
 
 Layout layout_for(int H, int L) {
   const size_t M = (size_t)1 << ilog2_ceil(L);
   Layout l;
-  l.tau = 256;
-  l.khat = l.tau + round256(sizeof(float2) * M);
+  l.khat = 256;
   l.k2 = l.khat + round256(sizeof(float2) * M * (size_t)H);
   l.total = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
   return l;
@@ -59,23 +58,29 @@ s4_status check_ws(const void* ws, size_t ws_bytes, int H, int L) {
 
 s4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? S4_OK : S4_ERR_CUDA; }
 
+cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
+                        const s4_c32* Ct, const float* dt, int H, int N, int r, int L, void* ws,
+                        cudaStream_t s) {
+  using namespace s4impl;
+  const int logM = ilog2_ceil(L);
+  char* w = static_cast<char*>(ws);
+  return launch_cauchy(reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
+                       reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
+                       reinterpret_cast<const float2*>(Ct), dt,
+                       reinterpret_cast<float2*>(w + layout_for(H, L).khat), H, N, r, 1 << logM,
+                       khat_cluster_log(logM), reinterpret_cast<unsigned*>(w), s);
+}
+
 s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
                    const s4_c32* Ct, const float* dt, int H, int N, int r, int L, s4_c32* K,
                    void* ws, cudaStream_t s) {
   using namespace s4impl;
   const int logM = ilog2_ceil(L);
-  const int M = 1 << logM;
-  const int logC = cluster_log(logM);
   const Layout lay = layout_for(H, L);
   char* w = static_cast<char*>(ws);
   unsigned* st = reinterpret_cast<unsigned*>(w);
-  float2* tau = reinterpret_cast<float2*>(w + lay.tau);
   float2* khat = reinterpret_cast<float2*>(w + lay.khat);
-  cudaError_t e = launch_tau(tau, M, logC, s);
-  if (e == cudaSuccess)
-    e = launch_cauchy(reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
-                      reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
-                      reinterpret_cast<const float2*>(Ct), dt, tau, khat, H, N, r, M, logC, st, s);
+  cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ct, dt, H, N, r, L, ws, s);
   if (e == cudaSuccess)
     e = logM <= kMaxLogRowCta
             ? launch_ifft_rows(logM, khat, reinterpret_cast<float2*>(K), H, L, st, s)
@@ -95,9 +100,9 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
   float2* yf = reinterpret_cast<float2*>(y);
   const int rows = batch * H;
   cudaError_t e;
-  if (logn <= kMaxLogRowCta) {
+  if (logn <= kMaxLogConvRow) {
     e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s);
-    if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, rows, H, L, st, s);
+    if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
     if (e == cudaSuccess) e = launch_conv_cluster(logn, u, k2, D, yf, rows, H, L, st, s);
@@ -148,13 +153,22 @@ TimedLaunch::TimedLaunch(const char* name, cudaStream_t s) : slot_(-1), s_(s) {
   slot_ = (int)g_recs.size();
   g_recs.push_back({name, pr.first, pr.second});
   ++g_used;
-  cudaEventRecord(pr.first, s);
+  record(pr.first, s);
+}
+
+// Inside a stream capture the events become event-record nodes of the graph.
+void TimedLaunch::record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
 }
 
 TimedLaunch::~TimedLaunch() {
   if (slot_ < 0) return;
   std::lock_guard<std::mutex> lk(g_tmu);
-  cudaEventRecord(g_recs[slot_].stop, s_);
+  record(g_recs[slot_].stop, s_);
 }
 
 }  // namespace s4impl
@@ -209,6 +223,21 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  const int logM = ilog2_ceil(L);
+  if (s4impl::kspec_supported(logM) && logM + 1 <= s4impl::kMaxLogConvRow) {
+    // root values -> (K, kernel spectrum) in one launch -> convolution
+    const Layout lay = layout_for(H, L);
+    char* w = static_cast<char*>(ws);
+    unsigned* st = reinterpret_cast<unsigned*>(w);
+    float2* khat = reinterpret_cast<float2*>(w + lay.khat);
+    float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
+    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, s);
+    if (e == cudaSuccess)
+      e = s4impl::launch_kspec_rows(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
+    if (e == cudaSuccess)
+      e = s4impl::launch_conv_rows(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L, st, s);
+    return cuda_status(e);
+  }
   const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);
   if (g != S4_OK) return g;
   return conv_impl(u, K, D, batch, H, L, y, ws, s);

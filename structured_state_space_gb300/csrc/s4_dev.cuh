@@ -145,51 +145,4 @@ __device__ __forceinline__ void apply_twiddles(float2* a, float2 w) {
   }
 }
 
-// Twiddle base table of one Stockham pass: tw[k] = exp(-2 pi i k / (P R)), k < P.
-__device__ __forceinline__ void fill_twiddles(float2* tw, int P, int PR, int tid, int nthreads) {
-  for (int k = tid; k < P; k += nthreads) {
-    float s, c;
-    sincospif(2.0f * (float)k / (float)PR, &s, &c);
-    tw[k] = make_float2(c, -s);
-  }
-}
-
-// One Stockham radix-R pass (Bainville's auto-sort form) over a row of N
-// points in padded shared memory.  P = product of the radices of the
-// earlier passes.  Butterfly i reads x[i + q N/R], multiplies by
-// w_{PR}^{q (i mod P)}, transforms, and writes to (i - k) R + k + q P.
-// `lt` is this thread's index in the row's T-thread group.
-template <int N, int R, int P, bool INV, int T>
-__device__ __forceinline__ void pass_smem(float2* buf, const float2* tw, int lt) {
-  constexpr int NB = N / R;
-  constexpr int PER = (NB + T - 1) / T;
-  float2 a[PER][R];
-#pragma unroll
-  for (int s = 0; s < PER; ++s) {
-    const int i = lt + s * T;
-    if (NB % T == 0 || i < NB) {
-#pragma unroll
-      for (int q = 0; q < R; ++q) a[s][q] = buf[pad(i + q * NB)];
-      if constexpr (P > 1) {
-        float2 w = tw[i & (P - 1)];
-        if (INV) w.y = -w.y;
-        apply_twiddles<R>(a[s], w);
-      }
-      dft<R, INV>(a[s]);
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int s = 0; s < PER; ++s) {
-    const int i = lt + s * T;
-    if (NB % T == 0 || i < NB) {
-      const int k = i & (P - 1);
-      const int j0 = (i - k) * R + k;
-#pragma unroll
-      for (int q = 0; q < R; ++q) buf[pad(j0 + q * P)] = a[s][q];
-    }
-  }
-  __syncthreads();
-}
-
 }  // namespace s4dev

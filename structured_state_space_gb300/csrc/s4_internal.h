@@ -18,36 +18,48 @@ class TimedLaunch {
   TimedLaunch& operator=(const TimedLaunch&) = delete;
 
  private:
+  static void record(cudaEvent_t e, cudaStream_t s);
   int slot_;
   cudaStream_t s_;
 };
 
-// Largest row that one CTA transforms in shared memory (log2 of the length).
+// Longest rows (log2 of the length) that one CTA transforms in shared
+// memory: the inverse transform of the root values holds one row, the
+// convolution two (a pair of batch rows) and so stops one size earlier.
 constexpr int kMaxLogRowCta = 14;
+constexpr int kMaxLogConvRow = 13;
 
-// log2 of the cluster size that splits a row of 2^logn points: rows of up to
-// 2^14 points stay in one CTA; 2^15 uses 4 CTAs of 2^13; 2^16 uses 8 of 2^13;
-// 2^17 uses 8 of 2^14.  Spectra of split rows are stored in blocked order.
+// log2 of the cluster size that splits a longer row of 2^logn points:
+// 2^14 uses 2 CTAs of 2^13 (convolution only); 2^15 uses 4 of 2^13; 2^16
+// uses 8 of 2^13; 2^17 uses 8 of 2^14.  Spectra of split rows are stored in
+// blocked order.
 __host__ __device__ constexpr int cluster_log(int logn) {
-  return logn <= kMaxLogRowCta ? 0 : (logn == 15 ? 2 : 3);
+  return logn <= 13 ? 0 : (logn == 14 ? 1 : (logn == 15 ? 2 : 3));
+}
+// Blocked layout of the root values (inverse transform of length 2^logM).
+__host__ __device__ constexpr int khat_cluster_log(int logM) {
+  return logM <= kMaxLogRowCta ? 0 : cluster_log(logM);
 }
 
-// tan(pi k / M) for every root k, as an fp32 (hi, lo) pair, stored in the
-// blocked root order used for Khat (position p -> root (p mod M/C) C + p div M/C).
-cudaError_t launch_tau(float2* tau, int M, int logC, cudaStream_t s);
-
-// Root values Khat[h][p] (blocked order) for every channel.
+// Root values Khat[h][p] for every channel, in the blocked root order
+// (position p -> root (p mod M/C) C + p div M/C, C = 2^logC).
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
-                          const float2* Ct, const float* dt, const float2* tau, float2* Khat, int H,
-                          int N, int r, int M, int logC, unsigned* status, cudaStream_t s);
+                          const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
+                          int M, int logC, unsigned* status, cudaStream_t s);
 
 // Single-CTA row transforms (log sizes up to kMaxLogRowCta).
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
                              const unsigned* st, cudaStream_t s);
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
                                  cudaStream_t s);
+// Layer path: inverse transform of the root values and the kernel spectrum in
+// one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported).
+bool kspec_supported(int logM);
+cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
+                              unsigned* st, cudaStream_t s);
+// (the row kernels pair batch rows; K2 from launch_spectrum_rows is scaled by 1/(2n))
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int rows, int H, int L, const unsigned* st, cudaStream_t s);
+                             int batch, int H, int L, const unsigned* st, cudaStream_t s);
 
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,

@@ -79,9 +79,9 @@ extern "C" s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const 
   float2* yf = reinterpret_cast<float2*>(y);
   const int rows = batch * H;
   cudaError_t e;
-  if (logn <= s4impl::kMaxLogRowCta) {
+  if (logn <= s4impl::kMaxLogConvRow) {
     e = s4impl::launch_spectrum_rows(logn, Kf, k2, H, L, st, s);
-    if (e == cudaSuccess) e = s4impl::launch_conv_rows(logn, u, k2, D, yf, rows, H, L, st, s);
+    if (e == cudaSuccess) e = s4impl::launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s);
   } else {
     e = s4impl::launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
     if (e == cudaSuccess) e = s4impl::launch_conv_cluster(logn, u, k2, D, yf, rows, H, L, st, s);

@@ -29,16 +29,29 @@ __host__ __device__ constexpr int plan_p(int logn, int idx, bool inv) {
   return p;
 }
 
-// Offset of pass idx's twiddle base table (passes 1.. have tables of P entries).
-__host__ __device__ constexpr int plan_tw_off(int logn, int idx, bool inv) {
+// ---- static twiddle tables (generated at build time, see gen_twiddles.py) ----
+// Pass idx >= 1 of a plan either reads a full row of its R-1 factors
+// w^(k q) ("rows": P <= 256, R > 2; row stride 18/10/6 entries for R =
+// 16/8/4) or the single base factor w^k from which it builds the powers.
+__host__ __device__ constexpr int tw_row_stride(int R) {
+  return R == 16 ? 18 : (R == 8 ? 10 : (R == 4 ? 6 : 2));
+}
+__host__ __device__ constexpr bool tw_is_rows(int P, int R) { return P <= 256 && R > 2; }
+__host__ __device__ constexpr int tw_pass_size(int logn, int idx, bool inv) {
+  return idx < 1 ? 0
+                 : (tw_is_rows(plan_p(logn, idx, inv), plan_radix(logn, idx, inv))
+                        ? plan_p(logn, idx, inv) * tw_row_stride(plan_radix(logn, idx, inv))
+                        : plan_p(logn, idx, inv));
+}
+// Offset of pass idx's table in the per-length array: forward passes first.
+__host__ __device__ constexpr int tw_offset(int logn, bool inv, int idx) {
   int off = 0;
-  for (int j = 1; j < idx; ++j) off += plan_p(logn, j, inv);
+  if (inv)
+    for (int j = 1; j < plan_npass(logn); ++j) off += tw_pass_size(logn, j, false);
+  for (int j = 1; j < idx; ++j) off += tw_pass_size(logn, j, inv);
   return off;
 }
-
-__host__ __device__ constexpr int plan_tw_size(int logn, bool inv) {
-  return plan_tw_off(logn, plan_npass(logn), inv);
-}
+__host__ __device__ constexpr int tw_total(int logn) { return tw_offset(logn, true, plan_npass(logn)); }
 
 // Threads that share one row, rows per CTA.
 __host__ __device__ constexpr int row_threads(int logn) {
@@ -46,26 +59,6 @@ __host__ __device__ constexpr int row_threads(int logn) {
 }
 __host__ __device__ constexpr int rows_per_cta(int logn) {
   return row_threads(logn) >= 128 ? 1 : 128 / row_threads(logn);
-}
-
-template <int LOGN, bool INV>
-__device__ __forceinline__ void fill_plan_twiddles(float2* tw, int tid, int nth) {
-#pragma unroll 1
-  for (int idx = 1; idx < plan_npass(LOGN); ++idx) {
-    const int P = plan_p(LOGN, idx, INV);
-    fill_twiddles(tw + plan_tw_off(LOGN, idx, INV), P, P * plan_radix(LOGN, idx, INV), tid, nth);
-  }
-}
-
-// Stockham passes FIRST..LAST of the plan, all in shared memory.
-template <int LOGN, bool INV, int IDX, int LAST, int T>
-__device__ __forceinline__ void run_passes(float2* buf, const float2* tw, int lt) {
-  if constexpr (IDX <= LAST) {
-    constexpr int R = plan_radix(LOGN, IDX, INV);
-    constexpr int P = plan_p(LOGN, IDX, INV);
-    pass_smem<(1 << LOGN), R, P, INV, T>(buf, tw + plan_tw_off(LOGN, IDX, INV), lt);
-    run_passes<LOGN, INV, IDX + 1, LAST, T>(buf, tw, lt);
-  }
 }
 
 }  // namespace s4dev

@@ -35,11 +35,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_workspace_bytes(lib):
-    # [256 status | M tan table | H M root values | H 2M spectra], each 256-aligned
+    # [256 status | H M root values | H 2M spectra], each 256-aligned
     H, L = 256, 1024
     M = 1024
-    assert s4.s4_workspace_bytes(H, 64, 1, L, 16) == 256 + 8 * M + 8 * H * M + 16 * H * M
-    assert s4.s4_workspace_bytes(3, 4, 1, 100, 1) == 256 + 1024 + 3072 + 6144  # M = 128
+    assert s4.s4_workspace_bytes(H, 64, 1, L, 16) == 256 + 8 * H * M + 16 * H * M
+    assert s4.s4_workspace_bytes(3, 4, 1, 100, 1) == 256 + 3072 + 6144  # M = 128
     for bad in [(0, 4, 1, 8, 1), (1, 0, 1, 8, 1), (1, 4, 0, 8, 1), (1, 4, 5, 8, 1), (1, 4, 1, 0, 1),
                 (1, 4, 1, 65537, 1), (1, 4, 1, 8, 0), (1, 65537, 1, 8, 1)]:
         assert s4.s4_workspace_bytes(*bad) == 0, bad
