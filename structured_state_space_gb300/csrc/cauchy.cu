@@ -14,8 +14,9 @@
 //
 // Arithmetic: s is carried as an fp32 (hi, lo) pair (tan(pi k/M) from a table
 // computed in float64 at build time, a = 2/Delta split exactly), so that the
-// difference s - lambda_j near a resonance keeps full fp32 relative accuracy.  Each pole then costs one
-// reciprocal and 4 (r+1)^2 FMAs per root.
+// difference s - lambda_j near a resonance keeps full fp32 relative accuracy.
+// Each (root, pole) then costs two adds, one FMA, one reciprocal and
+// 4 (r+1)^2 FMAs.
 #include <float.h>
 
 #include "s4_dev.cuh"
@@ -84,11 +85,16 @@ __device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
   return true;
 }
 
+// Per pole j in shared memory: Im lambda_j, (Re lambda_j)^2, then for each
+// weight w (order 0: (C~,B); 1+l: (C~,P_l); 1+r+i: (Q_i,B); 1+2r+i r+l: (Q_i,P_l))
+// the pair w and w (-Re lambda_j).  With d = s - lambda_j = -Re lambda_j + i dim,
+//   w / d = (w (-Re lambda_j) - i dim w) / |d|^2
+// costs two FMAs for the numerator and two for the accumulation.
 template <int RANK>
 struct CauchyLayout {
   static constexpr int NW = (RANK + 1) * (RANK + 1);      // weight vectors
-  static constexpr int PS = (3 + 2 * NW + 3) / 4 * 4;     // floats per pole (float4-padded)
-  // weight order: 0: (C~,B); 1+l: (C~,P_l); 1+r+i: (Q_i,B); 1+2r+i r+l: (Q_i,P_l)
+  static constexpr int PS = (2 + 4 * NW + 3) / 4 * 4;     // floats per pole (float4-padded)
+  static constexpr int JT = PS <= 48 ? 128 : 64;          // poles staged at a time
 };
 
 template <int RANK, int RPT, int T>
@@ -97,10 +103,11 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
     float2* __restrict__ Khat, int N, int logM, int logC, unsigned* __restrict__ status) {
   using Lay = CauchyLayout<RANK>;
-  constexpr int NW = Lay::NW, PS = Lay::PS, JT = 128;
+  constexpr int NW = Lay::NW, PS = Lay::PS, JT = Lay::JT;
   __shared__ __align__(16) float par[JT * PS];
   __shared__ float2 red[T / 32 + 1];
 
+  pdl_launch_dependents();  // the next kernel may start; it waits for this grid before reading
   const int h = blockIdx.x;
   const int M = 1 << logM;
   const float delta = dt[h];
@@ -144,32 +151,27 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
       float* pp = par + jj * PS;
       pp[0] = lam.y;
       pp[1] = lam.x * lam.x;
-      pp[2] = -lam.x;
+      const float nre = -lam.x;
+      auto put = [&](int widx, float2 w) {
+        pp[2 + 4 * widx] = w.x;
+        pp[3 + 4 * widx] = w.y;
+        pp[4 + 4 * widx] = w.x * nre;
+        pp[5 + 4 * widx] = w.y * nre;
+      };
       float2 w = conj_mul(c, b);
       cb = cadd(cb, w);
-      pp[3] = w.x;
-      pp[4] = w.y;
+      put(0, w);
 #pragma unroll
-      for (int l = 0; l < RANK; ++l) {
-        w = conj_mul(c, Pm[j * RANK + l]);
-        pp[3 + 2 * (1 + l)] = w.x;
-        pp[4 + 2 * (1 + l)] = w.y;
-      }
+      for (int l = 0; l < RANK; ++l) put(1 + l, conj_mul(c, Pm[j * RANK + l]));
 #pragma unroll
       for (int i = 0; i < RANK; ++i) {
         const float2 qi = Qm[j * RANK + i];
-        w = conj_mul(qi, b);
-        pp[3 + 2 * (1 + RANK + i)] = w.x;
-        pp[4 + 2 * (1 + RANK + i)] = w.y;
+        put(1 + RANK + i, conj_mul(qi, b));
 #pragma unroll
-        for (int l = 0; l < RANK; ++l) {
-          w = conj_mul(qi, Pm[j * RANK + l]);
-          pp[3 + 2 * (1 + 2 * RANK + i * RANK + l)] = w.x;
-          pp[4 + 2 * (1 + 2 * RANK + i * RANK + l)] = w.y;
-        }
+        for (int l = 0; l < RANK; ++l) put(1 + 2 * RANK + i * RANK + l, conj_mul(qi, Pm[j * RANK + l]));
       }
 #pragma unroll
-      for (int f = 3 + 2 * NW; f < PS; ++f) pp[f] = 0.f;
+      for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
     }
     __syncthreads();
 #pragma unroll 2
@@ -189,12 +191,13 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
         const float dim = (shi[rr] - pr[0]) + slo[rr];
         const float n2 = fmaf(dim, dim, pr[1]);
         const float rn = rcp_approx(n2);
-        const float er = pr[2] * rn, ei = -dim * rn;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float wx = pr[3 + 2 * w], wy = pr[4 + 2 * w];
-          acc[rr][w].x = fmaf(wx, er, fmaf(-wy, ei, acc[rr][w].x));
-          acc[rr][w].y = fmaf(wx, ei, fmaf(wy, er, acc[rr][w].y));
+          const float wx = pr[2 + 4 * w], wy = pr[3 + 4 * w];
+          const float tx = fmaf(dim, wy, pr[4 + 4 * w]);
+          const float ty = fmaf(-dim, wx, pr[5 + 4 * w]);
+          acc[rr][w].x = fmaf(rn, tx, acc[rr][w].x);
+          acc[rr][w].y = fmaf(rn, ty, acc[rr][w].y);
         }
       }
     }

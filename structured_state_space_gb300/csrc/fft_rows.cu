@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
+  pdl_launch_dependents();
+  pdl_wait();  // root values and status come from the previous kernel
   const bool zero = *((volatile const unsigned*)status) != 0u;
   const float sc = 1.f / M;
   bool fin = true;
@@ -379,7 +381,7 @@ conv_pair_kernel(
   float2* bufB = bufA + C::PADN;
   float2* const buf1[1] = {bufA};
   float2* const buf2[2] = {bufA, bufB};
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  bool zero = false, waited = false;
   const int pairs = ((batch + 1) / 2) * H;
   for (int p0 = blockIdx.x * C::ROWS; p0 < pairs; p0 += gridDim.x * C::ROWS) {
     const int p = p0 + slot;
@@ -410,6 +412,11 @@ conv_pair_kernel(
     }
     __syncthreads();
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(buf1, lt);
+    if (!waited) {  // the forward transform of u needed nothing from the previous kernel
+      pdl_wait();
+      zero = *((volatile const unsigned*)status) != 0u;
+      waited = true;
+    }
     // forward last pass; Z in natural order k = i + q NBL goes to bufB
     float2 z[PERL][RB];
 #pragma unroll
@@ -509,6 +516,25 @@ static int grid_for(KernelT k, int threads, size_t smem, int ctas_needed) {
   return ctas_needed < cap ? ctas_needed : cap;
 }
 
+// Launch with the programmatic-serialization attribute when `pdl` is set:
+// the kernel may start before the previous kernel on the stream finishes and
+// synchronises with it through pdl_wait().
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), int grid, int threads, size_t smem,
+                                    cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int LOGN>
 static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, const unsigned* st,
                                cudaStream_t s) {
@@ -550,7 +576,7 @@ static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, un
 
 template <int LOGN>
 static cudaError_t conv_launch(const float* u, const float2* K2, const float* D, float2* y, int batch,
-                               int H, int L, const unsigned* st, cudaStream_t s) {
+                               int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
   const int pairs = ((batch + 1) / 2) * H;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("conv", s);
@@ -563,7 +589,7 @@ static cudaError_t conv_launch(const float* u, const float2* K2, const float* D,
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv", s);
-    k<<<grid, C::THREADS, smem, s>>>(u, K2, D, y, batch, H, L, st);
+    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L, st);
   }
   return cudaGetLastError();
 }
@@ -579,8 +605,7 @@ static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H
   if (e != cudaSuccess) return e;
   const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
   TimedLaunch tl("kspec", s);
-  k<<<grid, C::THREADS, smem, s>>>(Khat, K, K2, H, L, scale, st);
-  return cudaGetLastError();
+  return launch_maybe_pdl(k, grid, C::THREADS, smem, s, true, Khat, K, K2, H, L, scale, st);
 }
 
 bool kspec_supported(int logM) { return logM >= 5 && logM <= 12; }
@@ -629,11 +654,11 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
 }
 
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int batch, int H, int L, const unsigned* st, cudaStream_t s) {
+                             int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
-    return conv_launch<X>(u, K2, D, y, batch, H, L, st, s);
+    return conv_launch<X>(u, K2, D, y, batch, H, L, st, s, pdl);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
     S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE

@@ -235,7 +235,8 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
     if (e == cudaSuccess)
       e = s4impl::launch_kspec_rows(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
     if (e == cudaSuccess)
-      e = s4impl::launch_conv_rows(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L, st, s);
+      e = s4impl::launch_conv_rows(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L, st, s,
+                                   /*pdl=*/true);
     return cuda_status(e);
   }
   const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);

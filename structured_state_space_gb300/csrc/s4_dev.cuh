@@ -34,6 +34,16 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
+// ---- programmatic dependent launch --------------------------------------------------
+// A kernel launched with the programmatic-serialization attribute may start
+// while the previous kernel on the stream is still running; it must call
+// pdl_wait() before it reads anything that kernel writes (a no-op for a
+// normal launch).  pdl_launch_dependents() lets the next such kernel start.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- padded shared-memory index: one spare slot per 16 entries ------------------
 // Keeps the Stockham read (stride n/R) and write (stride p) patterns free of
 // shared-memory bank conflicts for the radix plans used here.

@@ -53,13 +53,16 @@ cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
                                  cudaStream_t s);
 // Layer path: inverse transform of the root values and the kernel spectrum in
-// one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported).
+// one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported),
+// launched as a programmatic dependent of the root-value kernel.
 bool kspec_supported(int logM);
 cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
                               unsigned* st, cudaStream_t s);
 // (the row kernels pair batch rows; K2 from launch_spectrum_rows is scaled by 1/(2n))
+// `pdl`: launch as a programmatic dependent of the previous kernel (layer path).
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int batch, int H, int L, const unsigned* st, cudaStream_t s);
+                             int batch, int H, int L, const unsigned* st, cudaStream_t s,
+                             bool pdl = false);
 
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
