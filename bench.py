@@ -46,7 +46,8 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 # ---------------------------------------------------------------------------
 
 def dist_env():
-    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    from structured_state_space_gb300.multi import dist_env as _d
+    return _d()
 
 
 def read_peaks():
@@ -213,6 +214,7 @@ def run_ours(args):
 
     import structured_state_space_gb300 as s4
     from structured_state_space_gb300 import build as s4build
+    from structured_state_space_gb300 import multi
     from structured_state_space_gb300 import workloads as W
 
     rank, local_rank, world = dist_env()
@@ -274,20 +276,16 @@ def run_ours(args):
         graphs.append(g)
 
     def timed(body, k):
-        if world > 1:
-            dist.barrier()
+        # barrier + sync on both sides; the job time is the max over ranks
+        multi.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         body(k)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-            dist.barrier()
+        ms = multi.max_over_ranks(e0.elapsed_time(e1), device=dev)
+        multi.barrier()
         return ms
 
     def replay_steps(k):
@@ -389,8 +387,8 @@ def run_ours(args):
     e2e_steps_done = e2e_n
 
     samples_step = Bsz * H * L
-    value = samples_step * world * K / (ms_total / 1e3)
-    e2e_value = samples_step * world * e2e_steps_done / (ms_e2e / 1e3)
+    value = multi.job_throughput(samples_step, K, world, ms_total)
+    e2e_value = multi.job_throughput(samples_step, e2e_steps_done, world, ms_e2e)
 
     peaks, peak_src = read_peaks()
     # roofline of the dominant kernel
