@@ -53,7 +53,10 @@ typedef enum {
     S4_ERR_RESONANT_CORRECTION = 4,  /* I_r + Q^* R(z_k) P singular at some root */
     S4_ERR_NONFINITE = 5,            /* a root value or spectrum entry is inf/nan */
     S4_ERR_INVALID_STEP = 6,         /* some Delta_h <= 0 or not finite */
-    S4_ERR_CUDA = 7                  /* a CUDA runtime call or launch failed */
+    S4_ERR_CUDA = 7,                 /* a CUDA runtime call or launch failed */
+    S4_ERR_SINGULAR_BILINEAR = 8     /* G = I - (Delta/2) A not solved: some d_j = 1 - (Delta/2) lambda_j
+                                        is exactly 0 (the bordered branch, not taken on the GPU)
+                                        or I_r + (Delta/2) Q^* D^{-1} P is exactly singular */
 } s4_status;
 
 /* Bytes of scratch that s4_kernel_gen, s4_conv_fwd and s4_layer_fwd need for
@@ -140,6 +143,39 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
 #define S4_NOALLOC_SCRATCH_BYTES (8u << 20)
 s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const float* D,
                               int batch, int H, int L, s4_c32* y, void* stream);
+
+/*
+ * s4_ctilde -- form the truncated output vector from a conventional C.
+ * Page "Recurrent, LSTM, and structured state-space models": for a filter of
+ * transform length M (least power of two >= L) the output vector is
+ * C~ = (I - Abar^M)^* C; the filter procedure receives it as given data, and
+ * this entry point forms it.  Computed as C - (Abar^*)^M C with M steps of
+ * Abar^* w = 2 G^{-*} w - w (G = I - (Delta/2) A), each a rank-r Woodbury solve.
+ *   Lambda, P, Q, dt as for s4_kernel_gen; C [H][N] (input); Ctilde [H][N] (output).
+ *   N <= 256.  ws: at least 256 bytes (the status word; see s4_get_status).
+ * Device-detected statuses: S4_ERR_SINGULAR_BILINEAR, S4_ERR_INVALID_STEP (Ctilde zeros).
+ */
+s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const float* dt,
+                    const s4_c32* C, int H, int N, int r, int L, s4_c32* Ctilde,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * s4_recurrent_fwd -- the recurrent mode over L steps, for streaming inference.
+ * Page "Recurrent, LSTM, and structured state-space models", section "DPLR
+ * structured state-space parameterization", recurrent mode:
+ *     b_t = (I + (Delta/2) A) x_{t-1} + Delta B u_t,   G x_t = b_t,   y_t = C^* x_t + D u_t,
+ * G solved by the Woodbury inverse with D = diag(1 - (Delta/2) lambda_j).
+ *   Lambda, P, Q, B, dt, D as for s4_layer_fwd; C [H][N] is the conventional
+ *   output vector (not C~).  u [batch][H][L] inputs; y [batch][H][L] outputs.
+ *   x [batch][H][N]: the state x_{-1} on entry and x_{L-1} on return, so
+ *   consecutive calls continue one sequence (zeros for a fresh sequence).
+ *   N <= 256.  ws: at least 256 bytes (the status word).
+ * Device-detected statuses: S4_ERR_SINGULAR_BILINEAR, S4_ERR_INVALID_STEP (y and x zeros).
+ */
+s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
+                           const s4_c32* B, const s4_c32* C, const float* dt, const float* D,
+                           const float* u, int batch, int H, int N, int r, int L,
+                           s4_c32* x, s4_c32* y, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, then returns the device-detected status recorded in
  * `ws` by the last entry point that used it (S4_OK if none), or

@@ -37,7 +37,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "OracleStatus", "bilinear", "c_from_ctilde", "kernel_from_c", "s4_kernel",
+    "OracleStatus", "bilinear", "c_from_ctilde", "ctilde_from_c", "kernel_from_c", "s4_kernel",
     "s4_kernel_channels", "causal_conv", "causal_conv_at", "recurrence",
     "recurrent_solve_dplr", "transform_length", "radix2_dft", "dft_direct",
     "filter_root_values", "filter_kernel", "s4_layer", "cauchy_direct",
@@ -109,6 +109,15 @@ def c_from_ctilde(Abar, Ctilde, M: int):
     AM = np.linalg.matrix_power(Abar, M)
     lhs = (np.eye(N) - AM).conj().T
     return np.linalg.solve(lhs, _c(Ctilde))
+
+
+def ctilde_from_c(Abar, C, M: int):
+    """C~_M = (I - Abar^M)^* C ([RSS] truncated output vector), Abar^M by
+    repeated squaring."""
+    Abar = _c(Abar)
+    N = Abar.shape[0]
+    AM = np.linalg.matrix_power(Abar, M)
+    return (np.eye(N) - AM).conj().T @ _c(C)
 
 
 def kernel_from_c(Abar, Bbar, C, L: int):

@@ -10,6 +10,8 @@ Entry points (same names as the C ABI):
     s4_kernel_gen(Lambda, P, Q, B, Ctilde, dt, L)      -> K [H][L] complex64
     s4_conv_fwd(u, K, D)                               -> y [batch][H][L] complex64
     s4_layer_fwd(Lambda, P, Q, B, Ctilde, dt, D, u)    -> (K, y)
+    s4_ctilde(Lambda, P, Q, dt, C, L)                  -> C~ [H][N] complex64
+    s4_recurrent_fwd(Lambda, P, Q, B, C, dt, D, u, x)  -> (y, x)   (recurrent mode)
     s4_workspace_bytes(H, N, r, L, batch)
     s4_get_status(ws), s4_status_str(code)
 """
@@ -28,6 +30,7 @@ __all__ = [
 STATUS = {
     0: "S4_OK", 1: "S4_ERR_INVALID_ARG", 2: "S4_ERR_WORKSPACE", 3: "S4_ERR_RESONANT_DIAGONAL",
     4: "S4_ERR_RESONANT_CORRECTION", 5: "S4_ERR_NONFINITE", 6: "S4_ERR_INVALID_STEP", 7: "S4_ERR_CUDA",
+    8: "S4_ERR_SINGULAR_BILINEAR",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -35,7 +38,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
-    "s4_conv_fwd_noalloc",
+    "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd",
 ]
 
 
@@ -77,6 +80,10 @@ def load(path: str | None = None):
     lib.s4_timing_reset.restype = None
     lib.s4_timing_read.argtypes = [ctypes.c_char_p, i32p, f64p]
     lib.s4_timing_read.restype = i32
+    lib.s4_ctilde.argtypes = [vp] * 5 + [i32] * 4 + [vp, vp, sz, vp]
+    lib.s4_ctilde.restype = i32
+    lib.s4_recurrent_fwd.argtypes = [vp] * 8 + [i32] * 5 + [vp, vp, vp, sz, vp]
+    lib.s4_recurrent_fwd.restype = i32
     _lib = lib
     return lib
 
@@ -186,6 +193,46 @@ def s4_layer_fwd(Lambda, P, Q, B, Ctilde, dt, D, u, K=None, y=None, ws=None, str
         ws.numel(), _stream(stream))
     _check(code, "s4_layer_fwd")
     return K, y
+
+
+def s4_ctilde(Lambda, P, Q, dt, C, L, Ctilde=None, ws=None, stream=None):
+    torch = _torch()
+    H, N = Lambda.shape
+    r = P.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+    if Ctilde is None:
+        Ctilde = torch.empty((H, N), dtype=c64, device=Lambda.device)
+    if ws is None:
+        ws = torch.empty(256, dtype=torch.uint8, device=Lambda.device)
+    code = load().s4_ctilde(
+        _ptr(Lambda, c64, (H, N), "Lambda"), _ptr(P, c64, (H, N, r), "P"), _ptr(Q, c64, (H, N, r), "Q"),
+        _ptr(dt, f32, (H,), "dt"), _ptr(C, c64, (H, N), "C"), H, N, r, L,
+        _ptr(Ctilde, c64, (H, N), "Ctilde"), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _check(code, "s4_ctilde")
+    return Ctilde
+
+
+def s4_recurrent_fwd(Lambda, P, Q, B, C, dt, D, u, x=None, y=None, ws=None, stream=None):
+    """Recurrent mode over u's L steps; x (state, [batch][H][N]) is updated in place."""
+    torch = _torch()
+    H, N = Lambda.shape
+    r = P.shape[-1]
+    batch, _, L = u.shape
+    c64, f32 = torch.complex64, torch.float32
+    if x is None:
+        x = torch.zeros((batch, H, N), dtype=c64, device=u.device)
+    if y is None:
+        y = torch.empty((batch, H, L), dtype=c64, device=u.device)
+    if ws is None:
+        ws = torch.empty(256, dtype=torch.uint8, device=u.device)
+    code = load().s4_recurrent_fwd(
+        _ptr(Lambda, c64, (H, N), "Lambda"), _ptr(P, c64, (H, N, r), "P"), _ptr(Q, c64, (H, N, r), "Q"),
+        _ptr(B, c64, (H, N), "B"), _ptr(C, c64, (H, N), "C"), _ptr(dt, f32, (H,), "dt"),
+        _ptr(D, f32, (H,), "D"), _ptr(u, f32, (batch, H, L), "u"), batch, H, N, r, L,
+        _ptr(x, c64, (batch, H, N), "x"), _ptr(y, c64, (batch, H, L), "y"), ctypes.c_void_p(ws.data_ptr()),
+        ws.numel(), _stream(stream))
+    _check(code, "s4_recurrent_fwd")
+    return y, x
 
 
 def s4_get_status(ws, stream=None) -> int:

@@ -1,0 +1,348 @@
+// Recurrent mode of the bilinear-discretised DPLR model, and the formation of
+// the truncated output vector C~ from C.
+//
+// "Recurrent, LSTM, and structured state-space models", section "DPLR
+// structured state-space parameterization": with alpha = Delta/2,
+// G = I - alpha A, the recurrent mode computes b_t = (I + alpha A) x_{t-1} +
+// Delta B u_t, G x_t = b_t, y_t = C^* x_t (+ D u_t, the separate direct term);
+// the solve uses the Woodbury inverse with D = diag(d_j), d_j = 1 - alpha
+// lambda_j and the correction I_r + alpha Q^* D^{-1} P.  The truncated output
+// vector is C~ = (I - Abar^M)^* C.
+//
+// Since I + alpha A = 2I - G, one step is x_t = G^{-1}(2 x_{t-1} + Delta B u_t)
+// - x_{t-1}: one Woodbury solve, i.e. one reduction of r values over the N
+// states, plus one reduction for y_t.  Likewise Abar^* = 2 G^{-*} - I, and
+// G^* = diag(conj d_j) + alpha Q P^* has the correction W^* (W = I_r + alpha
+// Q^* D^{-1} P), so C~ = C - (Abar^*)^M C takes M solves with W^{-*}.
+//
+// One warp owns one sequence (one channel of one batch row, or one channel
+// for C~); lane l holds states j = l, l + 32, ...  W^{-1} is formed once per
+// warp.  An exactly zero d_j (the bordered branch of the pages' solver) or an
+// exactly singular W is reported as S4_ERR_SINGULAR_BILINEAR and the outputs
+// are zeros; this kernel does not take the bordered branch.
+#include <float.h>
+
+#include "s4_dev.cuh"
+#include "s4_internal.h"
+
+namespace s4dev {
+
+__device__ __forceinline__ float2 cconj(float2 a) { return make_float2(a.x, -a.y); }
+
+__device__ __forceinline__ float2 cdiv_safe(float2 a, float2 b) {  // a / b, b != 0
+  const float s = __fdiv_rn(1.f, fmaf(b.x, b.x, b.y * b.y));
+  return make_float2((a.x * b.x + a.y * b.y) * s, (a.y * b.x - a.x * b.y) * s);
+}
+
+__device__ __forceinline__ float2 warp_sum(float2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  return v;
+}
+
+// Invert an r x r complex matrix in place (Gauss-Jordan, partial pivoting).
+// Returns false on an exactly zero pivot.
+template <int R>
+__device__ bool invert_small(float2 (&A)[R][R]) {
+  float2 I[R][R];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int j = 0; j < R; ++j) I[i][j] = make_float2(i == j ? 1.f : 0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < R; ++c) {
+    int piv = c;
+    float best = fmaxf(fabsf(A[c][c].x), fabsf(A[c][c].y));
+#pragma unroll
+    for (int i = c + 1; i < R; ++i) {
+      const float m = fmaxf(fabsf(A[i][c].x), fabsf(A[i][c].y));
+      if (m > best) { best = m; piv = i; }
+    }
+    if (!(best > 0.f)) return false;
+#pragma unroll
+    for (int i = c + 1; i < R; ++i)
+      if (i == piv)
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          float2 t = A[c][j]; A[c][j] = A[i][j]; A[i][j] = t;
+          t = I[c][j]; I[c][j] = I[i][j]; I[i][j] = t;
+        }
+    const float2 inv = cdiv_safe(make_float2(1.f, 0.f), A[c][c]);
+#pragma unroll
+    for (int j = 0; j < R; ++j) { A[c][j] = cmul(A[c][j], inv); I[c][j] = cmul(I[c][j], inv); }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (i == c) continue;
+      const float2 f = A[i][c];
+#pragma unroll
+      for (int j = 0; j < R; ++j) { A[i][j] = csub(A[i][j], cmul(f, A[c][j])); I[i][j] = csub(I[i][j], cmul(f, I[c][j])); }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int j = 0; j < R; ++j) A[i][j] = I[i][j];
+  return true;
+}
+
+// Per-warp channel constants: dinv_j = 1/d_j, and W^{-1} (conjugate-transposed for C~).
+template <int RANK, int E>
+struct ChanConst {
+  float2 dinv[E];
+  float2 Winv[RANK][RANK];
+  bool ok;
+};
+
+template <int RANK, int E>
+__device__ void channel_constants(const float2* __restrict__ lam, const float2* __restrict__ Pm,
+                                  const float2* __restrict__ Qm, float alpha, int N, int lane,
+                                  ChanConst<RANK, E>& cc) {
+  bool zero_d = false;
+  float2 Wp[RANK][RANK];
+#pragma unroll
+  for (int i = 0; i < RANK; ++i)
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) Wp[i][l] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    cc.dinv[e] = make_float2(0.f, 0.f);
+    if (j < N) {
+      const float2 d = make_float2(fmaf(-alpha, lam[j].x, 1.f), -alpha * lam[j].y);
+      if (d.x == 0.f && d.y == 0.f) {
+        zero_d = true;
+        continue;
+      }
+      cc.dinv[e] = cdiv_safe(make_float2(1.f, 0.f), d);
+      // W = I + alpha Q^* D^{-1} P
+#pragma unroll
+      for (int i = 0; i < RANK; ++i) {
+        const float2 qd = cmul(cconj(Qm[(size_t)j * RANK + i]), cc.dinv[e]);
+#pragma unroll
+        for (int l = 0; l < RANK; ++l) Wp[i][l] = cadd(Wp[i][l], cmul(qd, Pm[(size_t)j * RANK + l]));
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RANK; ++i)
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) {
+      const float2 s = warp_sum(Wp[i][l]);
+      cc.Winv[i][l] = make_float2(alpha * s.x + (i == l ? 1.f : 0.f), alpha * s.y);
+    }
+  zero_d = __any_sync(0xffffffffu, zero_d);
+  cc.ok = !zero_d && invert_small<RANK>(cc.Winv);
+}
+
+// x_t = G^{-1}(2 x_{t-1} + Delta B u_t) - x_{t-1},  y_t = C^* x_t + D u_t.
+template <int RANK, int E>
+__global__ void __launch_bounds__(128) recurrent_kernel(
+    const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
+    const float2* __restrict__ Bv, const float2* __restrict__ Cv, const float* __restrict__ dt,
+    const float* __restrict__ Dskip, const float* __restrict__ u, int batch, int H, int N, int L,
+    float2* __restrict__ x, float2* __restrict__ y, unsigned* __restrict__ status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= batch * H) return;
+  const int h = warp % H;
+  const size_t pb = (size_t)h * N;
+  const float delta = dt[h];
+  const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
+  const float alpha = 0.5f * delta;
+  ChanConst<RANK, E> cc;
+  channel_constants<RANK, E>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
+  const bool ok = cc.ok && !bad;
+  float2 xs[E], eb[E], pd[E][RANK], qc[E][RANK], cc_[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    const bool in = j < N;
+    xs[e] = in ? x[(size_t)warp * N + j] : make_float2(0.f, 0.f);
+    eb[e] = in ? cscale(cmul(cc.dinv[e], Bv[pb + j]), delta) : make_float2(0.f, 0.f);  // D^{-1} Delta B
+    cc_[e] = in ? cconj(Cv[pb + j]) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) {
+      pd[e][l] = in ? cscale(cmul(cc.dinv[e], Pm[(pb + j) * RANK + l]), alpha) : make_float2(0.f, 0.f);
+      qc[e][l] = in ? cconj(Qm[(pb + j) * RANK + l]) : make_float2(0.f, 0.f);
+    }
+  }
+  const float dsk = Dskip[h];
+  const float* ur = u + (size_t)warp * L;
+  float2* yr = y + (size_t)warp * L;
+  for (int t = 0; t < L; ++t) {
+    const float ut = ur[t];
+    float2 w[E], s[RANK];
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) s[l] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {  // w = D^{-1}(2 x + Delta B u)
+      const float2 dx = cmul(cc.dinv[e], xs[e]);
+      w[e] = make_float2(fmaf(2.f, dx.x, eb[e].x * ut), fmaf(2.f, dx.y, eb[e].y * ut));
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(qc[e][l], w[e]));
+    }
+    float2 z[RANK];
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) s[l] = warp_sum(s[l]);
+#pragma unroll
+    for (int i = 0; i < RANK; ++i) {
+      z[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) z[i] = cadd(z[i], cmul(cc.Winv[i][l], s[l]));
+    }
+    float2 yp = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {  // x = w - alpha D^{-1} P z - x_prev
+      float2 v = csub(w[e], xs[e]);
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) v = csub(v, cmul(pd[e][l], z[l]));
+      xs[e] = v;
+      yp = cadd(yp, cmul(cc_[e], v));
+    }
+    yp = warp_sum(yp);
+    if (lane == 0) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    if (j < N) x[(size_t)warp * N + j] = ok ? xs[e] : make_float2(0.f, 0.f);
+  }
+  if (lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+}
+
+// C~ = C - (Abar^*)^M C with Abar^* w = 2 G^{-*} w - w.
+template <int RANK, int E>
+__global__ void __launch_bounds__(128) ctilde_kernel(
+    const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
+    const float* __restrict__ dt, const float2* __restrict__ Cv, int H, int N, int M,
+    float2* __restrict__ Ct, unsigned* __restrict__ status) {
+  const int h = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (h >= H) return;
+  const size_t pb = (size_t)h * N;
+  const float delta = dt[h];
+  const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
+  const float alpha = 0.5f * delta;
+  ChanConst<RANK, E> cc;
+  channel_constants<RANK, E>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
+  const bool ok = cc.ok && !bad;
+  // G^{-*} w = conj(D)^{-1} w - alpha conj(D)^{-1} Q W^{-*} P^* conj(D)^{-1} w
+  float2 dc[E], w[E], c0[E], qd[E][RANK], pc[E][RANK], Wh[RANK][RANK];
+#pragma unroll
+  for (int i = 0; i < RANK; ++i)
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) Wh[i][l] = cconj(cc.Winv[l][i]);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    const bool in = j < N;
+    dc[e] = cconj(cc.dinv[e]);
+    c0[e] = in ? Cv[pb + j] : make_float2(0.f, 0.f);
+    w[e] = c0[e];
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) {
+      qd[e][l] = in ? cscale(cmul(dc[e], Qm[(pb + j) * RANK + l]), alpha) : make_float2(0.f, 0.f);
+      pc[e][l] = in ? cconj(Pm[(pb + j) * RANK + l]) : make_float2(0.f, 0.f);
+    }
+  }
+  for (int it = 0; it < M; ++it) {
+    float2 v[E], s[RANK];
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) s[l] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      v[e] = cmul(dc[e], w[e]);
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(pc[e][l], v[e]));
+    }
+#pragma unroll
+    for (int l = 0; l < RANK; ++l) s[l] = warp_sum(s[l]);
+    float2 z[RANK];
+#pragma unroll
+    for (int i = 0; i < RANK; ++i) {
+      z[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) z[i] = cadd(z[i], cmul(Wh[i][l], s[l]));
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {  // w <- 2 G^{-*} w - w
+      float2 g = v[e];
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) g = csub(g, cmul(qd[e][l], z[l]));
+      w[e] = make_float2(fmaf(2.f, g.x, -w[e].x), fmaf(2.f, g.y, -w[e].y));
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    if (j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
+  }
+  if (lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+}
+
+}  // namespace s4dev
+
+namespace s4impl {
+using namespace s4dev;
+
+static int state_lanes(int N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
+
+template <int RANK, int E>
+static cudaError_t rec_launch(const float2* Lam, const float2* P, const float2* Q, const float2* B,
+                              const float2* C, const float* dt, const float* D, const float* u,
+                              int batch, int H, int N, int L, float2* x, float2* y, unsigned* st,
+                              cudaStream_t s) {
+  const long long warps = (long long)batch * H;
+  TimedLaunch tl("recurrent", s);
+  recurrent_kernel<RANK, E><<<(unsigned)((warps + 3) / 4), 128, 0, s>>>(Lam, P, Q, B, C, dt, D, u, batch,
+                                                                        H, N, L, x, y, st);
+  return cudaGetLastError();
+}
+
+template <int RANK, int E>
+static cudaError_t ct_launch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                             const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                             cudaStream_t s) {
+  TimedLaunch tl("ctilde", s);
+  ctilde_kernel<RANK, E><<<(H + 3) / 4, 128, 0, s>>>(Lam, P, Q, dt, C, H, N, M, Ct, st);
+  return cudaGetLastError();
+}
+
+#define S4_DISPATCH_RE(F, r, N, ...)                                     \
+  switch ((r) * 16 + state_lanes(N)) {                                   \
+    case 17: return F<1, 1>(__VA_ARGS__);                                \
+    case 18: return F<1, 2>(__VA_ARGS__);                                \
+    case 20: return F<1, 4>(__VA_ARGS__);                                \
+    case 24: return F<1, 8>(__VA_ARGS__);                                \
+    case 33: return F<2, 1>(__VA_ARGS__);                                \
+    case 34: return F<2, 2>(__VA_ARGS__);                                \
+    case 36: return F<2, 4>(__VA_ARGS__);                                \
+    case 40: return F<2, 8>(__VA_ARGS__);                                \
+    case 49: return F<3, 1>(__VA_ARGS__);                                \
+    case 50: return F<3, 2>(__VA_ARGS__);                                \
+    case 52: return F<3, 4>(__VA_ARGS__);                                \
+    case 56: return F<3, 8>(__VA_ARGS__);                                \
+    case 65: return F<4, 1>(__VA_ARGS__);                                \
+    case 66: return F<4, 2>(__VA_ARGS__);                                \
+    case 68: return F<4, 4>(__VA_ARGS__);                                \
+    case 72: return F<4, 8>(__VA_ARGS__);                                \
+    default: return cudaErrorInvalidValue;                               \
+  }
+
+cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
+                             const float2* C, const float* dt, const float* D, const float* u,
+                             int batch, int H, int N, int r, int L, float2* x, float2* y,
+                             unsigned* st, cudaStream_t s) {
+  S4_DISPATCH_RE(rec_launch, r, N, Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s)
+}
+
+cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                          const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
+                          cudaStream_t s) {
+  S4_DISPATCH_RE(ct_launch, r, N, Lam, P, Q, dt, C, H, N, M, Ct, st, s)
+}
+
+}  // namespace s4impl

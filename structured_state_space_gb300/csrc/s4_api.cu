@@ -244,6 +244,43 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
   return conv_impl(u, K, D, batch, H, L, y, ws, s);
 }
 
+s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const float* dt,
+                    const s4_c32* C, int H, int N, int r, int L, s4_c32* Ctilde, void* ws,
+                    size_t ws_bytes, void* stream) {
+  if (!Lambda || !P || !Q || !dt || !C || !Ctilde) return S4_ERR_INVALID_ARG;
+  if (!sizes_ok(H, N, r, L, 1) || N > 256) return S4_ERR_INVALID_ARG;
+  if (!aligned(Lambda, 8) || !aligned(P, 8) || !aligned(Q, 8) || !aligned(C, 8) || !aligned(Ctilde, 8) ||
+      !aligned(dt, 4))
+    return S4_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return S4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  return cuda_status(s4impl::launch_ctilde(
+      reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
+      reinterpret_cast<const float2*>(Q), dt, reinterpret_cast<const float2*>(C), H, N, r,
+      1 << ilog2_ceil(L), reinterpret_cast<float2*>(Ctilde), static_cast<unsigned*>(ws), s));
+}
+
+s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
+                           const s4_c32* C, const float* dt, const float* D, const float* u,
+                           int batch, int H, int N, int r, int L, s4_c32* x, s4_c32* y, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!Lambda || !P || !Q || !B || !C || !dt || !D || !u || !x || !y) return S4_ERR_INVALID_ARG;
+  if (H < 1 || N < 1 || N > 256 || r < 1 || r > kMaxR || L < 1 || batch < 1) return S4_ERR_INVALID_ARG;
+  if ((long long)batch * H > INT_MAX / 32) return S4_ERR_INVALID_ARG;
+  if (!aligned(Lambda, 8) || !aligned(P, 8) || !aligned(Q, 8) || !aligned(B, 8) || !aligned(C, 8) ||
+      !aligned(x, 8) || !aligned(y, 8) || !aligned(dt, 4) || !aligned(D, 4) || !aligned(u, 4))
+    return S4_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return S4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  return cuda_status(s4impl::launch_recurrent(
+      reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
+      reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
+      reinterpret_cast<const float2*>(C), dt, D, u, batch, H, N, r, L, reinterpret_cast<float2*>(x),
+      reinterpret_cast<float2*>(y), static_cast<unsigned*>(ws), s));
+}
+
 s4_status s4_get_status(const void* ws, void* stream) {
   if (ws == nullptr) return S4_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -253,6 +290,7 @@ s4_status s4_get_status(const void* ws, void* stream) {
   if (word & s4dev::ST_BAD_STEP) return S4_ERR_INVALID_STEP;
   if (word & s4dev::ST_RES_DIAG) return S4_ERR_RESONANT_DIAGONAL;
   if (word & s4dev::ST_RES_CORR) return S4_ERR_RESONANT_CORRECTION;
+  if (word & s4dev::ST_SINGULAR) return S4_ERR_SINGULAR_BILINEAR;
   if (word & s4dev::ST_NONFINITE) return S4_ERR_NONFINITE;
   return S4_OK;
 }
@@ -267,6 +305,7 @@ const char* s4_status_str(s4_status st) {
     case S4_ERR_NONFINITE: return "non-finite value";
     case S4_ERR_INVALID_STEP: return "step size not positive and finite";
     case S4_ERR_CUDA: return "CUDA error";
+    case S4_ERR_SINGULAR_BILINEAR: return "singular-bilinear-matrix";
   }
   return "unknown status";
 }

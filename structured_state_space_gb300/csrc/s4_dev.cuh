@@ -17,6 +17,7 @@ constexpr unsigned ST_RES_DIAG = 1u;   // s(z_k) - lambda_j == 0 (fp32)
 constexpr unsigned ST_RES_CORR = 2u;   // W(z_k) singular
 constexpr unsigned ST_NONFINITE = 4u;  // non-finite root value or spectrum
 constexpr unsigned ST_BAD_STEP = 8u;   // Delta <= 0 or not finite
+constexpr unsigned ST_SINGULAR = 16u;  // G = I - (Delta/2) A not solved (zero d_j or singular W)
 
 // ---- complex helpers ----------------------------------------------------------
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }

@@ -73,4 +73,15 @@ cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, cons
                                 float2* y, int rows, int H, int L, const unsigned* st,
                                 cudaStream_t s);
 
+// Recurrent mode over L steps from the state x (in/out), one warp per
+// (batch row, channel); N <= 256.
+cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
+                             const float2* C, const float* dt, const float* D, const float* u,
+                             int batch, int H, int N, int r, int L, float2* x, float2* y,
+                             unsigned* st, cudaStream_t s);
+// C~ = (I - Abar^M)^* C, one warp per channel; N <= 256.
+cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                          const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
+                          cudaStream_t s);
+
 }  // namespace s4impl

@@ -84,3 +84,16 @@ def test_host_argument_errors(lib):
     assert lib.s4_layer_fwd(*args, 1, 2, 4, 1, 8, _vp(A), _vp(A), _vp(A), 10, None) == 2
     # status read without a workspace
     assert lib.s4_get_status(None, None) == 2
+
+
+def test_host_argument_errors_recurrent_and_ctilde(lib):
+    A = 0x10000
+    p5 = [_vp(A)] * 5
+    assert lib.s4_ctilde(*p5, 2, 4, 1, 8, None, _vp(A), 256, None) == 1           # null output
+    assert lib.s4_ctilde(*p5, 2, 300, 1, 8, _vp(A), _vp(A), 256, None) == 1       # N > 256
+    assert lib.s4_ctilde(*p5, 2, 4, 1, 8, _vp(A), _vp(A), 64, None) == 2          # ws too small
+    p8 = [_vp(A)] * 8
+    assert lib.s4_recurrent_fwd(*p8, 1, 2, 4, 1, 8, _vp(A), None, _vp(A), 256, None) == 1
+    assert lib.s4_recurrent_fwd(*p8, 1, 2, 4, 5, 8, _vp(A), _vp(A), _vp(A), 256, None) == 1   # r > 4
+    assert lib.s4_recurrent_fwd(*p8, 1, 2, 4, 1, 8, _vp(A), _vp(A), None, 256, None) == 2
+    assert s4.s4_status_str(8) == "singular-bilinear-matrix"

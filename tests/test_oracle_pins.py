@@ -194,6 +194,20 @@ def test_generating_function_identity(N, r, L):
     assert np.linalg.norm(K_def - K_filt) <= 1e-10 * np.linalg.norm(K_def)
 
 
+@pytest.mark.parametrize("M", [1, 4, 64])
+def test_ctilde_formation_inverts_c_recovery(M):
+    # C~ formed from C, then C recovered from C~ (pinned through the
+    # generating-function identity), gives C back; and the kernel from C~
+    # equals the kernel from C by definition.
+    rng = np.random.default_rng(M + 5)
+    lam, P, Q, B, C, dt = _rand_dplr(rng, 5, 2)
+    _, Abar, Bbar = O.bilinear(lam, P, Q, B, dt)
+    Ct = O.ctilde_from_c(Abar, C, M)
+    np.testing.assert_allclose(O.c_from_ctilde(Abar, Ct, M), C, rtol=1e-10)
+    np.testing.assert_allclose(O.s4_kernel(lam, P, Q, B, Ct, dt, M), O.kernel_from_c(Abar, Bbar, C, M),
+                               rtol=1e-10, atol=1e-13)
+
+
 def test_root_value_at_minus_one_is_finite_formula():
     # z = -1: sum_j K_j (-1)^j over the full length M equals (Delta/2) C~^* B.
     rng = np.random.default_rng(9)
