@@ -120,7 +120,7 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-_FFT_FILES = ["fft_rows.cu", "s4_fft.cuh", "s4_dev.cuh", "s4_plan.cuh", "../gen_twiddles.py"]
+_FFT_FILES = ["fft_rows.cu", "s4_fft.cuh", "s4_kspec.cuh", "s4_dev.cuh", "s4_plan.cuh", "../gen_twiddles.py"]
 KERNEL_FILES = {
     "conv": _FFT_FILES,
     "cauchy": ["cauchy.cu", "s4_dev.cuh", "../gen_twiddles.py"],

@@ -16,6 +16,7 @@
 // The factor 1/2 and the inverse transform's 1/n are folded into K2.
 #include "s4_fft.cuh"
 #include "s4_internal.h"
+#include "s4_kspec.cuh"
 
 namespace s4dev {
 
@@ -236,117 +237,20 @@ template <int LOGM>
 __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
     float scale, unsigned* __restrict__ status) {
-  constexpr int LOGN = LOGM + 1;
-  using C = RowCfg<LOGN>;
+  using C = RowCfg<LOGM + 1>;
   constexpr int M = 1 << LOGM, n = C::n, T = C::T;
-  constexpr int TI = row_threads(LOGM);
-  static_assert(TI <= T, "thread split");
-  // inverse, length M
-  constexpr int NPI = plan_npass(LOGM);
-  constexpr int RI0 = plan_radix(LOGM, 0, true), RIL = plan_radix(LOGM, NPI - 1, true);
-  constexpr int NBI0 = M / RI0, PERI0 = NBI0 / TI, NBIL = M / RIL, PERIL = NBIL / TI;
-  using IXI0 = PassIdx<M, RI0, 1>;
-  using IXIL = PassIdx<M, RIL, M / RIL>;
-  using TWIL = PassTw<LOGM, NPI - 1, true>;
-  // forward, length n = 2M
-  constexpr int NPF = C::NP, RA = C::RA, RB = C::RB;
-  constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
-  using IXF0 = PassIdx<n, RA, 1>;
-  using IXFL = PassIdx<n, RB, n / RB>;
-  using TWFL = PassTw<LOGN, NPF - 1, false>;
-  static_assert(NPI >= 2 && NPF >= 2, "sizes");
   extern __shared__ float2 smem[];
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
   float2* buf = smem + slot * C::PADN;
-  float2* const bufs[1] = {buf};
   pdl_launch_dependents();
   pdl_wait();  // root values and status come from the previous kernel
   const bool zero = *((volatile const unsigned*)status) != 0u;
-  const float sc = 1.f / M;
   bool fin = true;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
     const bool act = h < H;
-    if (lt < TI) {  // inverse pass 0 (P = 1): root values -> shared
-#pragma unroll
-      for (int s = 0; s < PERI0; ++s) {
-        const int i = lt + s * TI;
-        float2 a[RI0];
-#pragma unroll
-        for (int q = 0; q < RI0; ++q)
-          a[q] = act ? Khat[(size_t)h * M + i + q * NBI0] : make_float2(0.f, 0.f);
-        dft<RI0, true>(a);
-#pragma unroll
-        for (int q = 0; q < RI0; ++q) buf[IXI0::wr(i, q)] = a[q];
-      }
-    }
-    __syncthreads();
-    passes_rows<LOGM, true, 1, NPI - 2, TI, 1>(bufs, lt);
-    float2 kv[PERIL][RIL];
-    if (lt < TI) {  // last inverse pass: K in registers
-#pragma unroll
-      for (int s = 0; s < PERIL; ++s) {
-        const int i = lt + s * TI;
-        float2 w[RIL];
-#pragma unroll
-        for (int q = 0; q < RIL; ++q) kv[s][q] = buf[IXIL::rd(i, q)];
-        TWIL::load(w, i);
-        TWIL::apply(kv[s], w);
-        dft<RIL, true>(kv[s]);
-      }
-    }
-    __syncthreads();
-    if (lt < TI) {  // K out (first L, scaled) and into shared memory, natural order
-#pragma unroll
-      for (int s = 0; s < PERIL; ++s) {
-        const int i = lt + s * TI;
-#pragma unroll
-        for (int q = 0; q < RIL; ++q) {
-          const int t = i + q * NBIL;
-          const float2 v = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(kv[s][q], sc);
-          if (act && t < L) K[(size_t)h * L + t] = v;
-          buf[pad(t)] = v;
-        }
-      }
-    }
-    __syncthreads();
-    {  // forward pass 0 of the spectrum (upper half is the zero padding)
-      float2 a[PER0][RA];
-#pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
-#pragma unroll
-        for (int q = 0; q < RA / 2; ++q) a[s][q] = buf[pad(i + q * NB0)];
-        dft<RA, false, true>(a[s]);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int s = 0; s < PER0; ++s) {
-        const int i = lt + s * T;
-#pragma unroll
-        for (int q = 0; q < RA; ++q) buf[IXF0::wr(i, q)] = a[s][q];
-      }
-      __syncthreads();
-    }
-    passes_rows<LOGN, false, 1, NPF - 2, T, 1>(bufs, lt);
-#pragma unroll
-    for (int s = 0; s < PERL; ++s) {  // last forward pass -> K2
-      const int i = lt + s * T;
-      float2 a[RB], w[RB];
-#pragma unroll
-      for (int q = 0; q < RB; ++q) a[q] = buf[IXFL::rd(i, q)];
-      TWFL::load(w, i);
-      TWFL::apply(a, w);
-      dft<RB, false>(a);
-      if (act) {
-#pragma unroll
-        for (int q = 0; q < RB; ++q) {
-          fin = fin && cfinite(a[q]);
-          K2[(size_t)h * n + i + q * NBL] = cscale(a[q], scale);
-        }
-      }
-    }
-    __syncthreads();
+    kspec_row<LOGM>(Khat + (size_t)(act ? h : 0) * M, K + (size_t)(act ? h : 0) * L,
+                    K2 + (size_t)(act ? h : 0) * n, L, scale, zero, act, buf, lt, fin);
   }
   if (!fin) atomicOr(status, ST_NONFINITE);
 }
