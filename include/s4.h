@@ -106,6 +106,20 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D,
                       void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * s4_conv_fwd_real -- real-output variant: y = Re(K) * u + D u with real y.
+ * The pages take no real part (K and y are complex); this variant serves the
+ * common layer convention that keeps only the real part of the kernel.  Its
+ * kernel spectrum is Hermitian, so two batch rows share one complex forward
+ * and one complex inverse transform, and y takes 4 bytes per sample.
+ *   u [batch][H][L] real inputs; K [H][L] complex (its real part is used);
+ *   D [H]; y [batch][H][L] real fp32 outputs.  ws as for s4_conv_fwd.
+ * Device-detected status: S4_ERR_NONFINITE (y zeros).
+ */
+s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D,
+                           int batch, int H, int L, float* y,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/*
  * s4_layer_fwd -- s4_kernel_gen followed by s4_conv_fwd on the same stream.
  * K [H][L] receives the generated kernel (caller-owned; it is also an input of
  * the convolution).  Statuses as for the two steps; a device-detected status

@@ -9,6 +9,7 @@ no fallback: if the library is missing or fails to load, these calls raise.
 Entry points (same names as the C ABI):
     s4_kernel_gen(Lambda, P, Q, B, Ctilde, dt, L)      -> K [H][L] complex64
     s4_conv_fwd(u, K, D)                               -> y [batch][H][L] complex64
+    s4_conv_fwd_real(u, K, D)                          -> y [batch][H][L] float32 (Re K)
     s4_layer_fwd(Lambda, P, Q, B, Ctilde, dt, D, u)    -> (K, y)
     s4_ctilde(Lambda, P, Q, dt, C, L)                  -> C~ [H][N] complex64
     s4_recurrent_fwd(Lambda, P, Q, B, C, dt, D, u, x)  -> (y, x)   (recurrent mode)
@@ -38,7 +39,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
-    "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd",
+    "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd", "s4_conv_fwd_real",
 ]
 
 
@@ -80,6 +81,8 @@ def load(path: str | None = None):
     lib.s4_timing_reset.restype = None
     lib.s4_timing_read.argtypes = [ctypes.c_char_p, i32p, f64p]
     lib.s4_timing_read.restype = i32
+    lib.s4_conv_fwd_real.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]
+    lib.s4_conv_fwd_real.restype = i32
     lib.s4_ctilde.argtypes = [vp] * 5 + [i32] * 4 + [vp, vp, sz, vp]
     lib.s4_ctilde.restype = i32
     lib.s4_recurrent_fwd.argtypes = [vp] * 8 + [i32] * 5 + [vp, vp, vp, sz, vp]
@@ -170,6 +173,23 @@ def s4_conv_fwd(u, K, D, y=None, ws=None, stream=None):
         batch, H, L, _ptr(y, c64, (batch, H, L), "y"), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
         _stream(stream))
     _check(code, "s4_conv_fwd")
+    return y
+
+
+def s4_conv_fwd_real(u, K, D, y=None, ws=None, stream=None):
+    """y = Re(K) * u + D u, real outputs."""
+    torch = _torch()
+    batch, H, L = u.shape
+    c64, f32 = torch.complex64, torch.float32
+    if y is None:
+        y = torch.empty((batch, H, L), dtype=f32, device=u.device)
+    if ws is None:
+        ws = workspace(H, 1, 1, L, batch, u.device)
+    code = load().s4_conv_fwd_real(
+        _ptr(u, f32, (batch, H, L), "u"), _ptr(K, c64, (H, L), "K"), _ptr(D, f32, (H,), "D"),
+        batch, H, L, _ptr(y, f32, (batch, H, L), "y"), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream(stream))
+    _check(code, "s4_conv_fwd_real")
     return y
 
 

@@ -93,7 +93,8 @@ __device__ __forceinline__ void cross_inverse(cg::cluster_group& cl, float2* buf
 // Kernel spectrum of n = 2M points per channel, blocked output order.
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
-    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, unsigned* __restrict__ status) {
+    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, int realk,
+    unsigned* __restrict__ status) {
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
@@ -113,7 +114,9 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
   const int ncl = gridDim.x / Cf::C;
   for (int h = blockIdx.x / Cf::C; h < H; h += ncl) {
     cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int, int, int t) {
-      return t < L ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+      float2 v = t < L ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+      if (realk) v.y = 0.f;
+      return v;
     });
     cl.sync();
     passes_rows<LOGM, false, 0, NP - 2, T, 1>(bufs, lt);
@@ -254,6 +257,84 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
   }
 }
 
+// Real-output convolution for long rows: two batch rows b, b+1 are the real
+// and imaginary parts of one complex row; with the spectrum of Re K (Hermitian)
+// the inverse transform gives y_b + i y_{b+1} directly.
+template <int LOGN>
+__global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_real_kernel(
+    const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
+    float* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
+  using Cf = ClusterCfg<LOGN>;
+  constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
+  constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
+  using IXL = PassIdx<m, RB, m / RB>;
+  using IXI0 = PassIdx<m, RB, 1>;
+  using TWL = PassTw<LOGM, NP - 1, false>;
+  cg::cluster_group cl = cg::this_cluster();
+  const int c = (int)cl.block_rank();
+  extern __shared__ float2 smem[];
+  float2* tw1 = smem;
+  float2* buf = tw1 + Cf::MI;
+  float2* const bufs[1] = {buf};
+  const int lt = threadIdx.x;
+  fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  __syncthreads();
+  cl.sync();
+  const float sc = 1.f / n;
+  const int ncl = gridDim.x / C;
+  const int pairs = ((batch + 1) / 2) * H;
+  for (int p = blockIdx.x / C; p < pairs; p += ncl) {
+    const int h = p % H, b0 = 2 * (p / H);
+    const bool has1 = b0 + 1 < batch;
+    const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
+    const float d = D[h];
+    float u0[Cf::PI][C / 2], u1[Cf::PI][C / 2];
+    cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int s, int q, int t) {
+      const float v0 = t < L ? u[row0 * L + t] : 0.f;
+      const float v1 = (has1 && t < L) ? u[row1 * L + t] : 0.f;
+      u0[s][q] = v0;
+      u1[s][q] = v1;
+      return make_float2(v0, v1);
+    });
+    cl.sync();
+    passes_rows<LOGM, false, 0, NP - 2, T, 1>(bufs, lt);
+    {
+      float2 a[PERL][RB];
+#pragma unroll
+      for (int s = 0; s < PERL; ++s) {
+        const int i = lt + s * T;
+        float2 w[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) a[s][q] = buf[IXL::rd(i, q)];
+        TWL::load(w, i);
+        TWL::apply(a[s], w);
+        dft<RB, false>(a[s]);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], K2[(size_t)h * n + (size_t)c * m + i + q * NBL]);
+        dft<RB, true>(a[s]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < PERL; ++s) {
+        const int i = lt + s * T;
+#pragma unroll
+        for (int q = 0; q < RB; ++q) buf[IXI0::wr(i, q)] = a[s][q];
+      }
+      __syncthreads();
+    }
+    passes_rows<LOGM, true, 1, NP - 1, T, 1>(bufs, lt);
+    cl.sync();
+    cross_inverse<LOGN, true>(cl, buf, tw1, c, lt, [&](int s, int q, int t, float2 v) {
+      if (t < L) {
+        y[row0 * L + t] = zero ? 0.f : fmaf(v.x, sc, d * u0[s][q]);
+        if (has1) y[row1 * L + t] = zero ? 0.f : fmaf(v.y, sc, d * u1[s][q]);
+      }
+    });
+    cl.sync();
+  }
+}
+
 }  // namespace s4dev
 
 namespace s4impl {
@@ -297,11 +378,34 @@ static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, const un
 }
 
 template <int LOGN>
-static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsigned* st, cudaStream_t s) {
+static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsigned* st, cudaStream_t s,
+                               bool realk) {
   using Cf = ClusterCfg<LOGN>;
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(spectrum_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "spectrum", s, K, K2,
-                          H, L, st);
+                          H, L, realk ? 1 : 0, st);
+}
+
+template <int LOGN>
+static cudaError_t conv_real_cl(const float* u, const float2* K2, const float* D, float* y, int batch,
+                                int H, int L, const unsigned* st, cudaStream_t s) {
+  using Cf = ClusterCfg<LOGN>;
+  const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
+  const int pairs = ((batch + 1) / 2) * H;
+  return launch_clustered(conv_cluster_real_kernel<LOGN>, Cf::C, Cf::T, smem, pairs, "conv_real", s, u,
+                          K2, D, y, batch, H, L, st);
+}
+
+cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2, const float* D,
+                                     float* y, int batch, int H, int L, const unsigned* st,
+                                     cudaStream_t s) {
+  switch (logn) {
+    case 14: return conv_real_cl<14>(u, K2, D, y, batch, H, L, st, s);
+    case 15: return conv_real_cl<15>(u, K2, D, y, batch, H, L, st, s);
+    case 16: return conv_real_cl<16>(u, K2, D, y, batch, H, L, st, s);
+    case 17: return conv_real_cl<17>(u, K2, D, y, batch, H, L, st, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int LOGN>
@@ -323,12 +427,12 @@ cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, 
 }
 
 cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
-                                    unsigned* st, cudaStream_t s) {
+                                    unsigned* st, cudaStream_t s, bool realk) {
   switch (logn) {
-    case 14: return spectrum_cl<14>(K, K2, H, L, st, s);
-    case 15: return spectrum_cl<15>(K, K2, H, L, st, s);
-    case 16: return spectrum_cl<16>(K, K2, H, L, st, s);
-    case 17: return spectrum_cl<17>(K, K2, H, L, st, s);
+    case 14: return spectrum_cl<14>(K, K2, H, L, st, s, realk);
+    case 15: return spectrum_cl<15>(K, K2, H, L, st, s, realk);
+    case 16: return spectrum_cl<16>(K, K2, H, L, st, s, realk);
+    case 17: return spectrum_cl<17>(K, K2, H, L, st, s, realk);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,13 +44,17 @@ __global__ void __launch_bounds__(128) ifft_small_kernel(const float2* __restric
 template <int LOGN>
 __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __restrict__ K,
                                                              float2* __restrict__ K2, int H, int L,
-                                                             float scale, unsigned* __restrict__ status) {
+                                                             float scale, int realk,
+                                                             unsigned* __restrict__ status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
   const int h = blockIdx.x * 128 + threadIdx.x;
   if (h >= H) return;
   float2 a[n];
 #pragma unroll
-  for (int q = 0; q < n / 2; ++q) a[q] = q < L ? K[(size_t)h * L + q] : make_float2(0.f, 0.f);
+  for (int q = 0; q < n / 2; ++q) {
+    a[q] = q < L ? K[(size_t)h * L + q] : make_float2(0.f, 0.f);
+    if (realk) a[q].y = 0.f;
+  }
   dft<n, false, true>(a);
   bool fin = true;
 #pragma unroll
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
 // Spectrum of each channel's kernel zero-padded to n = 2M, natural order, times `scale`.
 template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
-    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale,
+    const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale, int realk,
     unsigned* __restrict__ status) {
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
         a[q] = (act && t < L) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+        if (realk) a[q].y = 0.f;
       }
       dft<RA, false, true>(a);
 #pragma unroll
@@ -396,6 +401,136 @@ conv_pair_kernel(
   }
 }
 
+// Real-output convolution y = Re(K) * u + D u.  K2 = FFT_n(Re K zero-padded)/n
+// is Hermitian, so with z = u_b + i u_{b+1} the product Z K2 transforms back
+// to y_b + i y_{b+1}: one forward and one inverse transform per pair of rows.
+template <int LOGN>
+__global__ void __launch_bounds__(128) conv_real_small_kernel(const float* __restrict__ u,
+                                                              const float2* __restrict__ K2,
+                                                              const float* __restrict__ D,
+                                                              float* __restrict__ y, int batch, int H,
+                                                              int L, const unsigned* __restrict__ status) {
+  constexpr int n = 1 << LOGN;
+  const int pairs = ((batch + 1) / 2) * H;
+  const int p = blockIdx.x * 128 + threadIdx.x;
+  if (p >= pairs) return;
+  const int h = p % H, b0 = 2 * (p / H);
+  const bool has1 = b0 + 1 < batch;
+  const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  float u0[n / 2], u1[n / 2];
+  float2 z[n];
+#pragma unroll
+  for (int q = 0; q < n / 2; ++q) {
+    u0[q] = q < L ? u[row0 * L + q] : 0.f;
+    u1[q] = (has1 && q < L) ? u[row1 * L + q] : 0.f;
+    z[q] = make_float2(u0[q], u1[q]);
+  }
+  dft<n, false, true>(z);
+#pragma unroll
+  for (int k = 0; k < n; ++k) z[k] = cmul(z[k], K2[(size_t)h * n + k]);
+  dft<n, true, false, true>(z);
+  const float d = D[h];
+#pragma unroll
+  for (int q = 0; q < n / 2; ++q) {
+    if (q < L) {
+      y[row0 * L + q] = zero ? 0.f : fmaf(d, u0[q], z[q].x);
+      if (has1) y[row1 * L + q] = zero ? 0.f : fmaf(d, u1[q], z[q].y);
+    }
+  }
+}
+
+template <int LOGN>
+__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN>::THREADS))
+conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2,
+                      const float* __restrict__ D, float* __restrict__ y, int batch, int H, int L,
+                      const unsigned* __restrict__ status) {
+  using C = RowCfg<LOGN>;
+  constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
+  constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
+  using IXF0 = PassIdx<n, RA, 1>;
+  using IXFL = PassIdx<n, RB, n / RB>;
+  using IXI0 = PassIdx<n, RB, 1>;
+  using IXIL = PassIdx<n, RA, n / RA>;
+  using TWFL = PassTw<LOGN, NP - 1, false>;
+  using TWIL = PassTw<LOGN, NP - 1, true>;
+  extern __shared__ float2 smem[];
+  const int slot = threadIdx.x / T, lt = threadIdx.x % T;
+  float2* buf = smem + slot * C::PADN;
+  float2* const bufs[1] = {buf};
+  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const int pairs = ((batch + 1) / 2) * H;
+  for (int p0 = blockIdx.x * C::ROWS; p0 < pairs; p0 += gridDim.x * C::ROWS) {
+    const int p = p0 + slot;
+    const bool act = p < pairs;
+    const int h = act ? p % H : 0;
+    const int b0 = act ? 2 * (p / H) : 0;
+    const bool has1 = act && b0 + 1 < batch;
+    const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
+    const float d = act ? D[h] : 0.f;
+    float u0[PER0][RA / 2], u1[PER0][RA / 2];
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {  // forward pass 0: z = u_b + i u_{b+1}, zero-padded
+      const int i = lt + s * T;
+      float2 a[RA];
+#pragma unroll
+      for (int q = 0; q < RA / 2; ++q) {
+        const int t = i + q * NB0;
+        u0[s][q] = (act && t < L) ? u[row0 * L + t] : 0.f;
+        u1[s][q] = (has1 && t < L) ? u[row1 * L + t] : 0.f;
+        a[q] = make_float2(u0[s][q], u1[s][q]);
+      }
+      dft<RA, false, true>(a);
+#pragma unroll
+      for (int q = 0; q < RA; ++q) buf[IXF0::wr(i, q)] = a[q];
+    }
+    __syncthreads();
+    passes_rows<LOGN, false, 1, NP - 2, T, 1>(bufs, lt);
+    float2 a[PERL][RB];
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {  // last forward pass, product, first inverse pass
+      const int i = lt + s * T;
+      float2 w[RB];
+#pragma unroll
+      for (int q = 0; q < RB; ++q) a[s][q] = buf[IXFL::rd(i, q)];
+      TWFL::load(w, i);
+      TWFL::apply(a[s], w);
+      dft<RB, false>(a[s]);
+#pragma unroll
+      for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], __ldg(K2 + (size_t)h * n + i + q * NBL));
+      dft<RB, true>(a[s]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+#pragma unroll
+      for (int q = 0; q < RB; ++q) buf[IXI0::wr(i, q)] = a[s][q];
+    }
+    __syncthreads();
+    passes_rows<LOGN, true, 1, NP - 2, T, 1>(bufs, lt);
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {  // last inverse pass: y_b = Re, y_{b+1} = Im
+      const int i = lt + s * T;
+      float2 c[RA], w[RA];
+#pragma unroll
+      for (int q = 0; q < RA; ++q) c[q] = buf[IXIL::rd(i, q)];
+      TWIL::load(w, i);
+      TWIL::apply(c, w);
+      dft<RA, true, false, true>(c);
+#pragma unroll
+      for (int q = 0; q < RA / 2; ++q) {
+        const int t = i + q * NB0;
+        if (t < L) {
+          if (act) __stcs(y + row0 * L + t, zero ? 0.f : fmaf(d, u0[s][q], c[q].x));
+          if (has1) __stcs(y + row1 * L + t, zero ? 0.f : fmaf(d, u1[s][q], c[q].y));
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace s4dev
 
 // ----------------------------------------------------------------------------
@@ -460,11 +595,13 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, cons
 
 template <int LOGN>
 static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, unsigned* st,
-                                   cudaStream_t s) {
-  const float scale = 1.f / (float)(2 << LOGN);  // 1/(2n): pair split and inverse scaling
+                                   cudaStream_t s, bool realk) {
+  // 1/(2n): pair split and inverse scaling; 1/n for the real-kernel variant (no split)
+  const float scale = realk ? 1.f / (float)(1 << LOGN) : 1.f / (float)(2 << LOGN);
+  const int rk = realk ? 1 : 0;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("spectrum", s);
-    spectrum_small_kernel<LOGN><<<(H + 127) / 128, 128, 0, s>>>(K, K2, H, L, scale, st);
+    spectrum_small_kernel<LOGN><<<(H + 127) / 128, 128, 0, s>>>(K, K2, H, L, scale, rk, st);
   } else {
     using C = RowCfg<LOGN>;
     const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
@@ -473,7 +610,7 @@ static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, un
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("spectrum", s);
-    k<<<grid, C::THREADS, smem, s>>>(K, K2, H, L, scale, st);
+    k<<<grid, C::THREADS, smem, s>>>(K, K2, H, L, scale, rk, st);
   }
   return cudaGetLastError();
 }
@@ -529,6 +666,40 @@ cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K
   }
 }
 
+template <int LOGN>
+static cudaError_t conv_real_launch(const float* u, const float2* K2, const float* D, float* y,
+                                    int batch, int H, int L, const unsigned* st, cudaStream_t s) {
+  const int pairs = ((batch + 1) / 2) * H;
+  if constexpr (LOGN <= 4) {
+    TimedLaunch tl("conv_real", s);
+    conv_real_small_kernel<LOGN><<<(pairs + 127) / 128, 128, 0, s>>>(u, K2, D, y, batch, H, L, st);
+  } else {
+    using C = RowCfg<LOGN>;
+    const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
+    auto k = conv_real_pair_kernel<LOGN>;
+    cudaError_t e = prepare(k, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
+    TimedLaunch tl("conv_real", s);
+    k<<<grid, C::THREADS, smem, s>>>(u, K2, D, y, batch, H, L, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
+                                  int batch, int H, int L, const unsigned* st, cudaStream_t s) {
+  switch (logn) {
+#define S4_CASE(X) \
+  case X:          \
+    return conv_real_launch<X>(u, K2, D, y, batch, H, L, st, s);
+    S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
+    S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
+#undef S4_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
                              const unsigned* st, cudaStream_t s) {
   switch (logM) {
@@ -544,11 +715,11 @@ cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int
 }
 
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool realk) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
-    return spectrum_launch<X>(K, K2, H, L, st, s);
+    return spectrum_launch<X>(K, K2, H, L, st, s, realk);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
     S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE

@@ -208,6 +208,32 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch
   return conv_impl(u, K, D, batch, H, L, y, ws, s);
 }
 
+s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
+                           float* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!u || !K || !D || !y) return S4_ERR_INVALID_ARG;
+  if (!sizes_ok(H, 1, 1, L, batch)) return S4_ERR_INVALID_ARG;
+  if (!aligned(u, 16) || !aligned(K, 16) || !aligned(D, 4) || !aligned(y, 16)) return S4_ERR_INVALID_ARG;
+  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  if (wst != S4_OK) return wst;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  using namespace s4impl;
+  const int logn = ilog2_ceil(L) + 1;
+  char* w = static_cast<char*>(ws);
+  unsigned* st = reinterpret_cast<unsigned*>(w);
+  float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L).k2);
+  const float2* Kf = reinterpret_cast<const float2*>(K);
+  cudaError_t e;
+  if (logn <= kMaxLogConvRow) {
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true);
+    if (e == cudaSuccess) e = launch_conv_real_rows(logn, u, k2, D, y, batch, H, L, st, s);
+  } else {
+    e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s, /*realk=*/true);
+    if (e == cudaSuccess) e = launch_conv_real_cluster(logn, u, k2, D, y, batch, H, L, st, s);
+  }
+  return cuda_status(e);
+}
+
 s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
                        const s4_c32* Ctilde, const float* dt, const float* D, const float* u,
                        int batch, int H, int N, int r, int L, s4_c32* K, s4_c32* y, void* ws,

@@ -50,8 +50,10 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
 // Single-CTA row transforms (log sizes up to kMaxLogRowCta).
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
                              const unsigned* st, cudaStream_t s);
+// realk: the spectrum of Re K (real-output convolution), scaled by 1/n
+// instead of 1/(2n).
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool realk = false);
 // Layer path: inverse transform of the root values and the kernel spectrum in
 // one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported),
 // launched as a programmatic dependent of the root-value kernel.
@@ -68,7 +70,7 @@ cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const f
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
                                 const unsigned* st, cudaStream_t s);
 cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
-                                    unsigned* st, cudaStream_t s);
+                                    unsigned* st, cudaStream_t s, bool realk = false);
 cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, const float* D,
                                 float2* y, int rows, int H, int L, const unsigned* st,
                                 cudaStream_t s);
@@ -83,5 +85,13 @@ cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                           const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
                           cudaStream_t s);
+
+// Real-output convolution y = Re(K) * u + D u (real y), two batch rows per
+// complex transform; K2 from the spectrum launchers with realk = true.
+cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
+                                  int batch, int H, int L, const unsigned* st, cudaStream_t s);
+cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2, const float* D,
+                                     float* y, int batch, int H, int L, const unsigned* st,
+                                     cudaStream_t s);
 
 }  // namespace s4impl

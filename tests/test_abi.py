@@ -97,3 +97,10 @@ def test_host_argument_errors_recurrent_and_ctilde(lib):
     assert lib.s4_recurrent_fwd(*p8, 1, 2, 4, 5, 8, _vp(A), _vp(A), _vp(A), 256, None) == 1   # r > 4
     assert lib.s4_recurrent_fwd(*p8, 1, 2, 4, 1, 8, _vp(A), _vp(A), None, 256, None) == 2
     assert s4.s4_status_str(8) == "singular-bilinear-matrix"
+
+
+def test_host_argument_errors_conv_real(lib):
+    A = 0x10000
+    assert lib.s4_conv_fwd_real(None, _vp(A), _vp(A), 1, 2, 8, _vp(A), _vp(A), 1 << 20, None) == 1
+    assert lib.s4_conv_fwd_real(_vp(A), _vp(A), _vp(A), 1, 2, 8, _vp(A + 4), _vp(A), 1 << 20, None) == 1
+    assert lib.s4_conv_fwd_real(_vp(A), _vp(A), _vp(A), 1, 2, 8, _vp(A), _vp(A), 100, None) == 2

@@ -224,3 +224,24 @@ def test_timing_hooks_count_launches():
     finally:
         s4.timing.enable(False)
         s4.timing.reset()
+
+
+@pytest.mark.parametrize("H,L,batch", [(3, 1, 3), (2, 3, 1), (5, 16, 3), (4, 100, 2), (6, 1024, 5),
+                                       (3, 5000, 3), (2, 16384, 3), (2, 40000, 1)])
+def test_conv_real_matches_oracle(H, L, batch):
+    # y = Re(K) * u + D u with real outputs
+    rng = np.random.default_rng(H * 1000 + L)
+    u = rng.standard_normal((batch, H, L)).astype(np.float32)
+    K = ((rng.standard_normal((H, L)) + 1j * rng.standard_normal((H, L))) * 0.05).astype(np.complex64)
+    D = rng.standard_normal(H).astype(np.float32)
+    y = s4.s4_conv_fwd_real(torch.from_numpy(u).cuda(), torch.from_numpy(K).cuda(),
+                            torch.from_numpy(D).cuda()).cpu().numpy()
+    assert y.dtype == np.float32
+    Kr = K.real.astype(np.float64)
+    if L <= 20000:
+        ref = np.stack([[O.causal_conv(Kr[h], u[b, h], D[h]).real for h in range(H)] for b in range(batch)])
+        check_y(y, ref, f"real L{L}")
+    else:
+        ts = [0, 1, L // 2, L - 1]
+        ref = np.array([[O.causal_conv_at(Kr[h], u[b, h], D[h], ts).real for h in range(H)] for b in range(batch)])
+        check_y(y[:, :, ts], ref, f"real L{L}")
