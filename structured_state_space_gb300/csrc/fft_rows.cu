@@ -268,8 +268,33 @@ __host__ __device__ constexpr int conv_min_blocks(int logn, int threads) {
   return (logn >= 13 || threads >= 512) ? 1 : 512 / threads;
 }
 
+// Butterfly index of slot `sl` of the last forward pass (and the first inverse
+// pass) of a row.  With an even number of slots per thread, slot 2s takes
+// butterfly s T + lt and slot 2s+1 its mirror NBL - s T - lt (thread 0 pairs
+// the two self-mirrored butterflies 0 and NBL/2), so that every thread holds
+// both bins k and n - k of the spectrum; otherwise slot sl is lt + sl T.
+template <int T, int NBL, int PERL>
+__device__ __forceinline__ int last_bfly(int sl, int lt) {
+  if constexpr (PERL % 2 != 0) {
+    return lt + sl * T;
+  } else {
+    const int s = sl >> 1;
+    if ((sl & 1) == 0) return s * T + lt;
+    return (s == 0 && lt == 0) ? NBL / 2 : NBL - s * T - lt;
+  }
+}
+
+// Spectra of the two real rows of z = u_b + i u_{b+1} times the kernel
+// spectrum kv (already holding the skip term): 2 U_b kv and 2 U_{b+1} kv.
+__device__ __forceinline__ void split_mul(float2 zk, float2 zp, float2 kv, float2& a0, float2& a1) {
+  a0 = cmul(make_float2(zk.x + zp.x, zk.y - zp.y), kv);
+  a1 = cmul(make_float2(zk.y + zp.y, zp.x - zk.x), kv);
+}
+
 // Fused causal convolution, two batch rows (b, b+1) of one channel per row
-// group; K2 is the channel spectrum scaled by 1/(2n).
+// group; K2 is the channel spectrum scaled by 1/(2n).  The skip term D u is
+// the convolution with D times the unit impulse, whose spectrum is D in every
+// bin, so it enters as D/(2n) added to each K2 bin.
 template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN>::THREADS))
 conv_pair_kernel(
@@ -278,6 +303,7 @@ conv_pair_kernel(
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
+  constexpr bool MIRROR = PERL % 2 == 0;
   using IXF0 = PassIdx<n, RA, 1>;        // forward pass 0 writes
   using IXFL = PassIdx<n, RB, n / RB>;   // forward last pass reads
   using IXI0 = PassIdx<n, RB, 1>;        // inverse pass 0 writes
@@ -299,8 +325,8 @@ conv_pair_kernel(
     const int b0 = act ? 2 * (p / H) : 0;
     const bool has1 = act && b0 + 1 < batch;
     const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
-    const float d = act ? D[h] : 0.f;
-    float u0[PER0][RA / 2], u1[PER0][RA / 2];
+    const float dk = act ? D[h] * (0.5f / n) : 0.f;
+    const float2* K2h = K2 + (size_t)h * n;
     // forward pass 0: z = u_b + i u_{b+1}, zero-padded, global -> shared
 #pragma unroll
     for (int s = 0; s < PER0; ++s) {
@@ -309,11 +335,7 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
-        const float x0 = (act && t < L) ? u[row0 * L + t] : 0.f;
-        const float x1 = (has1 && t < L) ? u[row1 * L + t] : 0.f;
-        u0[s][q] = x0;
-        u1[s][q] = x1;
-        a[q] = make_float2(x0, x1);
+        a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
       }
       dft<RA, false, true>(a);
 #pragma unroll
@@ -326,51 +348,113 @@ conv_pair_kernel(
       zero = *((volatile const unsigned*)status) != 0u;
       waited = true;
     }
-    // forward last pass; Z in natural order k = i + q NBL goes to bufB
+    // forward last pass: Z in natural order, bin i + q NBL of butterfly i
     float2 z[PERL][RB];
 #pragma unroll
-    for (int s = 0; s < PERL; ++s) {
-      const int i = lt + s * T;
+    for (int sl = 0; sl < PERL; ++sl) {
+      const int i = last_bfly<T, NBL, PERL>(sl, lt);
       float2 w[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) z[s][q] = bufA[IXFL::rd(i, q)];
+      for (int q = 0; q < RB; ++q) z[sl][q] = bufA[IXFL::rd(i, q)];
       TWFL::load(w, i);
-      TWFL::apply(z[s], w);
-      dft<RB, false>(z[s]);
-#pragma unroll
-      for (int q = 0; q < RB; ++q) bufB[IXFL::rd(i, q)] = z[s][q];
+      TWFL::apply(z[sl], w);
+      dft<RB, false>(z[sl]);
     }
-    __syncthreads();
-    // split the two spectra, multiply by K2, first inverse pass (P = 1) in registers
-    float2 a0[PERL][RB], a1[PERL][RB];
+    // split the two spectra, multiply by K2 + D/(2n), first inverse pass (P = 1)
+    // in registers; row b+1 goes to bufB at once (unused since the last
+    // iteration), row b to bufA after every thread has read its last pass.
+    float2 (&a0)[PERL][RB] = z;  // row b's products replace Z in place
+    if constexpr (MIRROR) {
 #pragma unroll
-    for (int s = 0; s < PERL; ++s) {
-      const int i = lt + s * T;
+      for (int s = 0; s < PERL / 2; ++s) {
+        const int iA = last_bfly<T, NBL, PERL>(2 * s, lt), iB = last_bfly<T, NBL, PERL>(2 * s + 1, lt);
+        float2 kA[RB], kB[RB], a1A[RB], a1B[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) {
-        const int k = i + q * NBL;
-        const float2 zp = bufB[pad((n - k) & (n - 1))];
-        const float2 kv = __ldg(K2 + (size_t)h * n + k);
-        const float2 zk = z[s][q];
-        a0[s][q] = cmul(make_float2(zk.x + zp.x, zk.y - zp.y), kv);
-        a1[s][q] = cmul(make_float2(zk.y + zp.y, zp.x - zk.x), kv);
+        for (int q = 0; q < RB; ++q) {
+          kA[q] = __ldg(K2h + iA + q * NBL);
+          kB[q] = __ldg(K2h + iB + q * NBL);
+          kA[q].x += dk;
+          kB[q].x += dk;
+        }
+        float2* zA = z[2 * s];
+        float2* zB = z[2 * s + 1];
+        if (s == 0 && lt == 0) {
+          // butterflies 0 and NBL/2 are their own mirrors: bin q of 0 pairs
+          // with bin -q mod RB, bin q of NBL/2 with bin RB-1-q
+#pragma unroll
+          for (int q = 0; q <= RB / 2; ++q) {
+            const int qm = (RB - q) & (RB - 1);
+            const float2 zk = zA[q], zm = zA[qm];
+            split_mul(zk, zm, kA[q], zA[q], a1A[q]);
+            if (qm != q) split_mul(zm, zk, kA[qm], zA[qm], a1A[qm]);
+          }
+#pragma unroll
+          for (int q = 0; q < RB / 2; ++q) {
+            const int qm = RB - 1 - q;
+            const float2 zk = zB[q], zm = zB[qm];
+            split_mul(zk, zm, kB[q], zB[q], a1B[q]);
+            split_mul(zm, zk, kB[qm], zB[qm], a1B[qm]);
+          }
+        } else {  // bin q of iA pairs with bin RB-1-q of iB
+#pragma unroll
+          for (int q = 0; q < RB; ++q) {
+            const int qm = RB - 1 - q;
+            const float2 zk = zA[q], zm = zB[qm];
+            split_mul(zk, zm, kA[q], zA[q], a1A[q]);
+            split_mul(zm, zk, kB[qm], zB[qm], a1B[qm]);
+          }
+        }
+        dft<RB, true>(a1A);
+        dft<RB, true>(a1B);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          bufB[IXI0::wr(iA, q)] = a1A[q];
+          bufB[IXI0::wr(iB, q)] = a1B[q];
+        }
+        dft<RB, true>(zA);
+        dft<RB, true>(zB);
       }
-      dft<RB, true>(a0[s]);
-      dft<RB, true>(a1[s]);
+      __syncthreads();
+    } else {
+      // one butterfly per thread: the mirror bins sit in another thread
+#pragma unroll
+      for (int sl = 0; sl < PERL; ++sl) {
+        const int i = last_bfly<T, NBL, PERL>(sl, lt);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) bufB[IXFL::rd(i, q)] = z[sl][q];
+      }
+      __syncthreads();
+      float2 a1[PERL][RB];
+#pragma unroll
+      for (int sl = 0; sl < PERL; ++sl) {
+        const int i = last_bfly<T, NBL, PERL>(sl, lt);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int k = i + q * NBL;
+          float2 kv = __ldg(K2h + k);
+          kv.x += dk;
+          split_mul(z[sl][q], bufB[pad((n - k) & (n - 1))], kv, a0[sl][q], a1[sl][q]);
+        }
+        dft<RB, true>(a0[sl]);
+        dft<RB, true>(a1[sl]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int sl = 0; sl < PERL; ++sl) {
+        const int i = last_bfly<T, NBL, PERL>(sl, lt);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) bufB[IXI0::wr(i, q)] = a1[sl][q];
+      }
     }
-    __syncthreads();
 #pragma unroll
-    for (int s = 0; s < PERL; ++s) {
-      const int i = lt + s * T;
+    for (int sl = 0; sl < PERL; ++sl) {
+      const int i = last_bfly<T, NBL, PERL>(sl, lt);
 #pragma unroll
-      for (int q = 0; q < RB; ++q) {
-        bufA[IXI0::wr(i, q)] = a0[s][q];
-        bufB[IXI0::wr(i, q)] = a1[s][q];
-      }
+      for (int q = 0; q < RB; ++q) bufA[IXI0::wr(i, q)] = a0[sl][q];
     }
     __syncthreads();
     passes_rows<LOGN, true, 1, NP - 2, T, 2>(buf2, lt);
-    // last inverse pass: first L outputs of both rows + D u
+    // last inverse pass: first L outputs of both rows
 #pragma unroll
     for (int s = 0; s < PER0; ++s) {
       const int i = lt + s * T;
@@ -389,11 +473,8 @@ conv_pair_kernel(
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
         if (t < L) {
-          const float x0 = u0[s][q], x1 = u1[s][q];
-          if (act)
-            __stcs(y + row0 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, x0, c0[q].x), c0[q].y));
-          if (has1)
-            __stcs(y + row1 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(fmaf(d, x1, c1[q].x), c1[q].y));
+          if (act) __stcs(y + row0 * L + t, zero ? make_float2(0.f, 0.f) : c0[q]);
+          if (has1) __stcs(y + row1 * L + t, zero ? make_float2(0.f, 0.f) : c1[q]);
         }
       }
     }
@@ -404,6 +485,8 @@ conv_pair_kernel(
 // Real-output convolution y = Re(K) * u + D u.  K2 = FFT_n(Re K zero-padded)/n
 // is Hermitian, so with z = u_b + i u_{b+1} the product Z K2 transforms back
 // to y_b + i y_{b+1}: one forward and one inverse transform per pair of rows.
+// The row kernel adds the skip term as D/n to every K2 bin (the spectrum of
+// D times the unit impulse).
 template <int LOGN>
 __global__ void __launch_bounds__(128) conv_real_small_kernel(const float* __restrict__ u,
                                                               const float2* __restrict__ K2,
@@ -467,8 +550,7 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
     const int b0 = act ? 2 * (p / H) : 0;
     const bool has1 = act && b0 + 1 < batch;
     const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
-    const float d = act ? D[h] : 0.f;
-    float u0[PER0][RA / 2], u1[PER0][RA / 2];
+    const float dk = act ? D[h] * (1.f / n) : 0.f;  // skip term: D/n in every bin
 #pragma unroll
     for (int s = 0; s < PER0; ++s) {  // forward pass 0: z = u_b + i u_{b+1}, zero-padded
       const int i = lt + s * T;
@@ -476,9 +558,7 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
-        u0[s][q] = (act && t < L) ? u[row0 * L + t] : 0.f;
-        u1[s][q] = (has1 && t < L) ? u[row1 * L + t] : 0.f;
-        a[q] = make_float2(u0[s][q], u1[s][q]);
+        a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
       }
       dft<RA, false, true>(a);
 #pragma unroll
@@ -497,7 +577,11 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
       TWFL::apply(a[s], w);
       dft<RB, false>(a[s]);
 #pragma unroll
-      for (int q = 0; q < RB; ++q) a[s][q] = cmul(a[s][q], __ldg(K2 + (size_t)h * n + i + q * NBL));
+      for (int q = 0; q < RB; ++q) {
+        float2 kv = __ldg(K2 + (size_t)h * n + i + q * NBL);
+        kv.x += dk;
+        a[s][q] = cmul(a[s][q], kv);
+      }
       dft<RB, true>(a[s]);
     }
     __syncthreads();
@@ -522,8 +606,8 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
         if (t < L) {
-          if (act) __stcs(y + row0 * L + t, zero ? 0.f : fmaf(d, u0[s][q], c[q].x));
-          if (has1) __stcs(y + row1 * L + t, zero ? 0.f : fmaf(d, u1[s][q], c[q].y));
+          if (act) __stcs(y + row0 * L + t, zero ? 0.f : c[q].x);
+          if (has1) __stcs(y + row1 * L + t, zero ? 0.f : c[q].y);
         }
       }
     }

@@ -43,10 +43,10 @@ struct PassTw {
   // w[q] = w^(k q) for q = 1..R-1
   __device__ __forceinline__ static void load(float2 (&w)[R], int k) {
     if constexpr (ROWS) {
-      const float4* row = reinterpret_cast<const float4*>(table() + k * tw_row_stride(R));
+      const float4* col = reinterpret_cast<const float4*>(table()) + k;
 #pragma unroll
       for (int v = 0; v < R / 2; ++v) {
-        const float4 t = __ldg(row + v);
+        const float4 t = __ldg(col + v * P);
         w[1 + 2 * v] = make_float2(t.x, t.y);
         if (2 + 2 * v < R) w[2 + 2 * v] = make_float2(t.z, t.w);
       }

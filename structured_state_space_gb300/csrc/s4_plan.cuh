@@ -30,17 +30,16 @@ __host__ __device__ constexpr int plan_p(int logn, int idx, bool inv) {
 }
 
 // ---- static twiddle tables (generated at build time, see gen_twiddles.py) ----
-// Pass idx >= 1 of a plan either reads a full row of its R-1 factors
-// w^(k q) ("rows": P <= 256, R > 2; row stride 18/10/6 entries for R =
-// 16/8/4) or the single base factor w^k from which it builds the powers.
-__host__ __device__ constexpr int tw_row_stride(int R) {
-  return R == 16 ? 18 : (R == 8 ? 10 : (R == 4 ? 6 : 2));
-}
+// Pass idx >= 1 of a plan either reads its R-1 factors w^(k q) from a
+// column-major block ("rows": P <= 256, R > 2; float4 v of butterfly k,
+// holding w^(k(2v+1)) and w^(k(2v+2)), at float4 index v P + k, so that a
+// warp's consecutive k read consecutive 16-byte words) or the single base
+// factor w^k from which it builds the powers.
 __host__ __device__ constexpr bool tw_is_rows(int P, int R) { return P <= 256 && R > 2; }
 __host__ __device__ constexpr int tw_pass_size(int logn, int idx, bool inv) {
   return idx < 1 ? 0
                  : (tw_is_rows(plan_p(logn, idx, inv), plan_radix(logn, idx, inv))
-                        ? plan_p(logn, idx, inv) * tw_row_stride(plan_radix(logn, idx, inv))
+                        ? plan_p(logn, idx, inv) * plan_radix(logn, idx, inv)
                         : plan_p(logn, idx, inv));
 }
 // Offset of pass idx's table in the per-length array: forward passes first.
