@@ -191,6 +191,36 @@ s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* 
                            const float* u, int batch, int H, int N, int r, int L,
                            s4_c32* x, s4_c32* y, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * s4_hippo_dplr -- HiPPO state matrix in DPLR form (host routine, float64).
+ * Page "Recurrent, LSTM, and structured state-space models", the paragraph on
+ * the HiPPO generators and the DPLR / NPLR definitions:
+ *   kind S4_HIPPO_LEGS: G_nk = -sqrt((2n+1)(2k+1)) (n > k), -(n+1) (n = k), 0 (n < k)
+ *   kind S4_HIPPO_LEGT: G_nk = -(2n+1)(-1)^(n-k)/theta (n >= k), -(2n+1)/theta (n < k),
+ *                       taken through the similarity S_0 = diag(sqrt(2n+1)) diag((-1)^n)
+ *   kind S4_HIPPO_LAGT: G_nk = -1 (n >= k), 0 (n < k)
+ * The (similar) generator is split as H - U U^T with H normal and U of rank
+ * r = 1 (LegS, LagT) or 2 (LegT); a unitary W with H = W diag(Lambda) W^*
+ * (eigenvectors of a Hermitian matrix, by cyclic Jacobi rotations) gives
+ *     W^* S^{-1} G S W = diag(Lambda) - P P^*,   P = W^* U,
+ * i.e. the DPLR form with Q = P, and the state change x = S W x~ maps the
+ * input and output vectors to B~ = W^* S^{-1} B and C~ = W^* S^* C.
+ *   N: 1 .. 512.  theta: window of LegT (> 0, finite; ignored otherwise).
+ *   B, C: optional inputs [N] complex (interleaved re, im doubles; NULL = none).
+ *   Lambda [N] complex, P [N][r] complex (caller allocates room for [N][2]),
+ *   Bt, Ct [N] complex (required when B, C are given), *rank = r: outputs.
+ * All pointers are HOST pointers.  Runs synchronously on the calling thread,
+ * uses no GPU and allocates only host scratch.  Eigenvalues are returned in
+ * ascending order of Im Lambda; eigenvector phases (and so P, B~, C~) are
+ * one valid choice among many, while Lambda - P P^* is unique up to the
+ * unitary freedom of W and the kernel C^* Abar^j Bbar is unique.
+ * Returns S4_ERR_INVALID_ARG on bad arguments; S4_ERR_NONFINITE if the
+ * eigen-iteration does not converge.
+ */
+typedef enum { S4_HIPPO_LEGS = 0, S4_HIPPO_LEGT = 1, S4_HIPPO_LAGT = 2 } s4_hippo_kind;
+s4_status s4_hippo_dplr(int kind, int N, double theta, const double* B, const double* C,
+                        double* Lambda, double* P, double* Bt, double* Ct, int* rank);
+
 /* Synchronises `stream`, then returns the device-detected status recorded in
  * `ws` by the last entry point that used it (S4_OK if none), or
  * S4_ERR_CUDA if the synchronisation or the read fails. */

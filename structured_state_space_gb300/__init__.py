@@ -40,7 +40,10 @@ ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
     "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd", "s4_conv_fwd_real",
+    "s4_hippo_dplr",
 ]
+
+HIPPO_KINDS = {"legs": 0, "legt": 1, "lagt": 2}
 
 
 class S4Error(RuntimeError):
@@ -87,6 +90,8 @@ def load(path: str | None = None):
     lib.s4_ctilde.restype = i32
     lib.s4_recurrent_fwd.argtypes = [vp] * 8 + [i32] * 5 + [vp, vp, vp, sz, vp]
     lib.s4_recurrent_fwd.restype = i32
+    lib.s4_hippo_dplr.argtypes = [i32, i32, ctypes.c_double] + [vp] * 6 + [i32p]
+    lib.s4_hippo_dplr.restype = i32
     _lib = lib
     return lib
 
@@ -253,6 +258,44 @@ def s4_recurrent_fwd(Lambda, P, Q, B, C, dt, D, u, x=None, y=None, ws=None, stre
         ws.numel(), _stream(stream))
     _check(code, "s4_recurrent_fwd")
     return y, x
+
+
+def s4_hippo_dplr(kind, N, theta=1.0, B=None, C=None):
+    """HiPPO generator `kind` ("legs", "legt", "lagt") of size N in DPLR form
+    (host float64 routine of the library).  Returns a dict of complex128
+    numpy arrays Lambda [N], P = Q [N][r], and B~, C~ [N] when B, C are given,
+    plus the rank r."""
+    import numpy as np
+    if kind not in HIPPO_KINDS:
+        raise ValueError(f"kind must be one of {sorted(HIPPO_KINDS)}")
+    lib = load()
+    vp = ctypes.c_void_p
+
+    def host_in(v):
+        if v is None:
+            return None, None
+        a = np.ascontiguousarray(np.asarray(v, dtype=np.complex128).reshape(N))
+        return a, a.ctypes.data_as(vp)
+
+    Bin, Bp = host_in(B)
+    Cin, Cp = host_in(C)
+    Lam = np.zeros(N, np.complex128)
+    P = np.zeros(2 * N, np.complex128)
+    Bt = np.zeros(N, np.complex128) if B is not None else None
+    Ct = np.zeros(N, np.complex128) if C is not None else None
+    rank = ctypes.c_int(0)
+    code = lib.s4_hippo_dplr(HIPPO_KINDS[kind], int(N), float(theta), Bp, Cp, Lam.ctypes.data_as(vp),
+                             P.ctypes.data_as(vp), Bt.ctypes.data_as(vp) if Bt is not None else None,
+                             Ct.ctypes.data_as(vp) if Ct is not None else None, ctypes.byref(rank))
+    _check(code, "s4_hippo_dplr")
+    r = rank.value
+    out = {"Lambda": Lam, "P": P[: N * r].reshape(N, r).copy(), "rank": r}
+    out["Q"] = out["P"].copy()
+    if Bt is not None:
+        out["B"] = Bt
+    if Ct is not None:
+        out["C"] = Ct
+    return out
 
 
 def s4_get_status(ws, stream=None) -> int:

@@ -1,7 +1,8 @@
 """Build libs4.so for sm_103a with nvcc (no cmake, no torch extension machinery).
 
-Each .cu file under csrc/ is compiled in parallel to a position-independent
-object and the objects are linked into lib/libs4.so inside the package.
+Each source under csrc/ (CUDA .cu files and the host-only hippo.cpp) is
+compiled in parallel to a position-independent object and the objects are
+linked into lib/libs4.so inside the package.
 """
 from __future__ import annotations
 
@@ -18,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libs4.so")
-SOURCES = ["s4_api.cu", "cauchy.cu", "fft_rows.cu", "fft_cluster.cu", "s4_noalloc.cu", "recurrent.cu"]
+SOURCES = ["s4_api.cu", "cauchy.cu", "fft_rows.cu", "fft_cluster.cu", "s4_noalloc.cu", "recurrent.cu",
+           "hippo.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 GENDIR = os.path.join(OBJDIR, "gen")
@@ -57,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r

@@ -23,7 +23,17 @@
 #include "s4_internal.h"
 #include "s4_tan.cuh"
 
+#ifndef S4_CAUCHY_UNROLL
+#define S4_CAUCHY_UNROLL 2
+#endif
+
+#ifndef S4_CAUCHY_UNROLL
+#define S4_CAUCHY_UNROLL 2
+#endif
+
 namespace s4dev {
+
+constexpr int kCauchyUnroll = S4_CAUCHY_UNROLL;  // poles per unrolled step of the pole loop
 
 __device__ __forceinline__ float2 conj_mul(float2 a, float2 b) {  // conj(a) * b
   return make_float2(fmaf(a.x, b.x, a.y * b.y), fmaf(a.x, b.y, -a.y * b.x));
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
       for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
     }
     __syncthreads();
-#pragma unroll 2
+#pragma unroll kCauchyUnroll
     for (int jj = 0; jj < jn; ++jj) {
       float pr[PS];
       const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);

@@ -264,8 +264,11 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
 // (4 CTAs of 128 threads, 128 registers each) measured fastest at 2M = 2048 --
 // the kernel is latency-bound and occupancy beats the extra registers.  Rows
 // of 8192 points (256 threads) keep their registers (128 would spill).
+#ifndef S4_CONV_THREADS_PER_SM
+#define S4_CONV_THREADS_PER_SM 512
+#endif
 __host__ __device__ constexpr int conv_min_blocks(int logn, int threads) {
-  return (logn >= 13 || threads >= 512) ? 1 : 512 / threads;
+  return (logn >= 13 || threads >= S4_CONV_THREADS_PER_SM) ? 1 : S4_CONV_THREADS_PER_SM / threads;
 }
 
 // Butterfly index of slot `sl` of the last forward pass (and the first inverse
