@@ -112,11 +112,11 @@ __global__ void __launch_bounds__(128) conv_small_kernel(const float* __restrict
 // ----------------------------------------------------------------------------
 // Rows of length 32 .. 16384: Stockham passes over padded shared memory.
 // ----------------------------------------------------------------------------
-template <int LOGN>
+template <int LOGN, bool CONV = false>
 struct RowCfg {
   static constexpr int n = 1 << LOGN;
-  static constexpr int T = row_threads(LOGN);
-  static constexpr int ROWS = rows_per_cta(LOGN);
+  static constexpr int T = CONV ? conv_row_threads(LOGN) : row_threads(LOGN);
+  static constexpr int ROWS = T >= 128 ? 1 : 128 / T;
   static constexpr int THREADS = T * ROWS;
   static constexpr int NP = plan_npass(LOGN);
   static constexpr int RA = plan_radix(LOGN, 0, false);       // first forward radix
@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
 // Resident CTAs per SM the convolution is compiled for: 512 threads per SM
 // (4 CTAs of 128 threads, 128 registers each) measured fastest at 2M = 2048 --
 // the kernel is latency-bound and occupancy beats the extra registers.  Rows
-// of 8192 points (256 threads) keep their registers (128 would spill).
+// of 8192 points take one 512-thread CTA per SM (their shared memory allows
+// no second one).
 #ifndef S4_CONV_THREADS_PER_SM
 #define S4_CONV_THREADS_PER_SM 512
 #endif
@@ -299,11 +300,11 @@ __device__ __forceinline__ void split_mul(float2 zk, float2 zp, float2 kv, float
 // the convolution with D times the unit impulse, whose spectrum is D in every
 // bin, so it enters as D/(2n) added to each K2 bin.
 template <int LOGN>
-__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN>::THREADS))
+__global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
     float2* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
-  using C = RowCfg<LOGN>;
+  using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
   constexpr bool MIRROR = PERL % 2 == 0;
@@ -527,11 +528,11 @@ __global__ void __launch_bounds__(128) conv_real_small_kernel(const float* __res
 }
 
 template <int LOGN>
-__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN>::THREADS))
+__global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2,
                       const float* __restrict__ D, float* __restrict__ y, int batch, int H, int L,
                       const unsigned* __restrict__ status) {
-  using C = RowCfg<LOGN>;
+  using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
   using IXF0 = PassIdx<n, RA, 1>;
@@ -710,7 +711,7 @@ static cudaError_t conv_launch(const float* u, const float2* K2, const float* D,
     TimedLaunch tl("conv", s);
     conv_small_kernel<LOGN><<<(pairs + 127) / 128, 128, 0, s>>>(u, K2, D, y, batch, H, L, st);
   } else {
-    using C = RowCfg<LOGN>;
+    using C = RowCfg<LOGN, true>;
     const size_t smem = sizeof(float2) * 2 * (size_t)C::ROWS * C::PADN;
     auto k = conv_pair_kernel<LOGN>;
     cudaError_t e = prepare(k, smem);
@@ -761,7 +762,7 @@ static cudaError_t conv_real_launch(const float* u, const float2* K2, const floa
     TimedLaunch tl("conv_real", s);
     conv_real_small_kernel<LOGN><<<(pairs + 127) / 128, 128, 0, s>>>(u, K2, D, y, batch, H, L, st);
   } else {
-    using C = RowCfg<LOGN>;
+    using C = RowCfg<LOGN, true>;
     const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
     auto k = conv_real_pair_kernel<LOGN>;
     cudaError_t e = prepare(k, smem);

@@ -59,5 +59,11 @@ __host__ __device__ constexpr int row_threads(int logn) {
 __host__ __device__ constexpr int rows_per_cta(int logn) {
   return row_threads(logn) >= 128 ? 1 : 128 / row_threads(logn);
 }
+// The paired convolution kernels give 8192-point rows one thread per radix-16
+// butterfly (512 threads): they run one CTA per SM there, and the extra warps
+// hide latency (measured faster; the other kernels of that length are not).
+__host__ __device__ constexpr int conv_row_threads(int logn) {
+  return logn == 13 ? 512 : row_threads(logn);
+}
 
 }  // namespace s4dev
