@@ -234,12 +234,22 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
   if (!fin) atomicOr(status, ST_NONFINITE);
 }
 
+// Threads per SM the kspec kernel is compiled for (registers capped at
+// 65536 / this): 512 measured ~10 % faster at M = 4096 than no cap and equal at
+// M = 1024, with room left for the convolution's early CTAs.
+#ifndef S4_KSPEC_THREADS_PER_SM
+#define S4_KSPEC_THREADS_PER_SM 512
+#endif
+__host__ __device__ constexpr int kspec_min_blocks(int threads) {
+  return threads >= S4_KSPEC_THREADS_PER_SM ? 1 : S4_KSPEC_THREADS_PER_SM / threads;
+}
+
 // Layer path: for each channel, K = first L of (1/M) iFFT_M(Khat) (written
 // out) and, from the same shared-memory row, K2 = scale FFT_2M(K zero-padded).
 // One launch instead of two, and K is not read back.  Rows of 2M <= 2^13
 // points (LOGM = 5..12).
 template <int LOGM>
-__global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS) kspec_kernel(
+__global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(RowCfg<LOGM + 1>::THREADS)) kspec_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
     float scale, unsigned* __restrict__ status) {
   using C = RowCfg<LOGM + 1>;
