@@ -208,8 +208,15 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
   cl.sync();
   const float sc = 1.f / n;
   const int ncl = gridDim.x / C;
-  for (int row = blockIdx.x / C; row < rows; row += ncl) {
-    const int h = row % H;
+  const int batch = rows / H;
+  for (int idx = blockIdx.x / C; idx < rows; idx += ncl) {
+    // channel-major order: the batch rows of one channel run on neighbouring
+    // clusters at about the same time and share its spectrum through L2
+    const int h = idx / batch, row = (idx % batch) * H + h;
+    {  // this CTA's slice of the channel spectrum into L2 during the forward transform
+      const char* k2 = reinterpret_cast<const char*>(K2 + (size_t)h * n + (size_t)c * m);
+      for (int o = lt * 128; o < m * (int)sizeof(float2); o += T * 128) prefetch_l2(k2 + o);
+    }
     const float d = D[h];
     float uv[Cf::PI][C / 2];
     cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int s, int q, int t) {
@@ -284,8 +291,14 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_real_kernel(
   const float sc = 1.f / n;
   const int ncl = gridDim.x / C;
   const int pairs = ((batch + 1) / 2) * H;
+  const int pb = (batch + 1) / 2;
   for (int p = blockIdx.x / C; p < pairs; p += ncl) {
-    const int h = p % H, b0 = 2 * (p / H);
+    // channel-major order (see conv_cluster_kernel)
+    const int h = p / pb, b0 = 2 * (p % pb);
+    {
+      const char* k2 = reinterpret_cast<const char*>(K2 + (size_t)h * n + (size_t)c * m);
+      for (int o = lt * 128; o < m * (int)sizeof(float2); o += T * 128) prefetch_l2(k2 + o);
+    }
     const bool has1 = b0 + 1 < batch;
     const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
     const float d = D[h];

@@ -45,6 +45,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Hint: bring the line holding p into L2 (no effect on results).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---- padded shared-memory index: one spare slot per 16 entries ------------------
 // Keeps the Stockham read (stride n/R) and write (stride p) patterns free of
 // shared-memory bank conflicts for the radix plans used here.
