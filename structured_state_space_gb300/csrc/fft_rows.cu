@@ -298,13 +298,6 @@ __device__ __forceinline__ int last_bfly(int sl, int lt) {
   }
 }
 
-// Spectra of the two real rows of z = u_b + i u_{b+1} times the kernel
-// spectrum kv (already holding the skip term): 2 U_b kv and 2 U_{b+1} kv.
-__device__ __forceinline__ void split_mul(float2 zk, float2 zp, float2 kv, float2& a0, float2& a1) {
-  a0 = cmul(make_float2(zk.x + zp.x, zk.y - zp.y), kv);
-  a1 = cmul(make_float2(zk.y + zp.y, zp.x - zk.x), kv);
-}
-
 // Fused causal convolution, two batch rows (b, b+1) of one channel per row
 // group; K2 is the channel spectrum scaled by 1/(2n).  The skip term D u is
 // the convolution with D times the unit impulse, whose spectrum is D in every

@@ -28,6 +28,14 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
 __device__ __forceinline__ float2 cscale(float2 a, float s) { return make_float2(a.x * s, a.y * s); }
 __device__ __forceinline__ bool cfinite(float2 a) { return isfinite(a.x) && isfinite(a.y); }
 
+// Spectra of the two real rows of z = u_b + i u_{b+1} from Z[k] and zp =
+// Z[n-k], times the kernel spectrum kv: 2 U_b kv and 2 U_{b+1} kv, with
+// U_b = (Z[k] + conj Z[n-k])/2 and U_{b+1} = (Z[k] - conj Z[n-k])/(2i).
+__device__ __forceinline__ void split_mul(float2 zk, float2 zp, float2 kv, float2& a0, float2& a1) {
+  a0 = cmul(make_float2(zk.x + zp.x, zk.y - zp.y), kv);
+  a1 = cmul(make_float2(zk.y + zp.y, zp.x - zk.x), kv);
+}
+
 // Approximate reciprocal (PTX rcp.approx.ftz.f32, relative error ~2^-23).
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
