@@ -466,6 +466,217 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+PATHS = {
+    # path: (unit of the rate, timing families of the library, dominant family)
+    "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
+    "recurrent": ("channel-samples/s", ["recurrent"], "recurrent"),
+    "ctilde": ("channel-steps/s", ["ctilde"], "ctilde"),
+}
+
+
+def _oracle_path_unit(args):
+    """Oracle work of one unit of an auxiliary path (see run_path)."""
+    path, h, b = args
+    import numpy as np
+    import oracle.s4_oracle as O
+    from structured_state_space_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    p, u = _oracle_data()
+    if path == "conv_real":
+        K = _path_kernel(w)
+        O.causal_conv(K[h].real.astype(np.float64), u[b, h], p["D"][h])
+        return w.L
+    _, Abar, Bbar = O.bilinear(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["dt"][h])
+    if path == "recurrent":
+        O.recurrence(Abar, Bbar, p["Ctilde"][h], p["D"][h], u[b, h])
+        return w.L
+    O.ctilde_from_c(Abar, p["Ctilde"][h], w.M)
+    return w.M
+
+
+_PATH_K = None
+
+
+def _path_kernel(w):
+    """Seeded complex kernel [H][L] (complex64) fed to the real-output
+    convolution by both the GPU run and its CPU baseline (made once per process)."""
+    global _PATH_K
+    if _PATH_K is None:
+        import numpy as np
+        rng = np.random.default_rng(7000 + w.L)
+        _PATH_K = ((rng.standard_normal((w.H, w.L)) + 1j * rng.standard_normal((w.H, w.L))) * 0.05).astype(np.complex64)
+    return _PATH_K
+
+
+def run_path(args):
+    """One of the steps either side of the layer path, timed like the layer:
+    conv_real (s4_conv_fwd_real), recurrent (s4_recurrent_fwd over the L steps
+    of every row, state carried from call to call) or ctilde (s4_ctilde).  A
+    step is one call over the whole workload."""
+    import numpy as np
+    import torch
+
+    import structured_state_space_gb300 as s4
+    from structured_state_space_gb300 import build as s4build
+    from structured_state_space_gb300 import workloads as W
+
+    unit, families, dom = PATHS[args.path]
+    pool, procs = None, 0
+    if not args.no_cpu_baseline:
+        procs = max(1, os.cpu_count() or 1)
+        pool = make_pool(procs)
+    torch.cuda.set_device(0)
+    s4build.build()
+    s4.load()
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    H, N, r, L, Bsz, M = w.H, w.N, w.r, w.L, w.batch, w.M
+    p = W.make_params(w)
+    u_host = W.make_u(w, p)
+    dev = torch.device("cuda", 0)
+    prm = {k: torch.from_numpy(np.ascontiguousarray(p[k])).to(dev) for k in ["Lambda", "P", "Q", "B", "Ctilde", "dt", "D"]}
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    stream = torch.cuda.Stream(dev)
+    ws = s4.workspace(H, N, r, L, Bsz, dev)
+    if args.path == "ctilde":
+        set_bytes = H * N * 8 * 2
+        in_host, out_shape, out_dtype = None, (H, N), torch.complex64
+    else:
+        out_dtype = torch.float32 if args.path == "conv_real" else torch.complex64
+        set_bytes = Bsz * H * L * (4 + (4 if args.path == "conv_real" else 8))
+        in_host, out_shape = u_host, (Bsz, H, L)
+    nsets = min(16, max(3, math.ceil(2 * l2 / set_bytes) + 1))
+    ins = [torch.from_numpy(in_host).to(dev) for _ in range(nsets)] if in_host is not None else [None] * nsets
+    outs = [torch.empty(out_shape, dtype=out_dtype, device=dev) for _ in range(nsets)]
+    Kd = torch.from_numpy(_path_kernel(w)).to(dev) if args.path == "conv_real" else None
+    xs = torch.zeros((Bsz, H, N), dtype=torch.complex64, device=dev)
+
+    def call(i):
+        j = i % nsets
+        if args.path == "conv_real":
+            s4.s4_conv_fwd_real(ins[j], Kd, prm["D"], y=outs[j], ws=ws)
+        elif args.path == "recurrent":
+            s4.s4_recurrent_fwd(prm["Lambda"], prm["P"], prm["Q"], prm["B"], prm["Ctilde"], prm["dt"], prm["D"],
+                                ins[j], x=xs, y=outs[j], ws=ws)
+        else:
+            s4.s4_ctilde(prm["Lambda"], prm["P"], prm["Q"], prm["dt"], prm["Ctilde"], L, Ctilde=outs[j], ws=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    stream.synchronize()
+    if s4.s4_get_status(ws, stream) != 0:
+        raise RuntimeError("device status after warm-up")
+    G = nsets * 2
+    gbig = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gbig, stream=stream):
+        for i in range(G):
+            call(i)
+
+    def timed(body, k):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        body(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def replay(k):  # k rounded up to whole graphs
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, -(-k // G))):
+                gbig.replay()
+
+    K = max(G, -(-args.steps // G) * G)
+    sampler = ClockSampler(0)
+    sampler.start()
+    replay(max(args.warmup, G))
+    ms_total = timed(replay, K)
+    clocks = sampler.stop()
+    # per-kernel event times over S eager calls behind a graph head start
+    S = max(1, min(K, 200))
+    s4.timing.reset()
+    s4.timing.enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(S):
+            call(i)
+    torch.cuda.synchronize()
+    s4.timing.reset()
+
+    def prof(k):
+        with torch.cuda.stream(stream):
+            gbig.replay()
+            for i in range(k):
+                call(i)
+
+    timed(prof, S)
+    s4.timing.enable(False)
+    kern = {}
+    for name in families:
+        n, t = s4.timing.read(name)
+        kern[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1)}
+    s4.timing.reset()
+    per_call = Bsz * H * L if args.path != "ctilde" else H * M
+    value = per_call * K / (ms_total / 1e3)
+    peaks, peak_src = read_peaks()
+    fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    if args.path == "conv_real":
+        byts = Bsz * H * L * (4 + 4) + H * 2 * M * 8
+        ach = byts / (kern[dom]["avg_us"] * 1e-6) / 1e9
+        roof = {"kernel": "conv_real_pair_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "algorithmic": "u 4 B + y 4 B per channel-sample, Hermitian kernel spectrum 16 B per channel-root once"}
+    else:
+        steps = Bsz * H * L if args.path == "recurrent" else H * M
+        flops = steps * N * (20 + 16 * r)
+        ach = flops / (kern[dom]["avg_us"] * 1e-6) / 1e12
+        roof = {"kernel": f"{dom}_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": ach / fp32_peak, "traffic": None,
+                "algorithmic": f"{20 + 16 * r} flop per (row or channel, step, state element)",
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+    roof["peak_kind"] = f"of {peak_src}"
+    # end to end: input from pinned host memory, the call, output back, one stream
+    e2e = None
+    if in_host is not None:
+        in_pin = torch.from_numpy(in_host).pin_memory()
+        out_pin = torch.empty(out_shape, dtype=out_dtype).pin_memory()
+
+        def e2e_steps(k):
+            with torch.cuda.stream(stream):
+                for i in range(k):
+                    ins[i % nsets].copy_(in_pin, non_blocking=True)
+                    call(i)
+                    out_pin.copy_(outs[i % nsets], non_blocking=True)
+
+        n_e2e = max(3, min(K, 200))
+        e2e_steps(3)
+        ms_e2e = timed(e2e_steps, n_e2e)
+        e2e = {"value": per_call * n_e2e / (ms_e2e / 1e3), "unit": unit, "h2d_bytes_per_step": int(in_pin.numel() * 4),
+               "d2h_bytes_per_step": int(out_pin.numel() * out_pin.element_size()), "steps": n_e2e,
+               "how": "per step on one stream: H2D of u from pinned memory, the call, D2H of the output"}
+    line = {"metric": f"S4 {args.path} {unit}", "path": args.path, "value": value, "unit": unit, "n_gpus": 1,
+            "steps": K, "warmup": max(args.warmup, G), "ms_per_step": ms_total / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "N": N, "r": r, "H": H, "L": L, "M": M, "batch": Bsz},
+            "gpu_launches": int(round(sum(v["launches"] for v in kern.values()) / S)) * K,
+            "kernels": kern, "roofline": roof, "clocks": clocks, "e2e": e2e}
+    if pool is not None:
+        if args.path == "ctilde":
+            units = [(args.path, h, 0) for h in range(H)]
+            what = f"{len(units)} channels x M={M} steps"
+        else:
+            units = [(args.path, h, b) for h in range(H) for b in range(Bsz)]
+            what = f"{len(units)} rows x L={L}"
+        t0 = time.perf_counter()
+        done = sum(pool.map(_oracle_path_unit, units))
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": done / secs, "unit": unit, "cores": procs, "kind": "oracle",
+                                "sample": f"{what} ({done} units, {secs:.1f} s wall)"}
+        pool.close()
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -506,6 +717,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["layer"] + sorted(PATHS), default="layer",
+                    help="layer (the bench line) or a step either side of it")
     ap.add_argument("--workload", type=int, default=None,
                     help="seeded workload index (default 1, the benchmark workload)")
     args = ap.parse_args()
@@ -517,6 +730,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.path != "layer":
+        run_path(args)
     else:
         run_ours(args)
 
