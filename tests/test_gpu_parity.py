@@ -181,6 +181,79 @@ def test_status_clears_on_next_call():
     assert s4.s4_get_status(ws) == 0
 
 
+def _layer(d, u, ws, K=None, y=None, dt=None):
+    return s4.s4_layer_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"] if dt is None else dt,
+                           d["D"], u, K=K, y=y, ws=ws)
+
+
+def test_layer_status_protocol():
+    # a bad step in the last channel zeroes K and y of the whole call, and the
+    # next good call on the same workspace clears the status again
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    ut = torch.from_numpy(W.make_u(w, p)).cuda()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    bad = d["dt"].clone()
+    bad[w.H - 1] = -1.0
+    K, y = _layer(d, ut, ws, dt=bad)
+    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_INVALID_STEP"]
+    assert torch.count_nonzero(K).item() == 0 and torch.count_nonzero(y).item() == 0
+    K, y = _layer(d, ut, ws)
+    assert s4.s4_get_status(ws) == 0
+    assert torch.count_nonzero(K).item() > 0 and torch.count_nonzero(y).item() > 0
+    # a status left by another entry point is cleared by the layer call too
+    s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], bad, w.L, ws=ws)
+    assert s4.s4_get_status(ws) != 0
+    _layer(d, ut, ws, K=K, y=y)
+    assert s4.s4_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("L", [8, 32])
+def test_layer_resonance_zeroes_outputs(L):
+    # L = 32 takes the three-kernel layer path, L = 8 the generic one
+    g = W.scalar_example(L, u=list(range(1, L + 1)))
+    d = {k: torch.from_numpy(g[k]).cuda() for k in ["Lambda", "P", "Q", "B", "dt"]}
+    ws = s4.workspace(1, 1, 1, L, 1)
+    K, y = s4.s4_layer_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["B"], d["dt"],
+                           torch.zeros(1, device="cuda"), torch.from_numpy(g["u"]).cuda(), ws=ws)
+    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_RESONANT_DIAGONAL"]
+    assert torch.count_nonzero(K).item() == 0 and torch.count_nonzero(y).item() == 0
+
+
+def test_layer_calls_in_a_graph_match_eager():
+    # consecutive layer calls captured in one graph (each call's kernels chained
+    # by programmatic dependent launch) give bitwise the results of eager calls
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    u1 = torch.from_numpy(W.make_u(w, p)).cuda()
+    u2 = u1.flip(-1).contiguous()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    K1e, y1e = _layer(d, u1, ws)
+    K2e, y2e = _layer(d, u2, ws)
+    torch.cuda.synchronize()
+    K1, y1 = torch.empty_like(K1e), torch.empty_like(y1e)
+    K2, y2 = torch.empty_like(K2e), torch.empty_like(y2e)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _layer(d, u1, ws, K=K1, y=y1)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _layer(d, u1, ws, K=K1, y=y1)
+        _layer(d, u2, ws, K=K2, y=y2)
+    y1.zero_()
+    y2.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+    s.synchronize()
+    assert torch.equal(y1, y1e) and torch.equal(y2, y2e) and torch.equal(K2, K2e)
+    assert s4.s4_get_status(ws, s) == 0
+
+
 def test_host_errors_raise():
     w = W.WORKLOADS[0]
     p = W.make_params(w)
