@@ -54,9 +54,11 @@ typedef enum {
     S4_ERR_NONFINITE = 5,            /* a root value or spectrum entry is inf/nan */
     S4_ERR_INVALID_STEP = 6,         /* some Delta_h <= 0 or not finite */
     S4_ERR_CUDA = 7,                 /* a CUDA runtime call or launch failed */
-    S4_ERR_SINGULAR_BILINEAR = 8     /* G = I - (Delta/2) A not solved: some d_j = 1 - (Delta/2) lambda_j
+    S4_ERR_SINGULAR_BILINEAR = 8,    /* G = I - (Delta/2) A not solved: some d_j = 1 - (Delta/2) lambda_j
                                         is exactly 0 (the bordered branch, not taken on the GPU)
                                         or I_r + (Delta/2) Q^* D^{-1} P is exactly singular */
+    S4_ERR_TIMEOUT = 9               /* a kernel's bounded wait for an asynchronous copy into shared
+                                        memory ran out (the affected output is zeros) */
 } s4_status;
 
 /* Bytes of scratch that s4_kernel_gen, s4_conv_fwd and s4_layer_fwd need for

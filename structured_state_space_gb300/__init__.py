@@ -31,7 +31,7 @@ __all__ = [
 STATUS = {
     0: "S4_OK", 1: "S4_ERR_INVALID_ARG", 2: "S4_ERR_WORKSPACE", 3: "S4_ERR_RESONANT_DIAGONAL",
     4: "S4_ERR_RESONANT_CORRECTION", 5: "S4_ERR_NONFINITE", 6: "S4_ERR_INVALID_STEP", 7: "S4_ERR_CUDA",
-    8: "S4_ERR_SINGULAR_BILINEAR",
+    8: "S4_ERR_SINGULAR_BILINEAR", 9: "S4_ERR_TIMEOUT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 

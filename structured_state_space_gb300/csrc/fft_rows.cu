@@ -311,11 +311,18 @@ __device__ __forceinline__ int last_bfly(int sl, int lt) {
 // group; K2 is the channel spectrum scaled by 1/(2n).  The skip term D u is
 // the convolution with D times the unit impulse, whose spectrum is D in every
 // bin, so it enters as D/(2n) added to each K2 bin.
-template <int LOGN>
+//
+// STAGE (one pair per CTA, used for 2M = 8192): a third shared buffer receives, by bulk
+// asynchronous copies, the channel's K2 row (requested after the first
+// forward pass, used by the spectrum product) and the next pair's two input
+// rows (requested once the product has read K2, used by the next forward
+// pass 0), so neither global latency sits on the critical path.  Input rows
+// are staged only when L is a multiple of 4 (stage_u; 16-byte copies).
+template <int LOGN, bool STAGE>
 __global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
+    float2* __restrict__ y, int batch, int H, int L, unsigned* __restrict__ status, int stage_u) {
   using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
@@ -334,6 +341,36 @@ conv_pair_kernel(
   float2* const buf2[2] = {bufA, bufB};
   bool zero = false, waited = false;
   const int pairs = ((batch + 1) / 2) * H;
+  static_assert(!STAGE || C::ROWS == 1, "staging serves one pair per CTA");
+  float2* stage = bufB + C::PADN;  // STAGE: n entries (K2 row, or input rows as floats)
+  const float* stage_f = reinterpret_cast<const float*>(stage);
+  __shared__ unsigned long long bar;
+  unsigned ph = 0u;
+  bool stall = false;
+  // one thread: announce and copy the two input rows of pair q into the stage
+  auto issue_u = [&](int q) {
+    const int hq = q % H, bq = 2 * (q / H);
+    const unsigned bytes = (unsigned)L * 4u;
+    const bool two = bq + 1 < batch;
+    fence_proxy_async();
+    mbar_expect_tx(&bar, two ? 2u * bytes : bytes);
+    const size_t r0 = (size_t)bq * H + hq;
+    bulk_g2s(stage, u + r0 * L, bytes, &bar);
+    if (two) bulk_g2s(stage + n / 2, u + (r0 + H) * L, bytes, &bar);
+  };
+  auto issue_k2 = [&](const float2* src) {
+    fence_proxy_async();
+    mbar_expect_tx(&bar, (unsigned)(n * sizeof(float2)));
+    bulk_g2s(stage, src, (unsigned)(n * sizeof(float2)), &bar);
+  };
+  if constexpr (STAGE) {
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1u);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (stage_u && threadIdx.x == 0 && (int)blockIdx.x < pairs) issue_u(blockIdx.x);
+  }
   for (int p0 = blockIdx.x * C::ROWS; p0 < pairs; p0 += gridDim.x * C::ROWS) {
     const int p = p0 + slot;
     const bool act = p < pairs;
@@ -343,7 +380,12 @@ conv_pair_kernel(
     const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
     const float dk = act ? D[h] * (0.5f / n) : 0.f;
     const float2* K2h = K2 + (size_t)h * n;
-    // forward pass 0: z = u_b + i u_{b+1}, zero-padded, global -> shared
+    const bool from_stage = STAGE && stage_u;
+    if (from_stage) {  // this pair's input rows
+      stall |= !mbar_wait(&bar, ph);
+      ph ^= 1u;
+    }
+    // forward pass 0: z = u_b + i u_{b+1}, zero-padded, global (or stage) -> shared
 #pragma unroll
     for (int s = 0; s < PER0; ++s) {
       const int i = lt + s * T;
@@ -351,18 +393,23 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
-        a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
+        if (from_stage)
+          a[q] = make_float2(t < L ? stage_f[t] : 0.f, (has1 && t < L) ? stage_f[n + t] : 0.f);
+        else
+          a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
       }
       dft<RA, false, true>(a);
 #pragma unroll
       for (int q = 0; q < RA; ++q) bufA[IXF0::wr(i, q)] = a[q];
     }
     __syncthreads();
+    if (STAGE && waited && threadIdx.x == 0) issue_k2(K2h);  // the stage's inputs are consumed
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(buf1, lt);
     if (!waited) {  // the forward transform of u needed nothing from the previous kernel
       pdl_wait();
       zero = *((volatile const unsigned*)status) != 0u;
       waited = true;
+      if (STAGE && threadIdx.x == 0) issue_k2(K2h);  // K2 comes from the previous kernel
     }
     // forward last pass: Z in natural order, bin i + q NBL of butterfly i
     float2 z[PERL][RB];
@@ -380,6 +427,11 @@ conv_pair_kernel(
     // in registers; row b+1 goes to bufB at once (unused since the last
     // iteration), row b to bufA after every thread has read its last pass.
     float2 (&a0)[PERL][RB] = z;  // row b's products replace Z in place
+    if constexpr (STAGE) {  // the channel's K2 row
+      stall |= !mbar_wait(&bar, ph);
+      ph ^= 1u;
+    }
+    const float2* Kr = STAGE ? stage : K2h;
     if constexpr (MIRROR) {
 #pragma unroll
       for (int s = 0; s < PERL / 2; ++s) {
@@ -387,8 +439,8 @@ conv_pair_kernel(
         float2 kA[RB], kB[RB], a1A[RB], a1B[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          kA[q] = __ldg(K2h + iA + q * NBL);
-          kB[q] = __ldg(K2h + iB + q * NBL);
+          kA[q] = STAGE ? Kr[iA + q * NBL] : __ldg(K2h + iA + q * NBL);
+          kB[q] = STAGE ? Kr[iB + q * NBL] : __ldg(K2h + iB + q * NBL);
           kA[q].x += dk;
           kB[q].x += dk;
         }
@@ -431,6 +483,7 @@ conv_pair_kernel(
         dft<RB, true>(zB);
       }
       __syncthreads();
+      if (STAGE && stage_u && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
     } else {
       // one butterfly per thread: the mirror bins sit in another thread
 #pragma unroll
@@ -447,7 +500,7 @@ conv_pair_kernel(
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           const int k = i + q * NBL;
-          float2 kv = __ldg(K2h + k);
+          float2 kv = STAGE ? Kr[k] : __ldg(K2h + k);
           kv.x += dk;
           split_mul(z[sl][q], bufB[pad((n - k) & (n - 1))], kv, a0[sl][q], a1[sl][q]);
         }
@@ -455,6 +508,7 @@ conv_pair_kernel(
         dft<RB, true>(a1[sl]);
       }
       __syncthreads();
+      if (STAGE && stage_u && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
 #pragma unroll
       for (int sl = 0; sl < PERL; ++sl) {
         const int i = last_bfly<T, NBL, PERL>(sl, lt);
@@ -462,6 +516,7 @@ conv_pair_kernel(
         for (int q = 0; q < RB; ++q) bufB[IXI0::wr(i, q)] = a1[sl][q];
       }
     }
+    if (stall) zero = true;
 #pragma unroll
     for (int sl = 0; sl < PERL; ++sl) {
       const int i = last_bfly<T, NBL, PERL>(sl, lt);
@@ -496,6 +551,7 @@ conv_pair_kernel(
     }
     __syncthreads();
   }
+  if (stall && threadIdx.x == 0) atomicOr(status, ST_STALL);
 }
 
 // Real-output convolution y = Re(K) * u + D u.  K2 = FFT_n(Re K zero-padded)/n
@@ -724,13 +780,19 @@ static cudaError_t conv_launch(const float* u, const float2* K2, const float* D,
     conv_small_kernel<LOGN><<<(pairs + 127) / 128, 128, 0, s>>>(u, K2, D, y, batch, H, L, st);
   } else {
     using C = RowCfg<LOGN, true>;
-    const size_t smem = sizeof(float2) * 2 * (size_t)C::ROWS * C::PADN;
-    auto k = conv_pair_kernel<LOGN>;
+    // bulk-copy staging where one CTA (one pair) runs per SM, 2M = 8192: the
+    // kernel is latency bound there and staging measured 5 % faster; at 2M =
+    // 2048 (4 CTAs per SM) the third buffer cost more than it saved (the L1
+    // share of each SM shrinks with the shared-memory carve-out)
+    constexpr bool STAGE = C::ROWS == 1 && LOGN == 13;
+    const size_t smem = sizeof(float2) * (2 * (size_t)C::ROWS * C::PADN + (STAGE ? (size_t)C::n : 0));
+    auto k = conv_pair_kernel<LOGN, STAGE>;
     cudaError_t e = prepare(k, smem);
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv", s);
-    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L, st);
+    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L,
+                            const_cast<unsigned*>(st), (L % 4 == 0) ? 1 : 0);
   }
   return cudaGetLastError();
 }

@@ -313,6 +313,7 @@ s4_status s4_get_status(const void* ws, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return S4_ERR_CUDA;
   unsigned word = 0;
   if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return S4_ERR_CUDA;
+  if (word & s4dev::ST_STALL) return S4_ERR_TIMEOUT;
   if (word & s4dev::ST_BAD_STEP) return S4_ERR_INVALID_STEP;
   if (word & s4dev::ST_RES_DIAG) return S4_ERR_RESONANT_DIAGONAL;
   if (word & s4dev::ST_RES_CORR) return S4_ERR_RESONANT_CORRECTION;
@@ -332,6 +333,7 @@ const char* s4_status_str(s4_status st) {
     case S4_ERR_INVALID_STEP: return "step size not positive and finite";
     case S4_ERR_CUDA: return "CUDA error";
     case S4_ERR_SINGULAR_BILINEAR: return "singular-bilinear-matrix";
+    case S4_ERR_TIMEOUT: return "timeout";
   }
   return "unknown status";
 }

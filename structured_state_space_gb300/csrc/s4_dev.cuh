@@ -18,6 +18,7 @@ constexpr unsigned ST_RES_CORR = 2u;   // W(z_k) singular
 constexpr unsigned ST_NONFINITE = 4u;  // non-finite root value or spectrum
 constexpr unsigned ST_BAD_STEP = 8u;   // Delta <= 0 or not finite
 constexpr unsigned ST_SINGULAR = 16u;  // G = I - (Delta/2) A not solved (zero d_j or singular W)
+constexpr unsigned ST_STALL = 32u;     // a bounded wait on an asynchronous copy ran out
 
 // ---- complex helpers ----------------------------------------------------------
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
@@ -56,6 +57,48 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // Hint: bring the line holding p into L2 (no effect on results).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// ---- bulk asynchronous copies into shared memory, tracked by an mbarrier -----------
+// One thread announces the bytes of a round (mbar_expect_tx) and issues the
+// copies (bulk_g2s: 16-byte aligned addresses, sizes a multiple of 16); every
+// thread then waits for the round's phase.  The wait is bounded: it reports
+// false after kMbarWaitLimit polls instead of spinning forever.
+constexpr int kMbarWaitLimit = 1 << 22;
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// make an initialised mbarrier visible to the asynchronous (copy) proxy
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// order this CTA's earlier shared-memory accesses before later asynchronous copies
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
+  for (int it = 0; it < kMbarWaitLimit; ++it) {
+    unsigned done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
 }
 
 // ---- padded shared-memory index: one spare slot per 16 entries ------------------
