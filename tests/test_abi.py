@@ -49,6 +49,8 @@ def test_status_strings(lib):
     assert s4.s4_status_str(0) == "ok"
     assert s4.s4_status_str(3) == "resonant-diagonal"
     assert s4.s4_status_str(4) == "resonant-correction"
+    assert s4.s4_status_str(9) == "timeout"
+    assert s4.STATUS[9] == "S4_ERR_TIMEOUT"
     assert s4.s4_status_str(99) == "unknown status"
 
 
