@@ -294,6 +294,7 @@ using namespace s4dev;
 #define S4_CAUCHY_RPT1 2
 #endif
 
+
 template <int RANK, int RPT>
 static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
                                  const float2* B, const float2* Ct, const float* dt,
@@ -318,8 +319,9 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
     case 1:
       return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
                    : cauchy_launch<1, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
-    case 2:
-      return cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
+    case 2:  // 4 roots per thread on large grids measured 2 % faster (8 at rank 1 was 11 % slower)
+      return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
+                   : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     case 3:
       return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
     case 4:
