@@ -35,3 +35,12 @@ def test_import_and_load_do_not_import_the_oracle():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == "[]", r.stdout
+
+
+def test_missing_library_fails_loudly():
+    # no fallback: without the built library every entry point is unavailable
+    code = ("import structured_state_space_gb300 as s4\n"
+            "try:\n    s4.load('/nonexistent/libs4.so')\nexcept RuntimeError as e:\n    print('raised', 'not built' in str(e))\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == "raised True", r.stdout
