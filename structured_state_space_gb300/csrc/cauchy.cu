@@ -314,7 +314,10 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
                           const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
                           int M, int logC, unsigned* status, cudaStream_t s) {
   // roots per thread: enough CTAs to fill the GPU for small M, more ILP for large M
-  const bool small = (long long)H * M < 4LL * 128 * 4 * num_sms() * 8;
+  // 4 roots per thread (512 per CTA, 5 CTAs per SM at ~100 registers) once the
+  // grid holds at least two waves of such CTAs; 2 below that, to keep enough
+  // warps resident (measured: 2 roots faster at H M = 2.6e5, 4 faster at 2.1e6)
+  const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
   switch (r) {
     case 1:
       return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
