@@ -68,7 +68,8 @@ def test_kernel_from_c_through_ctilde():
     assert rel_l2(K[chans], np.array(ref)) <= REL
 
 
-@pytest.mark.parametrize("N,r,H,L,batch", [(4, 1, 2, 64, 1), (64, 1, 6, 1024, 2), (64, 2, 3, 500, 3), (200, 1, 2, 256, 2), (16, 4, 2, 128, 1)])
+@pytest.mark.parametrize("N,r,H,L,batch", [(4, 1, 2, 64, 1), (64, 1, 6, 1024, 2), (64, 2, 3, 500, 3), (200, 1, 2, 256, 2),
+                                           (16, 4, 2, 128, 1), (33, 1, 5, 77, 1)])
 def test_recurrent_matches_oracle_and_carries_state(N, r, H, L, batch):
     w = W.custom(N, r, H, L, batch, seed=3 * N + L)
     p = _with_c(w, 13)
