@@ -468,6 +468,7 @@ def run_ours(args):
 
 PATHS = {
     # path: (unit of the rate, timing families of the library, dominant family)
+    "conv": ("channel-samples/s", ["spectrum", "conv"], "conv"),
     "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
     "recurrent": ("channel-samples/s", ["recurrent"], "recurrent"),
     "ctilde": ("channel-steps/s", ["ctilde"], "ctilde"),
@@ -482,9 +483,9 @@ def _oracle_path_unit(args):
     from structured_state_space_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD_INDEX]
     p, u = _oracle_data()
-    if path == "conv_real":
-        K = _path_kernel(w)
-        O.causal_conv(K[h].real.astype(np.float64), u[b, h], p["D"][h])
+    if path in ("conv", "conv_real"):
+        K = _path_kernel(w)[h].astype(np.complex128)
+        O.causal_conv(K.real if path == "conv_real" else K, u[b, h], p["D"][h])
         return w.L
     _, Abar, Bbar = O.bilinear(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["dt"][h])
     if path == "recurrent":
@@ -498,8 +499,8 @@ _PATH_K = None
 
 
 def _path_kernel(w):
-    """Seeded complex kernel [H][L] (complex64) fed to the real-output
-    convolution by both the GPU run and its CPU baseline (made once per process)."""
+    """Seeded complex kernel [H][L] (complex64) fed to the convolution paths by
+    both the GPU run and its CPU baseline (made once per process)."""
     global _PATH_K
     if _PATH_K is None:
         import numpy as np
@@ -509,10 +510,10 @@ def _path_kernel(w):
 
 
 def run_path(args):
-    """One of the steps either side of the layer path, timed like the layer:
-    conv_real (s4_conv_fwd_real), recurrent (s4_recurrent_fwd over the L steps
-    of every row, state carried from call to call) or ctilde (s4_ctilde).  A
-    step is one call over the whole workload."""
+    """One of the entry points beside the layer, timed like the layer: conv
+    (s4_conv_fwd with a given kernel), conv_real (s4_conv_fwd_real), recurrent
+    (s4_recurrent_fwd over the L steps of every row, state carried from call
+    to call) or ctilde (s4_ctilde).  A step is one call over the whole workload."""
     import numpy as np
     import torch
 
@@ -548,12 +549,14 @@ def run_path(args):
     nsets = min(16, max(3, math.ceil(2 * l2 / set_bytes) + 1))
     ins = [torch.from_numpy(in_host).to(dev) for _ in range(nsets)] if in_host is not None else [None] * nsets
     outs = [torch.empty(out_shape, dtype=out_dtype, device=dev) for _ in range(nsets)]
-    Kd = torch.from_numpy(_path_kernel(w)).to(dev) if args.path == "conv_real" else None
+    Kd = torch.from_numpy(_path_kernel(w)).to(dev) if args.path in ("conv", "conv_real") else None
     xs = torch.zeros((Bsz, H, N), dtype=torch.complex64, device=dev)
 
     def call(i):
         j = i % nsets
-        if args.path == "conv_real":
+        if args.path == "conv":
+            s4.s4_conv_fwd(ins[j], Kd, prm["D"], y=outs[j], ws=ws)
+        elif args.path == "conv_real":
             s4.s4_conv_fwd_real(ins[j], Kd, prm["D"], y=outs[j], ws=ws)
         elif args.path == "recurrent":
             s4.s4_recurrent_fwd(prm["Lambda"], prm["P"], prm["Q"], prm["B"], prm["Ctilde"], prm["dt"], prm["D"],
@@ -620,12 +623,14 @@ def run_path(args):
     value = per_call * K / (ms_total / 1e3)
     peaks, peak_src = read_peaks()
     fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    if args.path == "conv_real":
-        byts = Bsz * H * L * (4 + 4) + H * 2 * M * 8
+    if args.path in ("conv", "conv_real"):
+        yb = 4 if args.path == "conv_real" else 8
+        byts = Bsz * H * L * (4 + yb) + H * 2 * M * 8
         ach = byts / (kern[dom]["avg_us"] * 1e-6) / 1e9
-        roof = {"kernel": "conv_real_pair_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
-                "algorithmic": "u 4 B + y 4 B per channel-sample, Hermitian kernel spectrum 16 B per channel-root once"}
+        roof = {"kernel": "conv_real_pair_kernel" if args.path == "conv_real" else "conv_pair_kernel", "bound": "hbm",
+                "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": None,
+                "algorithmic": f"u 4 B + y {yb} B per channel-sample, kernel spectrum 16 B per channel-root once"}
     else:
         steps = Bsz * H * L if args.path == "recurrent" else H * M
         flops = steps * N * (20 + 16 * r)

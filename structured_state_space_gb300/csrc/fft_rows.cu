@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
   bool fin = true;
+  pdl_launch_dependents();  // the convolution may be scheduled; it waits for this grid before reading K2
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
     const bool act = h < H;
@@ -613,7 +614,7 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  bool zero = false, waited = false;
   const int pairs = ((batch + 1) / 2) * H;
   for (int p0 = blockIdx.x * C::ROWS; p0 < pairs; p0 += gridDim.x * C::ROWS) {
     const int p = p0 + slot;
@@ -638,6 +639,11 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
     }
     __syncthreads();
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(bufs, lt);
+    if (!waited) {  // (a programmatic launch) K2 and the status come from the previous kernel
+      pdl_wait();
+      zero = *((volatile const unsigned*)status) != 0u;
+      waited = true;
+    }
     float2 a[PERL][RB];
 #pragma unroll
     for (int s = 0; s < PERL; ++s) {  // last forward pass, product, first inverse pass
@@ -830,7 +836,7 @@ cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K
 
 template <int LOGN>
 static cudaError_t conv_real_launch(const float* u, const float2* K2, const float* D, float* y,
-                                    int batch, int H, int L, const unsigned* st, cudaStream_t s) {
+                                    int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
   const int pairs = ((batch + 1) / 2) * H;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("conv_real", s);
@@ -843,17 +849,17 @@ static cudaError_t conv_real_launch(const float* u, const float2* K2, const floa
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv_real", s);
-    k<<<grid, C::THREADS, smem, s>>>(u, K2, D, y, batch, H, L, st);
+    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L, st);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
-                                  int batch, int H, int L, const unsigned* st, cudaStream_t s) {
+                                  int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
-    return conv_real_launch<X>(u, K2, D, y, batch, H, L, st, s);
+    return conv_real_launch<X>(u, K2, D, y, batch, H, L, st, s, pdl);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
     S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE

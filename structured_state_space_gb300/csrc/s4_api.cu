@@ -102,7 +102,9 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
     e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s);
-    if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s);
+    // programmatic dependent: the convolution transforms its input rows while
+    // the spectrum kernel finishes, and waits for it before reading K2
+    if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s, /*pdl=*/true);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
     if (e == cudaSuccess) e = launch_conv_cluster(logn, u, k2, D, yf, rows, H, L, st, s);
@@ -226,7 +228,7 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
     e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true);
-    if (e == cudaSuccess) e = launch_conv_real_rows(logn, u, k2, D, y, batch, H, L, st, s);
+    if (e == cudaSuccess) e = launch_conv_real_rows(logn, u, k2, D, y, batch, H, L, st, s, /*pdl=*/true);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s, /*realk=*/true);
     if (e == cudaSuccess) e = launch_conv_real_cluster(logn, u, k2, D, y, batch, H, L, st, s);

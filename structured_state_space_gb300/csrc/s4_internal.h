@@ -89,7 +89,7 @@ cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, c
 // Real-output convolution y = Re(K) * u + D u (real y), two batch rows per
 // complex transform; K2 from the spectrum launchers with realk = true.
 cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
-                                  int batch, int H, int L, const unsigned* st, cudaStream_t s);
+                                  int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl = false);
 cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2, const float* D,
                                      float* y, int batch, int H, int L, const unsigned* st,
                                      cudaStream_t s);
