@@ -468,6 +468,7 @@ def run_ours(args):
 
 PATHS = {
     # path: (unit of the rate, timing families of the library, dominant family)
+    "kernel_gen": ("channel-roots/s", ["cauchy", "ifft"], "cauchy"),
     "conv": ("channel-samples/s", ["spectrum", "conv"], "conv"),
     "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
     "recurrent": ("channel-samples/s", ["recurrent"], "recurrent"),
@@ -487,6 +488,9 @@ def _oracle_path_unit(args):
         K = _path_kernel(w)[h].astype(np.complex128)
         O.causal_conv(K.real if path == "conv_real" else K, u[b, h], p["D"][h])
         return w.L
+    if path == "kernel_gen":
+        O.s4_kernel(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["Ctilde"][h], p["dt"][h], w.L)
+        return w.M
     _, Abar, Bbar = O.bilinear(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["dt"][h])
     if path == "recurrent":
         O.recurrence(Abar, Bbar, p["Ctilde"][h], p["D"][h], u[b, h])
@@ -542,6 +546,9 @@ def run_path(args):
     if args.path == "ctilde":
         set_bytes = H * N * 8 * 2
         in_host, out_shape, out_dtype = None, (H, N), torch.complex64
+    elif args.path == "kernel_gen":
+        set_bytes = H * L * 8
+        in_host, out_shape, out_dtype = None, (H, L), torch.complex64
     else:
         out_dtype = torch.float32 if args.path == "conv_real" else torch.complex64
         set_bytes = Bsz * H * L * (4 + (4 if args.path == "conv_real" else 8))
@@ -554,7 +561,9 @@ def run_path(args):
 
     def call(i):
         j = i % nsets
-        if args.path == "conv":
+        if args.path == "kernel_gen":
+            s4.s4_kernel_gen(prm["Lambda"], prm["P"], prm["Q"], prm["B"], prm["Ctilde"], prm["dt"], L, K=outs[j], ws=ws)
+        elif args.path == "conv":
             s4.s4_conv_fwd(ins[j], Kd, prm["D"], y=outs[j], ws=ws)
         elif args.path == "conv_real":
             s4.s4_conv_fwd_real(ins[j], Kd, prm["D"], y=outs[j], ws=ws)
@@ -619,7 +628,7 @@ def run_path(args):
         n, t = s4.timing.read(name)
         kern[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1)}
     s4.timing.reset()
-    per_call = Bsz * H * L if args.path != "ctilde" else H * M
+    per_call = H * M if args.path in ("ctilde", "kernel_gen") else Bsz * H * L
     value = per_call * K / (ms_total / 1e3)
     peaks, peak_src = read_peaks()
     fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
@@ -631,6 +640,13 @@ def run_path(args):
                 "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "traffic": None,
                 "algorithmic": f"u 4 B + y {yb} B per channel-sample, kernel spectrum 16 B per channel-root once"}
+    elif args.path == "kernel_gen":
+        flops = H * M * N * (8 * (r + 1) ** 2 + 6)
+        ach = flops / (kern[dom]["avg_us"] * 1e-6) / 1e12
+        roof = {"kernel": "cauchy_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": ach / fp32_peak, "traffic": None,
+                "algorithmic": f"{8 * (r + 1) ** 2 + 6} flop per (channel, root, pole)",
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
     else:
         steps = Bsz * H * L if args.path == "recurrent" else H * M
         flops = steps * N * (20 + 16 * r)
@@ -667,9 +683,9 @@ def run_path(args):
             "gpu_launches": int(round(sum(v["launches"] for v in kern.values()) / S)) * K,
             "kernels": kern, "roofline": roof, "clocks": clocks, "e2e": e2e}
     if pool is not None:
-        if args.path == "ctilde":
+        if args.path in ("ctilde", "kernel_gen"):
             units = [(args.path, h, 0) for h in range(H)]
-            what = f"{len(units)} channels x M={M} steps"
+            what = f"{len(units)} channels x M={M} " + ("steps" if args.path == "ctilde" else "roots")
         else:
             units = [(args.path, h, b) for h in range(H) for b in range(Bsz)]
             what = f"{len(units)} rows x L={L}"

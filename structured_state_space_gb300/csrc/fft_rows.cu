@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
+  pdl_wait();  // (a programmatic launch) root values and status come from the previous kernel
   const bool zero = *((volatile const unsigned*)status) != 0u;
   const float sc = 1.f / n;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
@@ -750,7 +751,7 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, cons
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("ifft", s);
-    k<<<grid, C::THREADS, smem, s>>>(Khat, K, H, L, st);
+    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, true, Khat, K, H, L, st);
   }
   return cudaGetLastError();
 }
