@@ -91,7 +91,7 @@ def test_layer_matches_oracle(wi, nch, full_rows):
 @pytest.mark.parametrize("N,r,H,L,batch", [
     (4, 1, 3, 1, 2), (4, 1, 3, 2, 2), (5, 2, 2, 3, 1), (6, 1, 5, 16, 3), (8, 2, 4, 100, 2),
     (7, 3, 2, 33, 2), (4, 4, 2, 64, 1), (300, 1, 2, 200, 2), (16, 1, 9, 1000, 3),
-    (16, 2, 3, 5000, 2), (4, 1, 3, 6000, 3), (4, 1, 3, 3001, 3), (12, 1, 2, 16384, 1), (8, 1, 2, 20000, 2),
+    (16, 2, 3, 5000, 2), (4, 1, 3, 6000, 3), (4, 1, 3, 3001, 3), (4, 1, 3, 4000, 3), (12, 1, 2, 16384, 1), (8, 1, 2, 20000, 2),
     (8, 2, 2, 40000, 1),
 ])
 def test_edge_sizes(N, r, H, L, batch):
