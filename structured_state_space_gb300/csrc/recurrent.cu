@@ -234,20 +234,22 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
 }
 
 // C~ = C - (Abar^*)^M C with Abar^* w = 2 G^{-*} w - w.
-template <int RANK, int E>
+template <int RANK, int E, int G>
 __global__ void __launch_bounds__(128) ctilde_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float* __restrict__ dt, const float2* __restrict__ Cv, int H, int N, int M,
     float2* __restrict__ Ct, unsigned* __restrict__ status) {
-  const int h = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (h >= H) return;
+  const int gt = blockIdx.x * blockDim.x + threadIdx.x;
+  if ((gt & ~31) / G >= H) return;  // the whole warp is past the last channel
+  const bool valid = gt / G < H;    // (a surplus group runs on channel 0 and stores nothing)
+  const int h = valid ? gt / G : 0;
+  const int lane = threadIdx.x % G;
   const size_t pb = (size_t)h * N;
   const float delta = dt[h];
   const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
   const float alpha = 0.5f * delta;
   ChanConst<RANK, E> cc;
-  channel_constants<RANK, E>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
+  channel_constants<RANK, E, G>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
   const bool ok = cc.ok && !bad;
   // G^{-*} w = conj(D)^{-1} w - alpha conj(D)^{-1} Q W^{-*} P^* conj(D)^{-1} w
   float2 dc[E], w[E], c0[E], qd[E][RANK], pc[E][RANK], Wh[RANK][RANK];
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
     for (int l = 0; l < RANK; ++l) Wh[i][l] = cconj(cc.Winv[l][i]);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int j = lane + 32 * e;
+    const int j = lane + G * e;
     const bool in = j < N;
     dc[e] = cconj(cc.dinv[e]);
     c0[e] = in ? Cv[pb + j] : make_float2(0.f, 0.f);
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
       for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(pc[e][l], v[e]));
     }
 #pragma unroll
-    for (int l = 0; l < RANK; ++l) s[l] = warp_sum(s[l]);
+    for (int l = 0; l < RANK; ++l) s[l] = warp_sum<G>(s[l]);
     float2 z[RANK];
 #pragma unroll
     for (int i = 0; i < RANK; ++i) {
@@ -297,18 +299,16 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int j = lane + 32 * e;
-    if (j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
+    const int j = lane + G * e;
+    if (valid && j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
   }
-  if (lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+  if (valid && lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
 
 }  // namespace s4dev
 
 namespace s4impl {
 using namespace s4dev;
-
-static int state_lanes(int N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
 
 template <int RANK, int E, int G>
 static cudaError_t rec_launch(const float2* Lam, const float2* P, const float2* Q, const float2* B,
@@ -335,35 +335,28 @@ static cudaError_t rec_dispatch(const float2* Lam, const float2* P, const float2
   return rec_launch<RANK, 8, 32>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
 }
 
-template <int RANK, int E>
+template <int RANK, int E, int G>
 static cudaError_t ct_launch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                              const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
                              cudaStream_t s) {
+  const long long threads = (long long)H * G;
   TimedLaunch tl("ctilde", s);
-  ctilde_kernel<RANK, E><<<(H + 3) / 4, 128, 0, s>>>(Lam, P, Q, dt, C, H, N, M, Ct, st);
+  ctilde_kernel<RANK, E, G><<<(unsigned)((threads + 127) / 128), 128, 0, s>>>(Lam, P, Q, dt, C, H, N, M, Ct, st);
   return cudaGetLastError();
 }
 
-#define S4_DISPATCH_RE(F, r, N, ...)                                     \
-  switch ((r) * 16 + state_lanes(N)) {                                   \
-    case 17: return F<1, 1>(__VA_ARGS__);                                \
-    case 18: return F<1, 2>(__VA_ARGS__);                                \
-    case 20: return F<1, 4>(__VA_ARGS__);                                \
-    case 24: return F<1, 8>(__VA_ARGS__);                                \
-    case 33: return F<2, 1>(__VA_ARGS__);                                \
-    case 34: return F<2, 2>(__VA_ARGS__);                                \
-    case 36: return F<2, 4>(__VA_ARGS__);                                \
-    case 40: return F<2, 8>(__VA_ARGS__);                                \
-    case 49: return F<3, 1>(__VA_ARGS__);                                \
-    case 50: return F<3, 2>(__VA_ARGS__);                                \
-    case 52: return F<3, 4>(__VA_ARGS__);                                \
-    case 56: return F<3, 8>(__VA_ARGS__);                                \
-    case 65: return F<4, 1>(__VA_ARGS__);                                \
-    case 66: return F<4, 2>(__VA_ARGS__);                                \
-    case 68: return F<4, 4>(__VA_ARGS__);                                \
-    case 72: return F<4, 8>(__VA_ARGS__);                                \
-    default: return cudaErrorInvalidValue;                               \
-  }
+// One warp per channel: C~ runs one serial chain of M steps per channel with
+// only H chains in flight, so it is latency-bound and wants the most lanes
+// (the fewest elements per lane) on each chain.
+template <int RANK>
+static cudaError_t ct_dispatch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                               const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                               cudaStream_t s) {
+  if (N <= 32) return ct_launch<RANK, 1, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (N <= 64) return ct_launch<RANK, 2, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (N <= 128) return ct_launch<RANK, 4, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  return ct_launch<RANK, 8, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+}
 
 cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                              const float2* C, const float* dt, const float* D, const float* u,
@@ -381,7 +374,13 @@ cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                           const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
                           cudaStream_t s) {
-  S4_DISPATCH_RE(ct_launch, r, N, Lam, P, Q, dt, C, H, N, M, Ct, st, s)
+  switch (r) {
+    case 1: return ct_dispatch<1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 2: return ct_dispatch<2>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 3: return ct_dispatch<3>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 4: return ct_dispatch<4>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace s4impl
