@@ -256,20 +256,45 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(Ro
     float scale, unsigned* __restrict__ status) {
   using C = RowCfg<LOGM + 1>;
   constexpr int M = 1 << LOGM, n = C::n, T = C::T;
-  extern __shared__ float2 smem[];
+  constexpr bool STW = kspec_stage_tw(LOGM);
+  constexpr int TWI = kspec_tw_inv_len(LOGM), TWF = kspec_tw_fwd_len(LOGM);
+  static_assert(!STW || (TWI % 2 == 0 && TWF % 2 == 0 && tw_offset(LOGM, true, 1) % 2 == 0 &&
+                         tw_offset(LOGM + 1, false, 1) % 2 == 0),
+                "staged tables: 16-byte aligned offsets and sizes");
+  extern __shared__ __align__(16) float2 smem[];
+  __shared__ unsigned long long twbar;
   const int slot = threadIdx.x / T, lt = threadIdx.x % T;
   float2* buf = smem + slot * C::PADN;
+  float2* twi = smem + kspec_tw_base(C::ROWS * C::PADN);  // STW: inverse-plan tables, then forward-plan
+  float2* twf = twi + TWI;
+  bool stall = false;
+  if constexpr (STW) {  // the tables do not depend on the previous kernel: copy them now
+    if (threadIdx.x == 0) {
+      mbar_init(&twbar, 1u);
+      fence_mbar_init();
+      mbar_expect_tx(&twbar, (unsigned)((TWI + TWF) * sizeof(float2)));
+      bulk_g2s(twi, TwTab<LOGM>::ptr() + tw_offset(LOGM, true, 1), (unsigned)(TWI * sizeof(float2)), &twbar);
+      bulk_g2s(twf, TwTab<LOGM + 1>::ptr() + tw_offset(LOGM + 1, false, 1), (unsigned)(TWF * sizeof(float2)),
+               &twbar);
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+  }
   pdl_launch_dependents();
   pdl_wait();  // root values and status come from the previous kernel
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  bool zero = *((volatile const unsigned*)status) != 0u;
   bool fin = true;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
     const bool act = h < H;
-    kspec_row<LOGM>(Khat + (size_t)(act ? h : 0) * M, K + (size_t)(act ? h : 0) * L,
-                    K2 + (size_t)(act ? h : 0) * n, L, scale, zero, act, buf, lt, fin);
+    kspec_row<LOGM, STW>(Khat + (size_t)(act ? h : 0) * M, K + (size_t)(act ? h : 0) * L,
+                         K2 + (size_t)(act ? h : 0) * n, L, scale, zero || stall, act, buf, lt, fin, twi,
+                         twf, &twbar, &stall);
   }
   if (!fin) atomicOr(status, ST_NONFINITE);
+  if constexpr (STW) {
+    if (stall) mbar_wait(&twbar, 0u);  // one more bounded wait for the copy in flight
+  }
+  if (stall && threadIdx.x == 0) atomicOr(status, ST_STALL);
 }
 
 // Resident CTAs per SM the convolution is compiled for: 512 threads per SM
@@ -809,7 +834,9 @@ static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H
                                 cudaStream_t s) {
   using C = RowCfg<LOGM + 1>;
   const float scale = 1.f / (float)(4 << LOGM);  // 1/(2n), n = 2M
-  const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
+  const size_t smem = sizeof(float2) * (kspec_stage_tw(LOGM) ? (size_t)kspec_tw_base(C::ROWS * C::PADN) +
+                                                                  kspec_tw_inv_len(LOGM) + kspec_tw_fwd_len(LOGM)
+                                                            : (size_t)C::ROWS * C::PADN);
   auto k = kspec_kernel<LOGM>;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;

@@ -31,7 +31,8 @@ struct PassIdx {
 
 // Twiddle factors of pass IDX for butterfly k, applied to a[1..R-1]
 // (conjugated for an inverse pass).  `w` is filled from the table first so
-// several rows that share the butterfly index can reuse it.
+// several rows that share the butterfly index can reuse it.  With SMEM the
+// table is read from a shared-memory copy `sm` of this pass's table.
 template <int LOGN, int IDX, bool INV>
 struct PassTw {
   static constexpr int R = plan_radix(LOGN, IDX, INV);
@@ -40,18 +41,21 @@ struct PassTw {
   __device__ __forceinline__ static const float2* table() {
     return TwTab<LOGN>::ptr() + tw_offset(LOGN, INV, IDX);
   }
+  // offset of this pass's table from the plan's pass-1 table
+  static constexpr int REL = tw_offset(LOGN, INV, IDX) - tw_offset(LOGN, INV, 1);
   // w[q] = w^(k q) for q = 1..R-1
-  __device__ __forceinline__ static void load(float2 (&w)[R], int k) {
+  template <bool SMEM = false>
+  __device__ __forceinline__ static void load(float2 (&w)[R], int k, const float2* sm = nullptr) {
     if constexpr (ROWS) {
-      const float4* col = reinterpret_cast<const float4*>(table()) + k;
+      const float4* col = reinterpret_cast<const float4*>(SMEM ? sm : table()) + k;
 #pragma unroll
       for (int v = 0; v < R / 2; ++v) {
-        const float4 t = __ldg(col + v * P);
+        const float4 t = SMEM ? col[v * P] : __ldg(col + v * P);
         w[1 + 2 * v] = make_float2(t.x, t.y);
         if (2 + 2 * v < R) w[2 + 2 * v] = make_float2(t.z, t.w);
       }
     } else {
-      w[1] = __ldg(table() + k);
+      w[1] = SMEM ? sm[k] : __ldg(table() + k);
 #pragma unroll
       for (int q = 2; q < R; ++q) {
         const int hb = highbit(q);
@@ -67,9 +71,11 @@ struct PassTw {
 
 // One shared-memory Stockham pass of the plan, over NR rows that share the
 // thread layout (buffers bufs[0..NR-1]); T threads per row group do the work
-// (threads with lt >= T only take part in the barriers).
-template <int LOGN, int IDX, bool INV, int T, int NR>
-__device__ __forceinline__ void pass_rows(float2* const* bufs, int lt) {
+// (threads with lt >= T only take part in the barriers).  With STW the
+// twiddles come from `twsm`, a shared-memory copy of the plan's tables from
+// pass 1 on.
+template <int LOGN, int IDX, bool INV, int T, int NR, bool STW = false>
+__device__ __forceinline__ void pass_rows(float2* const* bufs, int lt, const float2* twsm = nullptr) {
   constexpr int N = 1 << LOGN;
   constexpr int R = plan_radix(LOGN, IDX, INV), P = plan_p(LOGN, IDX, INV);
   constexpr int NB = N / R, PER = NB / T;
@@ -88,7 +94,7 @@ __device__ __forceinline__ void pass_rows(float2* const* bufs, int lt) {
       for (int q = 0; q < R; ++q) a[r][s][q] = bufs[r][IX::rd(i, q)];
     if constexpr (P > 1) {
       float2 w[R];
-      TW::load(w, i & (P - 1));
+      TW::template load<STW>(w, i & (P - 1), STW ? twsm + TW::REL : nullptr);
 #pragma unroll
       for (int r = 0; r < NR; ++r) TW::apply(a[r][s], w);
     }
@@ -110,11 +116,11 @@ __device__ __forceinline__ void pass_rows(float2* const* bufs, int lt) {
   __syncthreads();
 }
 
-template <int LOGN, bool INV, int IDX, int LAST, int T, int NR>
-__device__ __forceinline__ void passes_rows(float2* const* bufs, int lt) {
+template <int LOGN, bool INV, int IDX, int LAST, int T, int NR, bool STW = false>
+__device__ __forceinline__ void passes_rows(float2* const* bufs, int lt, const float2* twsm = nullptr) {
   if constexpr (IDX <= LAST) {
-    pass_rows<LOGN, IDX, INV, T, NR>(bufs, lt);
-    passes_rows<LOGN, INV, IDX + 1, LAST, T, NR>(bufs, lt);
+    pass_rows<LOGN, IDX, INV, T, NR, STW>(bufs, lt, twsm);
+    passes_rows<LOGN, INV, IDX + 1, LAST, T, NR, STW>(bufs, lt, twsm);
   }
 }
 

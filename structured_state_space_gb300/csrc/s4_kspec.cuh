@@ -1,11 +1,11 @@
 // One channel of the layer path's inverse transform + kernel spectrum:
 //   K = first L of (1/M) iFFT_M(Khat)      (written out)
 //   K2 = scale FFT_2M(K zero-padded to 2M)  (written out, natural order)
-// from one shared-memory row of padded_len(2M) entries.  Used by the
-// stand-alone kspec kernel and by the root-value kernel's last CTA per
-// channel.  "Recurrent, LSTM, and structured state-space models", filter
-// mode (first L coefficients of the inverse radix-two transform) and
-// "Roots-of-unity orthogonality and radix-two FFT cost" (zero padding).
+// from one shared-memory row of padded_len(2M) entries (the body of the
+// layer path's kspec kernel).  "Recurrent, LSTM, and structured state-space
+// models", filter mode (first L coefficients of the inverse radix-two
+// transform) and "Roots-of-unity orthogonality and radix-two FFT cost" (zero
+// padding).
 #pragma once
 #include "s4_fft.cuh"
 
@@ -20,13 +20,34 @@ struct KspecCfg {
   static constexpr int PADN = padded_len(n);
 };
 
+// Twiddle tables a kspec CTA copies into shared memory at its start (the
+// inverse plan of M and the forward plan of 2M, each from pass 1 on), so that
+// one copy, in flight beside the root-value loads, replaces a first-touch L2
+// read in each pass.  Only where the copy is small (M <= 1024: 27 KiB) and
+// does not cost resident CTAs.
+__host__ __device__ constexpr bool kspec_stage_tw(int logm) { return logm <= 10; }
+__host__ __device__ constexpr int kspec_tw_inv_len(int logm) {
+  return tw_offset(logm, true, plan_npass(logm)) - tw_offset(logm, true, 1);
+}
+__host__ __device__ constexpr int kspec_tw_fwd_len(int logm) {
+  return tw_offset(logm + 1, false, plan_npass(logm + 1)) - tw_offset(logm + 1, false, 1);
+}
+// float2 offset of the staged tables after `rows_len` entries of row buffers
+// (rounded up to 16 bytes for the bulk copies)
+__host__ __device__ constexpr int kspec_tw_base(int rows_len) { return (rows_len + 1) & ~1; }
+
 // All threads with lt < nthreads_row take part in the barriers; lt >= T idle.
 // `zero`: write zeros (a device-detected condition).  Khat is read through
-// L2 (it may have been written by other SMs of the same grid).
-template <int LOGM>
+// L2 (it may have been written by other SMs of the same grid).  With STW the
+// twiddles come from the shared-memory copies twi (inverse plan of M) and twf
+// (forward plan of 2M), which arrive on the mbarrier `twbar` (phase 0); a
+// wait that gives up sets `stall`.
+template <int LOGM, bool STW = false>
 __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float2* __restrict__ Krow,
                                           float2* __restrict__ K2row, int L, float scale, bool zero,
-                                          bool act, float2* buf, int lt, bool& fin) {
+                                          bool act, float2* buf, int lt, bool& fin,
+                                          const float2* twi = nullptr, const float2* twf = nullptr,
+                                          unsigned long long* twbar = nullptr, bool* stall = nullptr) {
   using KC = KspecCfg<LOGM>;
   constexpr int LOGN = KC::LOGN, M = KC::M, n = KC::n, T = KC::T, TI = KC::TI;
   static_assert(TI <= T, "thread split");
@@ -58,7 +79,13 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
     }
   }
   __syncthreads();
-  passes_rows<LOGM, true, 1, NPI - 2, TI, 1>(bufs, lt);
+  if constexpr (STW) {
+    if (!mbar_wait(twbar, 0u)) {  // tables missing: the row is written as zeros
+      *stall = true;
+      zero = true;
+    }
+  }
+  passes_rows<LOGM, true, 1, NPI - 2, TI, 1, STW>(bufs, lt, twi);
   float2 kv[PERIL][RIL];
   if (lt < TI) {  // last inverse pass: K in registers
 #pragma unroll
@@ -67,7 +94,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       float2 w[RIL];
 #pragma unroll
       for (int q = 0; q < RIL; ++q) kv[s][q] = buf[IXIL::rd(i, q)];
-      TWIL::load(w, i);
+      TWIL::template load<STW>(w, i, STW ? twi + TWIL::REL : nullptr);
       TWIL::apply(kv[s], w);
       dft<RIL, true>(kv[s]);
     }
@@ -109,7 +136,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
     }
     __syncthreads();
   }
-  passes_rows<LOGN, false, 1, NPF - 2, T, 1>(bufs, lt);
+  passes_rows<LOGN, false, 1, NPF - 2, T, 1, STW>(bufs, lt, twf);
   if (lt < T) {
 #pragma unroll
     for (int s = 0; s < PERL; ++s) {  // last forward pass -> K2
@@ -117,7 +144,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       float2 a[RB], w[RB];
 #pragma unroll
       for (int q = 0; q < RB; ++q) a[q] = buf[IXFL::rd(i, q)];
-      TWFL::load(w, i);
+      TWFL::template load<STW>(w, i, STW ? twf + TWFL::REL : nullptr);
       TWFL::apply(a, w);
       dft<RB, false>(a);
       if (act) {
