@@ -11,7 +11,9 @@
 //
 // Since I + alpha A = 2I - G, one step is x_t = G^{-1}(2 x_{t-1} + Delta B u_t)
 // - x_{t-1}: one Woodbury solve, i.e. one reduction of r values over the N
-// states, plus one reduction for y_t.  Likewise Abar^* = 2 G^{-*} - I, and
+// states, plus one reduction for y_t (the recurrent kernel folds D^{-1} into
+// its per-state constants, so a step touches each state with three complex
+// multiply-adds and one complex product).  Likewise Abar^* = 2 G^{-*} - I, and
 // G^* = diag(conj d_j) + alpha Q P^* has the correction W^* (W = I_r + alpha
 // Q^* D^{-1} P), so C~ = C - (Abar^*)^M C takes M solves with W^{-*}.
 //
@@ -174,39 +176,51 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
   ChanConst<RANK, E> cc;
   channel_constants<RANK, E, G>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
   const bool ok = cc.ok && !bad;
-  float2 xs[E], eb[E], pd[E][RANK], qc[E][RANK], cc_[E];
+  // With w = D^{-1}(2 x + Delta B u) substituted, one step is
+  //   s = sum_j h_j x_j + c0 u,  h_j = 2 conj(Q_j) / d_j,  c0 = sum_j conj(Q_j) Delta B_j / d_j,
+  //   z = W^{-1} s,  x'_j = a_j x_j + e_j u - pd_j z,  a_j = 2/d_j - 1, e_j = Delta B_j / d_j,
+  // and the next step's partial s is accumulated while x' is formed.
+  float2 xs[E], av[E], eb[E], pd[E][RANK], hq[E][RANK], cc_[E], c0[RANK];
+#pragma unroll
+  for (int l = 0; l < RANK; ++l) c0[l] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
     const bool in = j < N;
+    const float2 di = cc.dinv[e];  // zero outside the states
     xs[e] = in ? x[(size_t)warp * N + j] : make_float2(0.f, 0.f);
-    eb[e] = in ? cscale(cmul(cc.dinv[e], Bv[pb + j]), delta) : make_float2(0.f, 0.f);  // D^{-1} Delta B
+    eb[e] = in ? cscale(cmul(di, Bv[pb + j]), delta) : make_float2(0.f, 0.f);
+    av[e] = in ? make_float2(fmaf(2.f, di.x, -1.f), 2.f * di.y) : make_float2(0.f, 0.f);
     cc_[e] = in ? cconj(Cv[pb + j]) : make_float2(0.f, 0.f);
 #pragma unroll
     for (int l = 0; l < RANK; ++l) {
-      pd[e][l] = in ? cscale(cmul(cc.dinv[e], Pm[(pb + j) * RANK + l]), alpha) : make_float2(0.f, 0.f);
-      qc[e][l] = in ? cconj(Qm[(pb + j) * RANK + l]) : make_float2(0.f, 0.f);
+      const float2 qcl = in ? cconj(Qm[(pb + j) * RANK + l]) : make_float2(0.f, 0.f);
+      pd[e][l] = in ? cscale(cmul(di, Pm[(pb + j) * RANK + l]), alpha) : make_float2(0.f, 0.f);
+      hq[e][l] = cscale(cmul(qcl, di), 2.f);
+      c0[l] = cadd(c0[l], cmul(qcl, eb[e]));
     }
   }
+#pragma unroll
+  for (int l = 0; l < RANK; ++l) c0[l] = warp_sum<G>(c0[l]);
   const float dsk = Dskip[h];
   const float* ur = u + (size_t)warp * L;
   float2* yr = y + (size_t)warp * L;
+  float2 s[RANK];  // this lane's part of sum_j h_j x_j for the coming step
+#pragma unroll
+  for (int l = 0; l < RANK; ++l) {
+    s[l] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[l] = cadd(s[l], cmul(hq[e][l], xs[e]));
+  }
 #pragma unroll kRecurrentUnroll
   for (int t = 0; t < L; ++t) {
     const float ut = ur[t];
-    float2 w[E], s[RANK];
-#pragma unroll
-    for (int l = 0; l < RANK; ++l) s[l] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < E; ++e) {  // w = D^{-1}(2 x + Delta B u)
-      const float2 dx = cmul(cc.dinv[e], xs[e]);
-      w[e] = make_float2(fmaf(2.f, dx.x, eb[e].x * ut), fmaf(2.f, dx.y, eb[e].y * ut));
-#pragma unroll
-      for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(qc[e][l], w[e]));
-    }
     float2 z[RANK];
 #pragma unroll
-    for (int l = 0; l < RANK; ++l) s[l] = warp_sum<G>(s[l]);
+    for (int l = 0; l < RANK; ++l) {
+      s[l] = warp_sum<G>(s[l]);
+      s[l] = make_float2(fmaf(c0[l].x, ut, s[l].x), fmaf(c0[l].y, ut, s[l].y));
+    }
 #pragma unroll
     for (int i = 0; i < RANK; ++i) {
       z[i] = make_float2(0.f, 0.f);
@@ -215,12 +229,17 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     }
     float2 yp = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < E; ++e) {  // x = w - alpha D^{-1} P z - x_prev
-      float2 v = csub(w[e], xs[e]);
+    for (int l = 0; l < RANK; ++l) s[l] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {  // x = a x + e u - pd z
+      float2 v = cmul(av[e], xs[e]);
+      v = make_float2(fmaf(eb[e].x, ut, v.x), fmaf(eb[e].y, ut, v.y));
 #pragma unroll
       for (int l = 0; l < RANK; ++l) v = csub(v, cmul(pd[e][l], z[l]));
       xs[e] = v;
       yp = cadd(yp, cmul(cc_[e], v));
+#pragma unroll
+      for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(hq[e][l], v));
     }
     yp = warp_sum<G>(yp);
     if (valid && lane == 0) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
