@@ -253,11 +253,24 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
 }
 
 // C~ = C - (Abar^*)^M C with Abar^* w = 2 G^{-*} w - w.
-template <int RANK, int E, int G>
+//
+// G^{-*} w = conj(D)^{-1} w - alpha conj(D)^{-1} Q W^{-*} P^* conj(D)^{-1} w, so
+// Abar^* = diag(a) - U V^T with a_j = 2/conj(d_j) - 1, U = 2 alpha conj(D)^{-1} Q W^{-*}
+// and V = conj(D)^{-1} conj(P) (V^T w = P^* conj(D)^{-1} w): diagonal plus rank r.
+// Its square is again diagonal plus low rank,
+//   (diag(a) - U V^T)^2 = diag(a^2) - [aU - U K, U] [V, aV]^T,  K = V^T U,
+// so LOGP squarings give Abar^{*P} (P = 2^LOGP) at rank P r, and M/P steps of
+// w <- a w - U (V^T w) finish the power: each step's P r reductions over the N
+// states share one pass of shuffle rounds, so the chain of dependent
+// reductions is M/P long instead of M, for the same arithmetic per original
+// step (about 8 r complex flop pairs per state).
+template <int RANK, int E, int G, int LOGP>
 __global__ void __launch_bounds__(128) ctilde_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float* __restrict__ dt, const float2* __restrict__ Cv, int H, int N, int M,
     float2* __restrict__ Ct, unsigned* __restrict__ status) {
+  constexpr int P = 1 << LOGP, KP = RANK * P;
+  constexpr int KH = KP / 2 > 0 ? KP / 2 : 1;  // columns before the last squaring
   const int gt = blockIdx.x * blockDim.x + threadIdx.x;
   if ((gt & ~31) / G >= H) return;  // the whole warp is past the last channel
   const bool valid = gt / G < H;    // (a surplus group runs on channel 0 and stores nothing)
@@ -270,51 +283,94 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
   ChanConst<RANK, E> cc;
   channel_constants<RANK, E, G>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
   const bool ok = cc.ok && !bad;
-  // G^{-*} w = conj(D)^{-1} w - alpha conj(D)^{-1} Q W^{-*} P^* conj(D)^{-1} w
-  float2 dc[E], w[E], c0[E], qd[E][RANK], pc[E][RANK], Wh[RANK][RANK];
-#pragma unroll
-  for (int i = 0; i < RANK; ++i)
-#pragma unroll
-    for (int l = 0; l < RANK; ++l) Wh[i][l] = cconj(cc.Winv[l][i]);
+  // factors of Abar^*: columns 0..RANK-1 of U, V
+  float2 av[E], w[E], c0[E], Uf[E][KP], Vf[E][KP];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
     const bool in = j < N;
-    dc[e] = cconj(cc.dinv[e]);
+    const float2 dc = cconj(cc.dinv[e]);  // zero outside the states
+    av[e] = in ? make_float2(fmaf(2.f, dc.x, -1.f), 2.f * dc.y) : make_float2(0.f, 0.f);
     c0[e] = in ? Cv[pb + j] : make_float2(0.f, 0.f);
     w[e] = c0[e];
+    float2 q2[RANK];
+#pragma unroll
+    for (int i = 0; i < RANK; ++i)
+      q2[i] = in ? cscale(cmul(dc, Qm[(pb + j) * RANK + i]), 2.f * alpha) : make_float2(0.f, 0.f);
 #pragma unroll
     for (int l = 0; l < RANK; ++l) {
-      qd[e][l] = in ? cscale(cmul(dc[e], Qm[(pb + j) * RANK + l]), alpha) : make_float2(0.f, 0.f);
-      pc[e][l] = in ? cconj(Pm[(pb + j) * RANK + l]) : make_float2(0.f, 0.f);
+      float2 u = make_float2(0.f, 0.f);  // (2 alpha conj(D)^{-1} Q W^{-*})_{j l}
+#pragma unroll
+      for (int i = 0; i < RANK; ++i) u = cadd(u, cmul(q2[i], cconj(cc.Winv[l][i])));
+      Uf[e][l] = u;
+      Vf[e][l] = in ? cmul(cconj(Pm[(pb + j) * RANK + l]), dc) : make_float2(0.f, 0.f);
     }
   }
-  for (int it = 0; it < M; ++it) {
-    float2 v[E], s[RANK];
+  // LOGP squarings: rank k -> 2k
 #pragma unroll
-    for (int l = 0; l < RANK; ++l) s[l] = make_float2(0.f, 0.f);
+  for (int lev = 0; lev < LOGP; ++lev) {
+    const int k = RANK << lev;
+    float2 Km[KH][KH];  // K = V^T U over the first k columns
+#pragma unroll
+    for (int m = 0; m < KH; ++m)
+#pragma unroll
+      for (int c = 0; c < KH; ++c) {
+        if (m < k && c < k) {
+          float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) t = cadd(t, cmul(Vf[e][m], Uf[e][c]));
+          Km[m][c] = warp_sum<G>(t);
+        }
+      }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      v[e] = cmul(dc[e], w[e]);
+      float2 un[KH];
 #pragma unroll
-      for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(pc[e][l], v[e]));
+      for (int c = 0; c < KH; ++c) {
+        if (c < k) {
+          float2 t = cmul(av[e], Uf[e][c]);
+#pragma unroll
+          for (int m = 0; m < KH; ++m)
+            if (m < k) t = csub(t, cmul(Uf[e][m], Km[m][c]));
+          un[c] = t;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < KH; ++c) {
+        if (c < k) {
+          Uf[e][k + c] = Uf[e][c];
+          Uf[e][c] = un[c];
+          Vf[e][k + c] = cmul(av[e], Vf[e][c]);
+        }
+      }
+      av[e] = cmul(av[e], av[e]);
+    }
+  }
+  float2 sv[KP];  // this lane's part of V^T w for the coming step
+#pragma unroll
+  for (int m = 0; m < KP; ++m) {
+    sv[m] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) sv[m] = cadd(sv[m], cmul(Vf[e][m], w[e]));
+  }
+  const int steps = M >> LOGP;
+  for (int it = 0; it < steps; ++it) {
+#pragma unroll
+    for (int m = 0; m < KP; ++m) sv[m] = warp_sum<G>(sv[m]);
+    float2 sn[KP];
+#pragma unroll
+    for (int m = 0; m < KP; ++m) sn[m] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {  // w <- Abar^{*P} w
+      float2 g = cmul(av[e], w[e]);
+#pragma unroll
+      for (int m = 0; m < KP; ++m) g = csub(g, cmul(Uf[e][m], sv[m]));
+      w[e] = g;
+#pragma unroll
+      for (int m = 0; m < KP; ++m) sn[m] = cadd(sn[m], cmul(Vf[e][m], g));
     }
 #pragma unroll
-    for (int l = 0; l < RANK; ++l) s[l] = warp_sum<G>(s[l]);
-    float2 z[RANK];
-#pragma unroll
-    for (int i = 0; i < RANK; ++i) {
-      z[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int l = 0; l < RANK; ++l) z[i] = cadd(z[i], cmul(Wh[i][l], s[l]));
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) {  // w <- 2 G^{-*} w - w
-      float2 g = v[e];
-#pragma unroll
-      for (int l = 0; l < RANK; ++l) g = csub(g, cmul(qd[e][l], z[l]));
-      w[e] = make_float2(fmaf(2.f, g.x, -w[e].x), fmaf(2.f, g.y, -w[e].y));
-    }
+    for (int m = 0; m < KP; ++m) sv[m] = sn[m];
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -354,27 +410,44 @@ static cudaError_t rec_dispatch(const float2* Lam, const float2* P, const float2
   return rec_launch<RANK, 8, 32>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
 }
 
-template <int RANK, int E, int G>
+template <int RANK, int E, int G, int LOGP>
 static cudaError_t ct_launch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                              const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
                              cudaStream_t s) {
   const long long threads = (long long)H * G;
   TimedLaunch tl("ctilde", s);
-  ctilde_kernel<RANK, E, G><<<(unsigned)((threads + 127) / 128), 128, 0, s>>>(Lam, P, Q, dt, C, H, N, M, Ct, st);
+  ctilde_kernel<RANK, E, G, LOGP><<<(unsigned)((threads + 127) / 128), 128, 0, s>>>(Lam, P, Q, dt, C, H, N, M, Ct, st);
   return cudaGetLastError();
 }
 
-// One warp per channel: C~ runs one serial chain of M steps per channel with
-// only H chains in flight, so it is latency-bound and wants the most lanes
-// (the fewest elements per lane) on each chain.
+// Look-ahead of 2^LOGP steps per reduction pass, as far as the registers hold
+// the factors (E x 2^LOGP x r <= 16 complex columns per lane) and M allows.
+constexpr int ct_logp(int rank, int e) {
+  int lp = 0;
+  while (lp < 4 && e * (rank << (lp + 1)) <= 16) ++lp;
+  return lp;
+}
+
+template <int RANK, int E>
+static cudaError_t ct_launch_p(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                               const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                               cudaStream_t s) {
+  constexpr int LP = ct_logp(RANK, E);
+  if (M % (1 << LP) == 0) return ct_launch<RANK, E, 32, LP>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  return ct_launch<RANK, E, 32, 0>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+}
+
+// One warp per channel: C~ runs one chain of M / 2^LOGP dependent steps per
+// channel with only H chains in flight, so it is latency-bound and wants the
+// most lanes (the fewest elements per lane) on each chain.
 template <int RANK>
 static cudaError_t ct_dispatch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                                const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
                                cudaStream_t s) {
-  if (N <= 32) return ct_launch<RANK, 1, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-  if (N <= 64) return ct_launch<RANK, 2, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-  if (N <= 128) return ct_launch<RANK, 4, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-  return ct_launch<RANK, 8, 32>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (N <= 32) return ct_launch_p<RANK, 1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (N <= 64) return ct_launch_p<RANK, 2>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (N <= 128) return ct_launch_p<RANK, 4>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  return ct_launch_p<RANK, 8>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
 }
 
 cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,

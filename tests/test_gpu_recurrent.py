@@ -39,7 +39,10 @@ def _with_c(w, seed):
     return p
 
 
-@pytest.mark.parametrize("N,r,H,L", [(4, 1, 3, 64), (64, 1, 8, 1024), (64, 2, 4, 300), (256, 1, 3, 4096), (33, 3, 2, 100)])
+# look-ahead of 16, 8, 4, 2 steps per reduction pass; (16, 4, ...) at rank 4;
+# (8, 1, 2, 3) has M = 4, below its look-ahead, and takes single steps
+@pytest.mark.parametrize("N,r,H,L", [(4, 1, 3, 64), (64, 1, 8, 1024), (64, 2, 4, 300), (256, 1, 3, 4096),
+                                     (33, 3, 2, 100), (16, 4, 2, 200), (8, 1, 2, 3), (128, 2, 2, 64)])
 def test_ctilde_matches_oracle(N, r, H, L):
     w = W.custom(N, r, H, L, 1, seed=7 * N + L)
     p = _with_c(w, 11)
