@@ -226,6 +226,28 @@ def oracle_rate(pool, procs, channels):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def fp32_probe(dev, fp32_peak, iters=4096, reps=5):
+    """FP32 issue rate the SMs sustain (the library's FFMA probe, 8 CTAs of 256
+    threads per SM), beside the peak derived from unit counts and clocks."""
+    import torch
+    import structured_state_space_gb300 as s4
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = sms * 8
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        s4.s4_fp32_probe(out, blocks, iters)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    flop = sum(s4.s4_fp32_probe(out, blocks, iters) for _ in range(reps))
+    e1.record()
+    torch.cuda.synchronize()
+    tf = flop / (e0.elapsed_time(e1) / 1e3) / 1e12
+    return {"achieved": tf, "unit": "TFLOP/s", "frac_of_derived_peak": tf / fp32_peak,
+            "how": f"s4_fp32_probe: {blocks} CTAs x 256 threads x {iters} iterations of 8 independent FFMA "
+                   f"chains, {reps} launches timed with CUDA events"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -456,6 +478,7 @@ def run_ours(args):
                             "algorithmic": "15 M log2(2M) + 16 M flop per batch row (real-input forward, "
                                            "complex inverse, 5 n log2 n per transform)"}
     roof["peak_kind"] = f"of {peak_src}"
+    roof["fp32_probe"] = fp32_probe(dev, fp32_peak)
     if dom != "cauchy" and kern.get("cauchy", {}).get("launches"):
         # the root-value kernel's FP32 fraction, beside the dominant kernel's
         cach = H * M * N * (8 * (r + 1) ** 2 + 6) / (kern["cauchy"]["avg_us"] * 1e-6) / 1e12

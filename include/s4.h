@@ -234,13 +234,25 @@ const char* s4_status_str(s4_status st);
 /* Optional per-kernel timing: when enabled, every kernel launch of the
  * library is bracketed by CUDA events recorded on its launch stream.
  * s4_timing_read syncs those events and returns, for the kernel family
- * `name` ("cauchy", "ifft", "spectrum", "conv", "tau"), the number of
- * launches and their summed duration in milliseconds since the last reset.
- * Timing state is per process; it is meant for benchmarks, not for use
- * from several host threads at once. */
+ * `name` ("cauchy", "ifft", "spectrum", "kspec", "conv", "conv_real",
+ * "recurrent", "ctilde"), the number of launches and their summed duration
+ * in milliseconds since the last reset.  Timing state is per process; it is
+ * meant for benchmarks, not for use from several host threads at once. */
 void s4_timing_enable(int on);
 void s4_timing_reset(void);
 int  s4_timing_read(const char* name, int* launches, double* total_ms);
+
+/* Measurement aid, outside the method: an FP32 issue-rate probe.  Launches
+ * `blocks` CTAs of 256 threads on `stream`; every thread runs `iters`
+ * iterations (rounded up to a multiple of 8) of 8 independent fused
+ * multiply-adds, 16 flop each, so one launch executes
+ * blocks x 256 x iters x 16 flop, and each thread writes one float to `out`
+ * (device memory, blocks x 256 floats, caller-owned) so that nothing is
+ * elided.  The caller times the launch (CUDA events on `stream`) to compare
+ * the FP32 peak derived from unit counts and clocks with the rate the SMs
+ * sustain.  Asynchronous; S4_ERR_INVALID_ARG for a null `out`, blocks < 1 or
+ * iters < 1; S4_ERR_CUDA if the launch fails. */
+s4_status s4_fp32_probe(float* out, int blocks, int iters, void* stream);
 
 #ifdef __cplusplus
 }

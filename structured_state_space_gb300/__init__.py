@@ -40,7 +40,7 @@ ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
     "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd", "s4_conv_fwd_real",
-    "s4_hippo_dplr",
+    "s4_hippo_dplr", "s4_fp32_probe",
 ]
 
 HIPPO_KINDS = {"legs": 0, "legt": 1, "lagt": 2}
@@ -92,6 +92,8 @@ def load(path: str | None = None):
     lib.s4_recurrent_fwd.restype = i32
     lib.s4_hippo_dplr.argtypes = [i32, i32, ctypes.c_double] + [vp] * 6 + [i32p]
     lib.s4_hippo_dplr.restype = i32
+    lib.s4_fp32_probe.argtypes = [vp, i32, i32, vp]
+    lib.s4_fp32_probe.restype = i32
     _lib = lib
     return lib
 
@@ -296,6 +298,18 @@ def s4_hippo_dplr(kind, N, theta=1.0, B=None, C=None):
     if Ct is not None:
         out["C"] = Ct
     return out
+
+
+def s4_fp32_probe(out, blocks: int, iters: int, stream=None) -> int:
+    """Launch the FP32 issue-rate probe (blocks x 256 threads, iters rounded up
+    to a multiple of 8, 16 flop per thread and iteration) into the float32
+    tensor `out` (at least blocks x 256 elements).  Returns the flop launched."""
+    torch = _torch()
+    if out.dtype != torch.float32 or not out.is_cuda or out.numel() < blocks * 256:
+        raise ValueError("out: a CUDA float32 tensor of blocks x 256 elements")
+    _check(load().s4_fp32_probe(ctypes.c_void_p(out.data_ptr()), int(blocks), int(iters), _stream(stream)),
+           "s4_fp32_probe")
+    return blocks * 256 * ((int(iters) + 7) // 8 * 8) * 16
 
 
 def s4_get_status(ws, stream=None) -> int:

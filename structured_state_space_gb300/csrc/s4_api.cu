@@ -173,9 +173,36 @@ TimedLaunch::~TimedLaunch() {
   record(g_recs[slot_].stop, s_);
 }
 
+// FP32 issue-rate probe (a measurement aid): 8 independent FMA chains per
+// thread, the iteration loop unrolled by 8 so that loop control is ~5 % of
+// the issued instructions.
+__global__ void __launch_bounds__(256) fp32_probe_kernel(float* __restrict__ out, int iters8) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = (float)(t & 255) * 1e-6f + (float)k * 1e-3f;
+  const float m = 0.99999988f, c = 1e-7f;  // a -> c / (1 - m): bounded, never denormal
+  for (int i = 0; i < iters8; ++i) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = fmaf(a[k], m, c);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sum += a[k];
+  out[t] = sum;
+}
+
 }  // namespace s4impl
 
 extern "C" {
+
+s4_status s4_fp32_probe(float* out, int blocks, int iters, void* stream) {
+  if (!out || blocks < 1 || iters < 1) return S4_ERR_INVALID_ARG;
+  s4impl::fp32_probe_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(out, (iters + 7) / 8);
+  return cudaGetLastError() == cudaSuccess ? S4_OK : S4_ERR_CUDA;
+}
 
 size_t s4_workspace_bytes(int H, int N, int r, int L, int batch) {
   if (!sizes_ok(H, N, r, L, batch)) return 0;

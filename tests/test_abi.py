@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     txt = open(HEADER).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(s4_[a-z_]+)\s*\(", txt)))
+    return sorted(set(re.findall(r"\b(s4_[a-z0-9_]+)\s*\(", txt)))
 
 
 def test_header_declares_the_binding_names():
@@ -106,3 +106,10 @@ def test_host_argument_errors_conv_real(lib):
     assert lib.s4_conv_fwd_real(None, _vp(A), _vp(A), 1, 2, 8, _vp(A), _vp(A), 1 << 20, None) == 1
     assert lib.s4_conv_fwd_real(_vp(A), _vp(A), _vp(A), 1, 2, 8, _vp(A + 4), _vp(A), 1 << 20, None) == 1
     assert lib.s4_conv_fwd_real(_vp(A), _vp(A), _vp(A), 1, 2, 8, _vp(A), _vp(A), 100, None) == 2
+
+
+def test_host_argument_errors_fp32_probe(lib):
+    A = 0x10000
+    assert lib.s4_fp32_probe(None, 8, 64, None) == 1
+    assert lib.s4_fp32_probe(_vp(A), 0, 64, None) == 1
+    assert lib.s4_fp32_probe(_vp(A), 8, 0, None) == 1

@@ -319,3 +319,14 @@ def test_conv_real_matches_oracle(H, L, batch):
         ts = [0, 1, L // 2, L - 1]
         ref = np.array([[O.causal_conv_at(Kr[h], u[b, h], D[h], ts).real for h in range(H)] for b in range(batch)])
         check_y(y[:, :, ts], ref, f"real L{L}")
+
+
+@pytest.mark.gpu
+def test_fp32_probe_runs_and_counts_flop():
+    # every lane's chain a <- a m + c converges to c / (1 - m); the flop count
+    # is blocks x 256 x iters (rounded to 8) x 16
+    out = torch.full((2 * 256,), float("nan"), dtype=torch.float32, device="cuda")
+    flop = s4.s4_fp32_probe(out, 2, 13)
+    torch.cuda.synchronize()
+    assert flop == 2 * 256 * 16 * 16
+    assert bool(torch.isfinite(out).all())
