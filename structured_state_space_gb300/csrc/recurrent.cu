@@ -15,10 +15,12 @@
 // its per-state constants, so a step touches each state with three complex
 // multiply-adds and one complex product).  Likewise Abar^* = 2 G^{-*} - I, and
 // G^* = diag(conj d_j) + alpha Q P^* has the correction W^* (W = I_r + alpha
-// Q^* D^{-1} P), so C~ = C - (Abar^*)^M C takes M solves with W^{-*}.
+// Q^* D^{-1} P), so C~ = C - (Abar^*)^M C takes M solves with W^{-*}; the C~
+// kernel groups them p at a time (Abar^{*p} as diagonal plus rank p r, see
+// ctilde_kernel).
 //
 // A group of G lanes owns one sequence (one channel of one batch row, or one
-// channel for C~): G = 16 for N <= 128 in the recurrent mode (two sequences per
+// channel for C~): G = 16 for N <= 64 in the recurrent mode (two sequences per
 // warp, so each reduction takes four shuffle rounds for both), otherwise 32;
 // lane l of a group holds states j = l, l + G, ...  W^{-1} is formed once per
 // group.  An exactly zero d_j (the bordered branch of the pages' solver) or an
