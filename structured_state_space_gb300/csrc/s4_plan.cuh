@@ -52,12 +52,9 @@ __host__ __device__ constexpr int tw_offset(int logn, bool inv, int idx) {
 }
 __host__ __device__ constexpr int tw_total(int logn) { return tw_offset(logn, true, plan_npass(logn)); }
 
-// Threads that share one row, rows per CTA.
+// Threads that share one row (RowCfg packs 128 / that many rows into a CTA when below 128).
 __host__ __device__ constexpr int row_threads(int logn) {
   return logn <= 4 ? 1 : (logn <= 12 ? (1 << (logn - 4)) : (1 << (logn - 5)));
-}
-__host__ __device__ constexpr int rows_per_cta(int logn) {
-  return row_threads(logn) >= 128 ? 1 : 128 / row_threads(logn);
 }
 // The paired convolution kernels give 8192-point rows one thread per radix-16
 // butterfly (512 threads): they run one CTA per SM there, and the extra warps
