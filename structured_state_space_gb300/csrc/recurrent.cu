@@ -52,6 +52,28 @@ __device__ __forceinline__ float2 warp_sum(float2 v) {
   return v;
 }
 
+// Sums over a 16-lane group of two complex values at once by recursive
+// halving: a (returned to every lane) and b (returned to lane 8 of the group,
+// the others get a partial value).  Offset 8 exchanges two floats, offset 4
+// one, offsets 2 and 1 one each; then three shuffles broadcast a and finish b:
+// 9 shuffles, 5 adds and 6 selects instead of 16 shuffles and 16 adds.
+__device__ __forceinline__ void group16_sum2(float2& a, float2& b) {
+  const unsigned lane = threadIdx.x & 15u;
+  const bool hi8 = lane & 8u, hi4 = lane & 4u;
+  float k0 = hi8 ? b.x : a.x, k1 = hi8 ? b.y : a.y;
+  const float s0 = hi8 ? a.x : b.x, s1 = hi8 ? a.y : b.y;
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+  float k = hi4 ? k1 : k0;  // lane holds (hi8 ? b : a).(hi4 ? y : x)
+  k += __shfl_xor_sync(0xffffffffu, hi4 ? k0 : k1, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  a.x = __shfl_sync(0xffffffffu, k, 0, 16);
+  a.y = __shfl_sync(0xffffffffu, k, 4, 16);
+  const float by = __shfl_sync(0xffffffffu, k, 12, 16);
+  b = make_float2(k, by);  // complete in lane 8
+}
+
 // Invert an r x r complex matrix in place (Gauss-Jordan, partial pivoting).
 // Returns false on an exactly zero pivot.
 template <int R>
@@ -214,13 +236,18 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
 #pragma unroll
     for (int e = 0; e < E; ++e) s[l] = cadd(s[l], cmul(hq[e][l], xs[e]));
   }
+  // rank 1 in 16-lane groups: a step ends with one joint reduction of the next
+  // step's s and this step's output, so s enters each step already summed
+  constexpr bool JOINT = RANK == 1 && G == 16;
+  if constexpr (JOINT) s[0] = warp_sum<G>(s[0]);
+  const int ylane = JOINT ? 8 : 0;  // the lane that holds the summed output
 #pragma unroll kRecurrentUnroll
   for (int t = 0; t < L; ++t) {
     const float ut = ur[t];
     float2 z[RANK];
 #pragma unroll
     for (int l = 0; l < RANK; ++l) {
-      s[l] = warp_sum<G>(s[l]);
+      if constexpr (!JOINT) s[l] = warp_sum<G>(s[l]);
       s[l] = make_float2(fmaf(c0[l].x, ut, s[l].x), fmaf(c0[l].y, ut, s[l].y));
     }
 #pragma unroll
@@ -243,8 +270,12 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
 #pragma unroll
       for (int l = 0; l < RANK; ++l) s[l] = cadd(s[l], cmul(hq[e][l], v));
     }
-    yp = warp_sum<G>(yp);
-    if (valid && lane == 0) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
+    if constexpr (JOINT) {
+      group16_sum2(s[0], yp);
+    } else {
+      yp = warp_sum<G>(yp);
+    }
+    if (valid && lane == ylane) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
