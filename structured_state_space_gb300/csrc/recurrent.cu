@@ -74,6 +74,36 @@ __device__ __forceinline__ void group16_sum2(float2& a, float2& b) {
   b = make_float2(k, by);  // complete in lane 8
 }
 
+// Sums of NF floats over the G lanes of a group, returned to every lane, by
+// recursive halving (NF a power of two <= G): at offset G/2 each lane keeps one
+// half of its values and sends the other, at G/4 a half of that, ... until one
+// value is left, which the remaining offsets finish; component j then sits in
+// lane j G/NF, from which it is broadcast.  NF - 1 + log2(G/NF) exchange
+// shuffles and NF broadcasts instead of NF log2(G).
+template <int NF, int G>
+__device__ __forceinline__ void group_sum_all(float (&v)[NF]) {
+  static_assert((NF & (NF - 1)) == 0 && NF <= G, "NF: a power of two <= G");
+  const unsigned lane = threadIdx.x % G;
+  float w[NF];
+#pragma unroll
+  for (int i = 0; i < NF; ++i) w[i] = v[i];
+  int off = G / 2;
+#pragma unroll
+  for (int cnt = NF; cnt > 1; cnt >>= 1, off >>= 1) {
+    const bool hi = lane & off;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float keep = hi ? w[cnt / 2 + i] : w[i];
+      const float send = hi ? w[i] : w[cnt / 2 + i];
+      w[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+#pragma unroll
+  for (int o = G / (2 * NF); o > 0; o >>= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], o);
+#pragma unroll
+  for (int j = 0; j < NF; ++j) v[j] = __shfl_sync(0xffffffffu, w[0], j * (G / NF), G);
+}
+
 // Invert an r x r complex matrix in place (Gauss-Jordan, partial pivoting).
 // Returns false on an exactly zero pivot.
 template <int R>
@@ -387,9 +417,24 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
     for (int e = 0; e < E; ++e) sv[m] = cadd(sv[m], cmul(Vf[e][m], w[e]));
   }
   const int steps = M >> LOGP;
+  // the step's KP complex sums together by recursive halving when 2 KP is a
+  // power of two no larger than the group
+  constexpr bool HALVE = ((2 * KP) & (2 * KP - 1)) == 0 && 2 * KP <= G;
   for (int it = 0; it < steps; ++it) {
+    if constexpr (HALVE) {
+      float f[2 * KP];
 #pragma unroll
-    for (int m = 0; m < KP; ++m) sv[m] = warp_sum<G>(sv[m]);
+      for (int m = 0; m < KP; ++m) {
+        f[2 * m] = sv[m].x;
+        f[2 * m + 1] = sv[m].y;
+      }
+      group_sum_all<2 * KP, G>(f);
+#pragma unroll
+      for (int m = 0; m < KP; ++m) sv[m] = make_float2(f[2 * m], f[2 * m + 1]);
+    } else {
+#pragma unroll
+      for (int m = 0; m < KP; ++m) sv[m] = warp_sum<G>(sv[m]);
+    }
     float2 sn[KP];
 #pragma unroll
     for (int m = 0; m < KP; ++m) sn[m] = make_float2(0.f, 0.f);
