@@ -27,8 +27,14 @@
  *  - Argument errors are detected on the host before anything is enqueued
  *    and returned synchronously.  Conditions that depend on device data
  *    (resonances, non-finite values, a bad step size) are recorded in a
- *    status word inside `ws` and read with s4_get_status; when one is
- *    recorded, the affected output (K, or y) is written as all zeros.
+ *    status block at the start of `ws` and read with s4_get_status; when one
+ *    is recorded, the affected output (K, or y) is written as all zeros.
+ *    The block holds the flags, the generation they were set under and the
+ *    generation of the last call: most entry points clear it (an enqueued
+ *    memset) before their kernels; s4_layer_fwd does not, it tags its flags
+ *    with a fresh generation instead, so a layer call is kernels only and
+ *    chains to the kernel before it on the stream.  Either way s4_get_status
+ *    reports the last call only, whatever `ws` held before.
  *  - Concurrent calls that share one `ws` race; give each stream its own.
  *
  * Supported sizes: 1 <= H, 1 <= N <= 65536, 1 <= r <= 4, 1 <= L <= 65536,

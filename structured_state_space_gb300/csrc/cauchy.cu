@@ -105,16 +105,20 @@ struct CauchyLayout {
   static constexpr int JT = PS <= 48 ? 128 : 64;          // poles staged at a time
 };
 
+// (4 roots per thread: compiled for 4 CTAs per SM, the schedule measured fastest;
+// left to itself the compiler picks a tighter, slower one)
 template <int RANK, int RPT, int T>
-__global__ void __launch_bounds__(T) cauchy_kernel(
+__global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
-    float2* __restrict__ Khat, int N, int logM, int logC, unsigned* __restrict__ status) {
+    float2* __restrict__ Khat, int N, int logM, int logC, St status) {
   using Lay = CauchyLayout<RANK>;
   constexpr int NW = Lay::NW, PS = Lay::PS, JT = Lay::JT;
   __shared__ __align__(16) float par[JT * PS];
   __shared__ float2 red[T / 32 + 1];
 
+  pdl_wait();  // (a programmatic launch) the previous kernel on the stream is done
+  st_record_gen(status);
   pdl_launch_dependents();  // the next kernel may start; it waits for this grid before reading
   const int h = blockIdx.x;
   const int M = 1 << logM;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(T) cauchy_kernel(
     }
     Khat[(size_t)h * M + pos[rr]] = Hk;
   }
-  if (flags) atomicOr(status, flags);
+  if (flags) st_flag(status, flags);
 }
 
 }  // namespace s4dev
@@ -293,42 +297,65 @@ using namespace s4dev;
 #ifndef S4_CAUCHY_RPT1
 #define S4_CAUCHY_RPT1 2
 #endif
+// ... and on grids of two waves or more (4 was faster there until the status
+// generation entered the kernel: the compiler then schedules the 4-root kernel
+// more tightly (85 registers, or 109 when told 4 CTAs per SM suffice), and 2
+// roots measured 1-2 % faster on both large workloads)
+#ifndef S4_CAUCHY_RPT1_BIG
+#define S4_CAUCHY_RPT1_BIG 2
+#endif
 
 
 template <int RANK, int RPT>
 static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
                                  const float2* B, const float2* Ct, const float* dt,
-                                 float2* Khat, int H, int N, int M, int logC, unsigned* status,
-                                 cudaStream_t s) {
+                                 float2* Khat, int H, int N, int M, int logC, St status,
+                                 cudaStream_t s, bool pdl) {
   constexpr int T = S4_CAUCHY_T;
   const int tiles = (M + T * RPT - 1) / (T * RPT);
   dim3 grid(H, tiles);
   TimedLaunch tl("cauchy", s);
   int logM = 0;
   while ((1 << logM) < M) ++logM;
-  cauchy_kernel<RANK, RPT, T><<<grid, T, 0, s>>>(Lambda, P, Q, B, Ct, dt, Khat, N, logM, logC, status);
-  return cudaGetLastError();
+  // A programmatic launch lets this grid's CTAs become resident while the
+  // previous kernel drains; that pays when the grid fits in one wave.  A larger
+  // grid's first wave would only sit on the SMs beside the previous kernel's tail.
+  static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
+  if (pdl && per_sm < 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T>, T, 0) != cudaSuccess)
+    per_sm = 0;
+  pdl = pdl && (long long)grid.x * grid.y <= (long long)per_sm * num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(T);
+  cfg.stream = s;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T>, Lambda, P, Q, B, Ct, dt, Khat, N, logM, logC,
+                            status);
 }
 
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
                           const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
-                          int M, int logC, unsigned* status, cudaStream_t s) {
-  // roots per thread: enough CTAs to fill the GPU for small M, more ILP for large M
-  // 4 roots per thread (512 per CTA, 5 CTAs per SM at ~100 registers) once the
-  // grid holds at least two waves of such CTAs; 2 below that, to keep enough
-  // warps resident (measured: 2 roots faster at H M = 2.6e5, 4 faster at 2.1e6)
+                          int M, int logC, St status, cudaStream_t s, bool pdl) {
+  // roots per thread: rank 1 takes 2 on every grid (S4_CAUCHY_RPT1_BIG); rank 2
+  // takes 4 (512 per CTA) once the grid holds at least two waves of such CTAs
+  // and 2 below that, to keep enough warps resident
   const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
   switch (r) {
     case 1:
-      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
-                   : cauchy_launch<1, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
+      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<1, S4_CAUCHY_RPT1_BIG>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
     case 2:  // 4 roots per thread on large grids measured 2 % faster (8 at rank 1 was 11 % slower)
-      return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s)
-                   : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
+      return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
     case 3:
-      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
+      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
     case 4:
-      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s);
+      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
     default:
       return cudaErrorInvalidValue;
   }

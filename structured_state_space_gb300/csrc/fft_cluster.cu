@@ -97,7 +97,7 @@ __device__ __forceinline__ void cross_inverse(cg::cluster_group& cl, float2* buf
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
     const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, int realk,
-    unsigned* __restrict__ status) {
+    St status) {
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
     }
     cl.sync();
   }
-  if (!fin) atomicOr(status, ST_NONFINITE);
+  if (!fin) st_flag(status, ST_NONFINITE);
 }
 
 // Inverse transform of M = n root values per channel (blocked input order),
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, int H, int L,
-    const unsigned* __restrict__ status) {
+    St status) {
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM;
   constexpr int R0 = plan_radix(LOGM, 0, true), NB0 = m / R0, PER0 = NB0 / T;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
   float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   __syncthreads();
   cl.sync();
   const float sc = 1.f / n;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int rows, int H, int L, const unsigned* __restrict__ status) {
+    float2* __restrict__ y, int rows, int H, int L, St status) {
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
   float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   __syncthreads();
   cl.sync();
   const float sc = 1.f / n;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN, true>::T) conv_cluster_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
+    float2* __restrict__ y, int batch, int H, int L, St status) {
   using Cf = ClusterCfg<LOGN, true>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN, true>::T) conv_cluster_pair_k
   float2* const buf2[2] = {bufA, bufB};
   const int lt = threadIdx.x;
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   __syncthreads();
   cl.sync();
   const float sc = 0.5f / n;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN, true>::T) conv_cluster_pair_k
 template <int LOGN>
 __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_real_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float* __restrict__ y, int batch, int H, int L, const unsigned* __restrict__ status) {
+    float* __restrict__ y, int batch, int H, int L, St status) {
   using Cf = ClusterCfg<LOGN>;
   constexpr int n = Cf::n, m = Cf::m, T = Cf::T, NP = Cf::NP, LOGM = Cf::LOGM, C = Cf::C;
   constexpr int RB = plan_radix(LOGM, NP - 1, false), NBL = m / RB, PERL = NBL / T;
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_real_kernel(
   float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   __syncthreads();
   cl.sync();
   const float sc = 1.f / n;
@@ -496,7 +496,7 @@ static cudaError_t launch_clustered(void (*kern)(KArgs...), int C, int threads, 
 }
 
 template <int LOGN>
-static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, const unsigned* st,
+static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, St st,
                            cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
@@ -504,7 +504,7 @@ static cudaError_t ifft_cl(const float2* Khat, float2* K, int H, int L, const un
 }
 
 template <int LOGN>
-static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsigned* st, cudaStream_t s,
+static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, St st, cudaStream_t s,
                                bool realk) {
   using Cf = ClusterCfg<LOGN>;
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
@@ -514,7 +514,7 @@ static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, unsign
 
 template <int LOGN>
 static cudaError_t conv_pair_cl(const float* u, const float2* K2, const float* D, float2* y, int batch,
-                                int H, int L, const unsigned* st, cudaStream_t s) {
+                                int H, int L, St st, cudaStream_t s) {
   using Cf = ClusterCfg<LOGN, true>;
   const size_t smem = sizeof(float2) * (Cf::MI + 2 * (size_t)Cf::PADM);
   const int pairs = ((batch + 1) / 2) * H;
@@ -524,7 +524,7 @@ static cudaError_t conv_pair_cl(const float* u, const float2* K2, const float* D
 
 template <int LOGN>
 static cudaError_t conv_real_cl(const float* u, const float2* K2, const float* D, float* y, int batch,
-                                int H, int L, const unsigned* st, cudaStream_t s) {
+                                int H, int L, St st, cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   const int pairs = ((batch + 1) / 2) * H;
@@ -533,7 +533,7 @@ static cudaError_t conv_real_cl(const float* u, const float2* K2, const float* D
 }
 
 cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2, const float* D,
-                                     float* y, int batch, int H, int L, const unsigned* st,
+                                     float* y, int batch, int H, int L, St st,
                                      cudaStream_t s) {
   switch (logn) {
     case 14: return conv_real_cl<14>(u, K2, D, y, batch, H, L, st, s);
@@ -546,7 +546,7 @@ cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2,
 
 template <int LOGN>
 static cudaError_t conv_cl(const float* u, const float2* K2, const float* D, float2* y, int rows, int H,
-                           int L, const unsigned* st, cudaStream_t s) {
+                           int L, St st, cudaStream_t s) {
   using Cf = ClusterCfg<LOGN>;
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(conv_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, rows, "conv", s, u, K2, D, y,
@@ -554,7 +554,7 @@ static cudaError_t conv_cl(const float* u, const float2* K2, const float* D, flo
 }
 
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
-                                const unsigned* st, cudaStream_t s) {
+                                St st, cudaStream_t s) {
   switch (logM) {
     case 15: return ifft_cl<15>(Khat, K, H, L, st, s);
     case 16: return ifft_cl<16>(Khat, K, H, L, st, s);
@@ -563,7 +563,7 @@ cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, 
 }
 
 cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
-                                    unsigned* st, cudaStream_t s, bool realk) {
+                                    St st, cudaStream_t s, bool realk) {
   switch (logn) {
     case 14: return spectrum_cl<14>(K, K2, H, L, st, s, realk);
     case 15: return spectrum_cl<15>(K, K2, H, L, st, s, realk);
@@ -574,7 +574,7 @@ cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H
 }
 
 cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, const float* D,
-                                float2* y, int rows, int H, int L, const unsigned* st,
+                                float2* y, int rows, int H, int L, St st,
                                 cudaStream_t s) {
   // two batch rows per complex row where two row buffers fit a CTA (2^14..2^16);
   // one row at a time at 2^17

@@ -26,11 +26,11 @@ namespace s4dev {
 template <int LOGN>
 __global__ void __launch_bounds__(128) ifft_small_kernel(const float2* __restrict__ Khat,
                                                          float2* __restrict__ K, int H, int L,
-                                                         const unsigned* __restrict__ status) {
+                                                         St status) {
   constexpr int n = 1 << LOGN;
   const int h = blockIdx.x * 128 + threadIdx.x;
   if (h >= H) return;
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   float2 a[n];
 #pragma unroll
   for (int q = 0; q < n; ++q) a[q] = Khat[(size_t)h * n + q];
@@ -45,7 +45,7 @@ template <int LOGN>
 __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __restrict__ K,
                                                              float2* __restrict__ K2, int H, int L,
                                                              float scale, int realk,
-                                                             unsigned* __restrict__ status) {
+                                                             St status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
   const int h = blockIdx.x * 128 + threadIdx.x;
   if (h >= H) return;
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __res
     fin = fin && cfinite(a[q]);
     K2[(size_t)h * n + q] = cscale(a[q], scale);
   }
-  if (!fin) atomicOr(status, ST_NONFINITE);
+  if (!fin) st_flag(status, ST_NONFINITE);
 }
 
 // rows of length n <= 16 with K2 scaled by 1/(2n): two rows per thread
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(128) conv_small_kernel(const float* __restrict
                                                          const float2* __restrict__ K2,
                                                          const float* __restrict__ D,
                                                          float2* __restrict__ y, int batch, int H,
-                                                         int L, const unsigned* __restrict__ status) {
+                                                         int L, St status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
   const int pairs = ((batch + 1) / 2) * H;
   const int p = blockIdx.x * 128 + threadIdx.x;
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(128) conv_small_kernel(const float* __restrict
   const int h = p % H, b0 = 2 * (p / H);
   const bool has1 = b0 + 1 < batch;
   const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   float u0[n / 2], u1[n / 2];
   float2 z[n];
 #pragma unroll
@@ -128,7 +128,7 @@ struct RowCfg {
 template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, int H, int L,
-    const unsigned* __restrict__ status) {
+    St status) {
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP;
   constexpr int R0 = plan_radix(LOGN, 0, true), RL = plan_radix(LOGN, NP - 1, true);
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
   pdl_wait();  // (a programmatic launch) root values and status come from the previous kernel
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   const float sc = 1.f / n;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
 template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
     const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale, int realk,
-    unsigned* __restrict__ status) {
+    St status) {
   using C = RowCfg<LOGN>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
     }
     __syncthreads();
   }
-  if (!fin) atomicOr(status, ST_NONFINITE);
+  if (!fin) st_flag(status, ST_NONFINITE);
 }
 
 // Threads per SM the kspec kernel is compiled for (registers capped at
@@ -253,7 +253,7 @@ __host__ __device__ constexpr int kspec_min_blocks(int threads) {
 template <int LOGM>
 __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(RowCfg<LOGM + 1>::THREADS)) kspec_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
-    float scale, unsigned* __restrict__ status) {
+    float scale, St status) {
   using C = RowCfg<LOGM + 1>;
   constexpr int M = 1 << LOGM, n = C::n, T = C::T;
   constexpr bool STW = kspec_stage_tw(LOGM);
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(Ro
   }
   pdl_launch_dependents();
   pdl_wait();  // root values and status come from the previous kernel
-  bool zero = *((volatile const unsigned*)status) != 0u;
+  bool zero = st_bad(status);
   bool fin = true;
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
@@ -290,11 +290,11 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(Ro
                          K2 + (size_t)(act ? h : 0) * n, L, scale, zero || stall, act, buf, lt, fin, twi,
                          twf, &twbar, &stall);
   }
-  if (!fin) atomicOr(status, ST_NONFINITE);
+  if (!fin) st_flag(status, ST_NONFINITE);
   if constexpr (STW) {
     if (stall) mbar_wait(&twbar, 0u);  // one more bounded wait for the copy in flight
   }
-  if (stall && threadIdx.x == 0) atomicOr(status, ST_STALL);
+  if (stall && threadIdx.x == 0) st_flag(status, ST_STALL);
 }
 
 // Resident CTAs per SM the convolution is compiled for: 512 threads per SM
@@ -349,7 +349,7 @@ template <int LOGN, bool STAGE>
 __global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int batch, int H, int L, unsigned* __restrict__ status, int stage_u) {
+    float2* __restrict__ y, int batch, int H, int L, St status, int stage_u) {
   using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
@@ -434,7 +434,7 @@ conv_pair_kernel(
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(buf1, lt);
     if (!waited) {  // the forward transform of u needed nothing from the previous kernel
       pdl_wait();
-      zero = *((volatile const unsigned*)status) != 0u;
+      zero = st_bad(status);
       waited = true;
       if (STAGE && threadIdx.x == 0) issue_k2(K2h);  // K2 comes from the previous kernel
     }
@@ -578,7 +578,7 @@ conv_pair_kernel(
     }
     __syncthreads();
   }
-  if (stall && threadIdx.x == 0) atomicOr(status, ST_STALL);
+  if (stall && threadIdx.x == 0) st_flag(status, ST_STALL);
 }
 
 // Real-output convolution y = Re(K) * u + D u.  K2 = FFT_n(Re K zero-padded)/n
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(128) conv_real_small_kernel(const float* __res
                                                               const float2* __restrict__ K2,
                                                               const float* __restrict__ D,
                                                               float* __restrict__ y, int batch, int H,
-                                                              int L, const unsigned* __restrict__ status) {
+                                                              int L, St status) {
   constexpr int n = 1 << LOGN;
   const int pairs = ((batch + 1) / 2) * H;
   const int p = blockIdx.x * 128 + threadIdx.x;
@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(128) conv_real_small_kernel(const float* __res
   const int h = p % H, b0 = 2 * (p / H);
   const bool has1 = b0 + 1 < batch;
   const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
-  const bool zero = *((volatile const unsigned*)status) != 0u;
+  const bool zero = st_bad(status);
   float u0[n / 2], u1[n / 2];
   float2 z[n];
 #pragma unroll
@@ -626,7 +626,7 @@ template <int LOGN>
 __global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_real_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2,
                       const float* __restrict__ D, float* __restrict__ y, int batch, int H, int L,
-                      const unsigned* __restrict__ status) {
+                      St status) {
   using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
@@ -667,7 +667,7 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(bufs, lt);
     if (!waited) {  // (a programmatic launch) K2 and the status come from the previous kernel
       pdl_wait();
-      zero = *((volatile const unsigned*)status) != 0u;
+      zero = st_bad(status);
       waited = true;
     }
     float2 a[PERL][RB];
@@ -763,7 +763,7 @@ static cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), int grid, int thread
 }
 
 template <int LOGN>
-static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, const unsigned* st,
+static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, St st,
                                cudaStream_t s) {
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("ifft", s);
@@ -782,7 +782,7 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, cons
 }
 
 template <int LOGN>
-static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, unsigned* st,
+static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, St st,
                                    cudaStream_t s, bool realk) {
   // 1/(2n): pair split and inverse scaling; 1/n for the real-kernel variant (no split)
   const float scale = realk ? 1.f / (float)(1 << LOGN) : 1.f / (float)(2 << LOGN);
@@ -805,7 +805,7 @@ static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, un
 
 template <int LOGN>
 static cudaError_t conv_launch(const float* u, const float2* K2, const float* D, float2* y, int batch,
-                               int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
+                               int H, int L, St st, cudaStream_t s, bool pdl) {
   const int pairs = ((batch + 1) / 2) * H;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("conv", s);
@@ -824,13 +824,13 @@ static cudaError_t conv_launch(const float* u, const float2* K2, const float* D,
     const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv", s);
     return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L,
-                            const_cast<unsigned*>(st), (L % 4 == 0) ? 1 : 0);
+                            st, (L % 4 == 0) ? 1 : 0);
   }
   return cudaGetLastError();
 }
 
 template <int LOGM>
-static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H, int L, unsigned* st,
+static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H, int L, St st,
                                 cudaStream_t s) {
   using C = RowCfg<LOGM + 1>;
   const float scale = 1.f / (float)(4 << LOGM);  // 1/(2n), n = 2M
@@ -848,7 +848,7 @@ static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H
 bool kspec_supported(int logM) { return logM >= 5 && logM <= 12; }
 
 cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
-                              unsigned* st, cudaStream_t s) {
+                              St st, cudaStream_t s) {
   switch (logM) {
     case 5: return kspec_launch<5>(Khat, K, K2, H, L, st, s);
     case 6: return kspec_launch<6>(Khat, K, K2, H, L, st, s);
@@ -864,7 +864,7 @@ cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K
 
 template <int LOGN>
 static cudaError_t conv_real_launch(const float* u, const float2* K2, const float* D, float* y,
-                                    int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
+                                    int batch, int H, int L, St st, cudaStream_t s, bool pdl) {
   const int pairs = ((batch + 1) / 2) * H;
   if constexpr (LOGN <= 4) {
     TimedLaunch tl("conv_real", s);
@@ -883,7 +883,7 @@ static cudaError_t conv_real_launch(const float* u, const float2* K2, const floa
 }
 
 cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
-                                  int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
+                                  int batch, int H, int L, St st, cudaStream_t s, bool pdl) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
@@ -897,7 +897,7 @@ cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, co
 }
 
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
-                             const unsigned* st, cudaStream_t s) {
+                             St st, cudaStream_t s) {
   switch (logM) {
 #define S4_CASE(X) \
   case X:          \
@@ -910,7 +910,7 @@ cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int
   }
 }
 
-cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
+cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, St st,
                                  cudaStream_t s, bool realk) {
   switch (logn) {
 #define S4_CASE(X) \
@@ -925,7 +925,7 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
 }
 
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl) {
+                             int batch, int H, int L, St st, cudaStream_t s, bool pdl) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Cv, const float* __restrict__ dt,
     const float* __restrict__ Dskip, const float* __restrict__ u, int batch, int H, int N, int L,
-    float2* __restrict__ x, float2* __restrict__ y, unsigned* __restrict__ status) {
+    float2* __restrict__ x, float2* __restrict__ y, St status) {
   const int gt = blockIdx.x * blockDim.x + threadIdx.x;
   if ((gt & ~31) / G >= batch * H) return;  // the whole warp is past the last sequence
   // a group past the last sequence (odd count, G = 16) runs on sequence 0 and
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     const int j = lane + G * e;
     if (valid && j < N) x[(size_t)warp * N + j] = ok ? xs[e] : make_float2(0.f, 0.f);
   }
-  if (valid && lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+  if (valid && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
 
 // C~ = C - (Abar^*)^M C with Abar^* w = 2 G^{-*} w - w.
@@ -331,7 +331,7 @@ template <int RANK, int E, int G, int LOGP>
 __global__ void __launch_bounds__(128) ctilde_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float* __restrict__ dt, const float2* __restrict__ Cv, int H, int N, int M,
-    float2* __restrict__ Ct, unsigned* __restrict__ status) {
+    float2* __restrict__ Ct, St status) {
   constexpr int P = 1 << LOGP, KP = RANK * P;
   constexpr int KH = KP / 2 > 0 ? KP / 2 : 1;  // columns before the last squaring
   const int gt = blockIdx.x * blockDim.x + threadIdx.x;
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
     const int j = lane + G * e;
     if (valid && j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
   }
-  if (valid && lane == 0 && !ok) atomicOr(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+  if (valid && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
 
 }  // namespace s4dev
@@ -466,7 +466,7 @@ using namespace s4dev;
 template <int RANK, int E, int G>
 static cudaError_t rec_launch(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                               const float2* C, const float* dt, const float* D, const float* u,
-                              int batch, int H, int N, int L, float2* x, float2* y, unsigned* st,
+                              int batch, int H, int N, int L, float2* x, float2* y, St st,
                               cudaStream_t s) {
   const long long threads = (long long)batch * H * G;
   TimedLaunch tl("recurrent", s);
@@ -479,7 +479,7 @@ static cudaError_t rec_launch(const float2* Lam, const float2* P, const float2* 
 template <int RANK>
 static cudaError_t rec_dispatch(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                                 const float2* C, const float* dt, const float* D, const float* u,
-                                int batch, int H, int N, int L, float2* x, float2* y, unsigned* st,
+                                int batch, int H, int N, int L, float2* x, float2* y, St st,
                                 cudaStream_t s) {
   if (N <= 16) return rec_launch<RANK, 1, 16>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
   if (N <= 32) return rec_launch<RANK, 2, 16>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
@@ -490,7 +490,7 @@ static cudaError_t rec_dispatch(const float2* Lam, const float2* P, const float2
 
 template <int RANK, int E, int G, int LOGP>
 static cudaError_t ct_launch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
-                             const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                             const float2* C, int H, int N, int M, float2* Ct, St st,
                              cudaStream_t s) {
   const long long threads = (long long)H * G;
   TimedLaunch tl("ctilde", s);
@@ -508,7 +508,7 @@ constexpr int ct_logp(int rank, int e) {
 
 template <int RANK, int E>
 static cudaError_t ct_launch_p(const float2* Lam, const float2* P, const float2* Q, const float* dt,
-                               const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                               const float2* C, int H, int N, int M, float2* Ct, St st,
                                cudaStream_t s) {
   constexpr int LP = ct_logp(RANK, E);
   if (M % (1 << LP) == 0) return ct_launch<RANK, E, 32, LP>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
@@ -520,7 +520,7 @@ static cudaError_t ct_launch_p(const float2* Lam, const float2* P, const float2*
 // most lanes (the fewest elements per lane) on each chain.
 template <int RANK>
 static cudaError_t ct_dispatch(const float2* Lam, const float2* P, const float2* Q, const float* dt,
-                               const float2* C, int H, int N, int M, float2* Ct, unsigned* st,
+                               const float2* C, int H, int N, int M, float2* Ct, St st,
                                cudaStream_t s) {
   if (N <= 32) return ct_launch_p<RANK, 1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
   if (N <= 64) return ct_launch_p<RANK, 2>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
@@ -531,7 +531,7 @@ static cudaError_t ct_dispatch(const float2* Lam, const float2* P, const float2*
 cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                              const float2* C, const float* dt, const float* D, const float* u,
                              int batch, int H, int N, int r, int L, float2* x, float2* y,
-                             unsigned* st, cudaStream_t s) {
+                             St st, cudaStream_t s) {
   switch (r) {
     case 1: return rec_dispatch<1>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
     case 2: return rec_dispatch<2>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
@@ -542,7 +542,7 @@ cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q
 }
 
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
-                          const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
+                          const float2* C, int H, int N, int r, int M, float2* Ct, St st,
                           cudaStream_t s) {
   switch (r) {
     case 1: return ct_dispatch<1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);

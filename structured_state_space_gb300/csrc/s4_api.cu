@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -58,9 +59,23 @@ s4_status check_ws(const void* ws, size_t ws_bytes, int H, int L) {
 
 s4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? S4_OK : S4_ERR_CUDA; }
 
+// The status block at the start of the workspace (see s4impl::St).
+s4impl::St status_of(void* ws, unsigned gen) { return s4impl::St{static_cast<unsigned*>(ws), gen}; }
+constexpr size_t kStatusBlockBytes = 3 * sizeof(unsigned);
+
+// Generations of layer calls: 1, 2, ... (0 marks a status block reset by a memset).
+unsigned next_generation() {
+  static std::atomic<unsigned> g_gen{0};
+  unsigned g;
+  do {
+    g = g_gen.fetch_add(1u) + 1u;
+  } while (g == 0u);
+  return g;
+}
+
 cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
                         const s4_c32* Ct, const float* dt, int H, int N, int r, int L, void* ws,
-                        cudaStream_t s) {
+                        s4impl::St st, bool pdl, cudaStream_t s) {
   using namespace s4impl;
   const int logM = ilog2_ceil(L);
   char* w = static_cast<char*>(ws);
@@ -68,19 +83,18 @@ cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
                        reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
                        reinterpret_cast<const float2*>(Ct), dt,
                        reinterpret_cast<float2*>(w + layout_for(H, L).khat), H, N, r, 1 << logM,
-                       khat_cluster_log(logM), reinterpret_cast<unsigned*>(w), s);
+                       khat_cluster_log(logM), st, s, pdl);
 }
 
 s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
                    const s4_c32* Ct, const float* dt, int H, int N, int r, int L, s4_c32* K,
-                   void* ws, cudaStream_t s) {
+                   void* ws, s4impl::St st, bool pdl, cudaStream_t s) {
   using namespace s4impl;
   const int logM = ilog2_ceil(L);
   const Layout lay = layout_for(H, L);
   char* w = static_cast<char*>(ws);
-  unsigned* st = reinterpret_cast<unsigned*>(w);
   float2* khat = reinterpret_cast<float2*>(w + lay.khat);
-  cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ct, dt, H, N, r, L, ws, s);
+  cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ct, dt, H, N, r, L, ws, st, pdl, s);
   if (e == cudaSuccess)
     e = logM <= kMaxLogRowCta
             ? launch_ifft_rows(logM, khat, reinterpret_cast<float2*>(K), H, L, st, s)
@@ -89,12 +103,11 @@ s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const
 }
 
 s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
-                    s4_c32* y, void* ws, cudaStream_t s) {
+                    s4_c32* y, void* ws, s4impl::St st, cudaStream_t s) {
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
   const Layout lay = layout_for(H, L);
   char* w = static_cast<char*>(ws);
-  unsigned* st = reinterpret_cast<unsigned*>(w);
   float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   float2* yf = reinterpret_cast<float2*>(y);
@@ -220,8 +233,8 @@ s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
-  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);
+  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
+  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, status_of(ws, 0u), false, s);
 }
 
 s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -233,8 +246,8 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
-  return conv_impl(u, K, D, batch, H, L, y, ws, s);
+  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
+  return conv_impl(u, K, D, batch, H, L, y, ws, status_of(ws, 0u), s);
 }
 
 s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -245,11 +258,11 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
   char* w = static_cast<char*>(ws);
-  unsigned* st = reinterpret_cast<unsigned*>(w);
+  const St st = status_of(ws, 0u);
   float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L).k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   cudaError_t e;
@@ -277,16 +290,18 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  // No reset of the status block: this call's flags carry a fresh generation,
+  // so the call is kernels only and its first kernel (root values) can be a
+  // programmatic dependent of whatever kernel precedes it on the stream.
+  const s4impl::St st = status_of(ws, next_generation());
   const int logM = ilog2_ceil(L);
   if (s4impl::kspec_supported(logM) && logM + 1 <= s4impl::kMaxLogConvRow) {
     // root values -> (K, kernel spectrum) in one launch -> convolution
     const Layout lay = layout_for(H, L);
     char* w = static_cast<char*>(ws);
-    unsigned* st = reinterpret_cast<unsigned*>(w);
     float2* khat = reinterpret_cast<float2*>(w + lay.khat);
     float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
-    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, s);
+    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, true, s);
     if (e == cudaSuccess)
       e = s4impl::launch_kspec_rows(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
     if (e == cudaSuccess)
@@ -294,9 +309,9 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
                                    /*pdl=*/true);
     return cuda_status(e);
   }
-  const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, s);
+  const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, true, s);
   if (g != S4_OK) return g;
-  return conv_impl(u, K, D, batch, H, L, y, ws, s);
+  return conv_impl(u, K, D, batch, H, L, y, ws, st, s);
 }
 
 s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const float* dt,
@@ -309,11 +324,11 @@ s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, cons
     return S4_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return S4_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
   return cuda_status(s4impl::launch_ctilde(
       reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
       reinterpret_cast<const float2*>(Q), dt, reinterpret_cast<const float2*>(C), H, N, r,
-      1 << ilog2_ceil(L), reinterpret_cast<float2*>(Ctilde), static_cast<unsigned*>(ws), s));
+      1 << ilog2_ceil(L), reinterpret_cast<float2*>(Ctilde), status_of(ws, 0u), s));
 }
 
 s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
@@ -328,20 +343,21 @@ s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* 
     return S4_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return S4_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
   return cuda_status(s4impl::launch_recurrent(
       reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
       reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
       reinterpret_cast<const float2*>(C), dt, D, u, batch, H, N, r, L, reinterpret_cast<float2*>(x),
-      reinterpret_cast<float2*>(y), static_cast<unsigned*>(ws), s));
+      reinterpret_cast<float2*>(y), status_of(ws, 0u), s));
 }
 
 s4_status s4_get_status(const void* ws, void* stream) {
   if (ws == nullptr) return S4_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return S4_ERR_CUDA;
-  unsigned word = 0;
-  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return S4_ERR_CUDA;
+  unsigned blk[3] = {0u, 0u, 0u};  // flags, their generation, the last call's generation
+  if (cudaMemcpy(blk, ws, sizeof(blk), cudaMemcpyDeviceToHost) != cudaSuccess) return S4_ERR_CUDA;
+  const unsigned word = blk[1] == blk[2] ? blk[0] : 0u;  // older flags are stale
   if (word & s4dev::ST_STALL) return S4_ERR_TIMEOUT;
   if (word & s4dev::ST_BAD_STEP) return S4_ERR_INVALID_STEP;
   if (word & s4dev::ST_RES_DIAG) return S4_ERR_RESONANT_DIAGONAL;

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "s4_internal.h"
+
 namespace s4dev {
 
 // ---- device status bits (kept in the first word of the workspace) ----------
@@ -53,6 +55,35 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---- device status of a call (see St) --------------------------------------------
+using s4impl::St;
+
+// Set `flags` for this call: the 64-bit word (flags, generation) takes this
+// call's generation, keeping the flags already set in it only if they carry
+// the same generation.  A CAS loop; every failed round means another thread's
+// update went in, and the loop is bounded all the same.
+__device__ __forceinline__ void st_flag(St st, unsigned flags) {
+  unsigned long long* w = reinterpret_cast<unsigned long long*>(st.w);
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(w);
+  for (int it = 0; it < (1 << 16); ++it) {
+    const unsigned base = (unsigned)(old >> 32) == st.gen ? (unsigned)old : 0u;
+    const unsigned long long nw = ((unsigned long long)st.gen << 32) | base | flags;
+    if (nw == old) return;
+    const unsigned long long prev = atomicCAS(w, old, nw);
+    if (prev == old) return;
+    old = prev;
+  }
+}
+// Whether a kernel of this call has set a flag so far.
+__device__ __forceinline__ bool st_bad(St st) {
+  const unsigned long long v = *reinterpret_cast<volatile const unsigned long long*>(st.w);
+  return (unsigned)(v >> 32) == st.gen && (unsigned)v != 0u;
+}
+// The first kernel of a call records its generation for s4_get_status.
+__device__ __forceinline__ void st_record_gen(St st) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) st.w[2] = st.gen;
+}
 
 // Hint: bring the line holding p into L2 (no effect on results).
 __device__ __forceinline__ void prefetch_l2(const void* p) {

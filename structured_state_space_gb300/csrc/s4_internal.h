@@ -5,6 +5,16 @@
 
 namespace s4impl {
 
+// The device status of one call: `w` points to the workspace's status block of
+// three 32-bit words [flags, generation of the flags, generation of the last
+// call]; `gen` is this call's generation.  Flags carrying another generation are
+// stale and read as clear, so a call need not reset the block before its
+// kernels run (gen 0: the block was zeroed by a memset before the call).
+struct St {
+  unsigned* w;
+  unsigned gen;
+};
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
@@ -42,37 +52,40 @@ __host__ __device__ constexpr int khat_cluster_log(int logM) {
 }
 
 // Root values Khat[h][p] for every channel, in the blocked root order
-// (position p -> root (p mod M/C) C + p div M/C, C = 2^logC).
+// (position p -> root (p mod M/C) C + p div M/C, C = 2^logC).  The kernel
+// records the call's generation (it is a call's first kernel); `pdl`: launch
+// it as a programmatic dependent of the previous kernel on the stream, which
+// it waits for before any memory access.
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
                           const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
-                          int M, int logC, unsigned* status, cudaStream_t s);
+                          int M, int logC, St status, cudaStream_t s, bool pdl = false);
 
 // Single-CTA row transforms (log sizes up to kMaxLogRowCta).
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
-                             const unsigned* st, cudaStream_t s);
+                             St st, cudaStream_t s);
 // realk: the spectrum of Re K (real-output convolution), scaled by 1/n
 // instead of 1/(2n).
-cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, unsigned* st,
+cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, St st,
                                  cudaStream_t s, bool realk = false);
 // Layer path: inverse transform of the root values and the kernel spectrum in
 // one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported),
 // launched as a programmatic dependent of the root-value kernel.
 bool kspec_supported(int logM);
 cudaError_t launch_kspec_rows(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
-                              unsigned* st, cudaStream_t s);
+                              St st, cudaStream_t s);
 // (the row kernels pair batch rows; K2 from launch_spectrum_rows is scaled by 1/(2n))
 // `pdl`: launch as a programmatic dependent of the previous kernel (layer path).
 cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const float* D, float2* y,
-                             int batch, int H, int L, const unsigned* st, cudaStream_t s,
+                             int batch, int H, int L, St st, cudaStream_t s,
                              bool pdl = false);
 
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
-                                const unsigned* st, cudaStream_t s);
+                                St st, cudaStream_t s);
 cudaError_t launch_spectrum_cluster(int logn, const float2* K, float2* K2, int H, int L,
-                                    unsigned* st, cudaStream_t s, bool realk = false);
+                                    St st, cudaStream_t s, bool realk = false);
 cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, const float* D,
-                                float2* y, int rows, int H, int L, const unsigned* st,
+                                float2* y, int rows, int H, int L, St st,
                                 cudaStream_t s);
 
 // Recurrent mode over L steps from the state x (in/out), one warp per
@@ -80,18 +93,18 @@ cudaError_t launch_conv_cluster(int logn, const float* u, const float2* K2, cons
 cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                              const float2* C, const float* dt, const float* D, const float* u,
                              int batch, int H, int N, int r, int L, float2* x, float2* y,
-                             unsigned* st, cudaStream_t s);
+                             St st, cudaStream_t s);
 // C~ = (I - Abar^M)^* C, one warp per channel; N <= 256.
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
-                          const float2* C, int H, int N, int r, int M, float2* Ct, unsigned* st,
+                          const float2* C, int H, int N, int r, int M, float2* Ct, St st,
                           cudaStream_t s);
 
 // Real-output convolution y = Re(K) * u + D u (real y), two batch rows per
 // complex transform; K2 from the spectrum launchers with realk = true.
 cudaError_t launch_conv_real_rows(int logn, const float* u, const float2* K2, const float* D, float* y,
-                                  int batch, int H, int L, const unsigned* st, cudaStream_t s, bool pdl = false);
+                                  int batch, int H, int L, St st, cudaStream_t s, bool pdl = false);
 cudaError_t launch_conv_real_cluster(int logn, const float* u, const float2* K2, const float* D,
-                                     float* y, int batch, int H, int L, const unsigned* st,
+                                     float* y, int batch, int H, int L, St st,
                                      cudaStream_t s);
 
 }  // namespace s4impl

@@ -71,10 +71,10 @@ extern "C" s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const 
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return S4_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned* st = static_cast<unsigned*>(base);
+  const s4impl::St st{static_cast<unsigned*>(base), 0u};
   float2* k2 = reinterpret_cast<float2*>(static_cast<char*>(base) + 256);
-  // the status word must start at zero; the spectrum is fully overwritten
-  if (cudaMemsetAsync(st, 0, sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
+  // the status block starts at zero (generation 0); the spectrum is fully overwritten
+  if (cudaMemsetAsync(base, 0, 3 * sizeof(unsigned), s) != cudaSuccess) return S4_ERR_CUDA;
   const float2* Kf = reinterpret_cast<const float2*>(K);
   float2* yf = reinterpret_cast<float2*>(y);
   const int rows = batch * H;

@@ -212,6 +212,39 @@ def test_layer_status_protocol():
     assert s4.s4_get_status(ws) == 0
 
 
+def test_layer_status_on_an_uninitialised_workspace():
+    # layer calls do not reset the status block: flags carry the call's
+    # generation, so whatever the workspace held before reads as clear
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    ut = torch.from_numpy(W.make_u(w, p)).cuda()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    ws.fill_(0xFF)
+    K, y = _layer(d, ut, ws)
+    assert s4.s4_get_status(ws) == 0
+    K_ref, y_ref = _layer(d, ut, s4.workspace(w.H, w.N, w.r, w.L, w.batch))
+    assert torch.equal(K, K_ref) and torch.equal(y, y_ref)
+
+
+def test_layer_flags_do_not_leak_into_other_entry_points():
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    ut = torch.from_numpy(W.make_u(w, p)).cuda()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    bad = d["dt"].clone()
+    bad[3] = float("nan")
+    K, _ = _layer(d, ut, ws)
+    for clean in (lambda: s4.s4_conv_fwd(ut, K, d["D"], ws=ws),
+                  lambda: s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=ws),
+                  lambda: s4.s4_ctilde(d["Lambda"], d["P"], d["Q"], d["dt"], d["Ctilde"], w.L, ws=ws)):
+        _layer(d, ut, ws, dt=bad)
+        assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_INVALID_STEP"]
+        clean()
+        assert s4.s4_get_status(ws) == 0
+
+
 @pytest.mark.parametrize("L", [8, 32])
 def test_layer_resonance_zeroes_outputs(L):
     # L = 32 takes the three-kernel layer path, L = 8 the generic one
