@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
   float2* buf = tw1 + Cf::MI;
   float2* const bufs[1] = {buf};
   const int lt = threadIdx.x;
+  st_record_gen(status);  // the first kernel of a convolution call (launched normally)
   fill_cross_twiddles(tw1, c, Cf::MI, n, lt, T);
   __syncthreads();
   cl.sync();

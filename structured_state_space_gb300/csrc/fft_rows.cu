@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(128) spectrum_small_kernel(const float2* __res
                                                              float scale, int realk,
                                                              St status) {
   constexpr int n = 1 << LOGN;  // n = 2M >= 2
+  pdl_wait();  // (a programmatic launch) the previous kernel on the stream is done
+  st_record_gen(status);  // the first kernel of a convolution call
   const int h = blockIdx.x * 128 + threadIdx.x;
   if (h >= H) return;
   float2 a[n];
@@ -194,6 +196,8 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
   float2* buf = smem + slot * C::PADN;
   float2* const bufs[1] = {buf};
   bool fin = true;
+  pdl_wait();  // (a programmatic launch) the previous kernel on the stream is done
+  st_record_gen(status);  // the first kernel of a convolution call
   pdl_launch_dependents();  // the convolution may be scheduled; it waits for this grid before reading K2
   for (int h0 = blockIdx.x * C::ROWS; h0 < H; h0 += gridDim.x * C::ROWS) {
     const int h = h0 + slot;
@@ -783,7 +787,7 @@ static cudaError_t ifft_launch(const float2* Khat, float2* K, int H, int L, St s
 
 template <int LOGN>
 static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, St st,
-                                   cudaStream_t s, bool realk) {
+                                   cudaStream_t s, bool realk, bool pdl) {
   // 1/(2n): pair split and inverse scaling; 1/n for the real-kernel variant (no split)
   const float scale = realk ? 1.f / (float)(1 << LOGN) : 1.f / (float)(2 << LOGN);
   const int rk = realk ? 1 : 0;
@@ -798,7 +802,7 @@ static cudaError_t spectrum_launch(const float2* K, float2* K2, int H, int L, St
     if (e != cudaSuccess) return e;
     const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("spectrum", s);
-    k<<<grid, C::THREADS, smem, s>>>(K, K2, H, L, scale, rk, st);
+    return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, K, K2, H, L, scale, rk, st);
   }
   return cudaGetLastError();
 }
@@ -911,11 +915,11 @@ cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int
 }
 
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, St st,
-                                 cudaStream_t s, bool realk) {
+                                 cudaStream_t s, bool realk, bool pdl) {
   switch (logn) {
 #define S4_CASE(X) \
   case X:          \
-    return spectrum_launch<X>(K, K2, H, L, st, s, realk);
+    return spectrum_launch<X>(K, K2, H, L, st, s, realk, pdl);
     S4_CASE(1) S4_CASE(2) S4_CASE(3) S4_CASE(4) S4_CASE(5) S4_CASE(6) S4_CASE(7)
     S4_CASE(8) S4_CASE(9) S4_CASE(10) S4_CASE(11) S4_CASE(12) S4_CASE(13)
 #undef S4_CASE

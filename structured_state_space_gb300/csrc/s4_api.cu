@@ -114,7 +114,7 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
   const int rows = batch * H;
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
-    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s);
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, false, /*pdl=*/true);
     // programmatic dependent: the convolution transforms its input rows while
     // the spectrum kernel finishes, and waits for it before reading K2
     if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s, /*pdl=*/true);
@@ -233,8 +233,7 @@ s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
-  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, status_of(ws, 0u), false, s);
+  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, status_of(ws, next_generation()), true, s);
 }
 
 s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -246,8 +245,7 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
-  return conv_impl(u, K, D, batch, H, L, y, ws, status_of(ws, 0u), s);
+  return conv_impl(u, K, D, batch, H, L, y, ws, status_of(ws, next_generation()), s);
 }
 
 s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -258,16 +256,15 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) != cudaSuccess) return S4_ERR_CUDA;
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
   char* w = static_cast<char*>(ws);
-  const St st = status_of(ws, 0u);
+  const St st = status_of(ws, next_generation());
   float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L).k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
-    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true);
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true, /*pdl=*/true);
     if (e == cudaSuccess) e = launch_conv_real_rows(logn, u, k2, D, y, batch, H, L, st, s, /*pdl=*/true);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s, /*realk=*/true);

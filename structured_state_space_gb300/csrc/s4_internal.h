@@ -64,9 +64,11 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
 cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int L,
                              St st, cudaStream_t s);
 // realk: the spectrum of Re K (real-output convolution), scaled by 1/n
-// instead of 1/(2n).
+// instead of 1/(2n).  The spectrum kernels are a convolution call's first
+// kernel: they record the call's generation; `pdl`: launch as a programmatic
+// dependent of the previous kernel on the stream (waited for before any access).
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, St st,
-                                 cudaStream_t s, bool realk = false);
+                                 cudaStream_t s, bool realk = false, bool pdl = false);
 // Layer path: inverse transform of the root values and the kernel spectrum in
 // one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported),
 // launched as a programmatic dependent of the root-value kernel.
