@@ -290,6 +290,46 @@ def test_layer_calls_in_a_graph_match_eager():
     assert s4.s4_get_status(ws, s) == 0
 
 
+def test_entry_points_chained_in_a_graph_match_eager():
+    # kernel generation and the two convolutions, alternating in one graph, each
+    # call's first kernel a programmatic dependent of the previous call's last:
+    # bitwise the eager results, and the status of the last call
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    u = torch.from_numpy(W.make_u(w, p)).cuda()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    Ke = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=ws)
+    ye = s4.s4_conv_fwd(u, Ke, d["D"], ws=ws)
+    yre = s4.s4_conv_fwd_real(u, Ke, d["D"], ws=ws)
+    torch.cuda.synchronize()
+    K, y, yr = torch.empty_like(Ke), torch.empty_like(ye), torch.empty_like(yre)
+    s = torch.cuda.Stream()
+
+    def calls():
+        s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, K=K, ws=ws, stream=s)
+        s4.s4_conv_fwd(u, K, d["D"], y=y, ws=ws, stream=s)
+        s4.s4_conv_fwd_real(u, K, d["D"], y=yr, ws=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+        calls()
+    K.zero_()
+    y.zero_()
+    yr.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+    s.synchronize()
+    assert torch.equal(K, Ke) and torch.equal(y, ye) and torch.equal(yr, yre)
+    assert s4.s4_get_status(ws, s) == 0
+
+
 def test_host_errors_raise():
     w = W.WORKLOADS[0]
     p = W.make_params(w)
