@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
       float2 a[R0];
 #pragma unroll
       for (int q = 0; q < R0; ++q)
-        a[q] = act ? Khat[(size_t)h * n + i + q * NB0] : make_float2(0.f, 0.f);
+        a[q] = act ? __ldcg(Khat + (size_t)h * n + i + q * NB0) : make_float2(0.f, 0.f);
       dft<R0, true>(a);
 #pragma unroll
       for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
@@ -470,8 +470,8 @@ conv_pair_kernel(
         float2 kA[RB], kB[RB], a1A[RB], a1B[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          kA[q] = STAGE ? Kr[iA + q * NBL] : __ldg(K2h + iA + q * NBL);
-          kB[q] = STAGE ? Kr[iB + q * NBL] : __ldg(K2h + iB + q * NBL);
+          kA[q] = STAGE ? Kr[iA + q * NBL] : __ldcg(K2h + iA + q * NBL);
+          kB[q] = STAGE ? Kr[iB + q * NBL] : __ldcg(K2h + iB + q * NBL);
           kA[q].x += dk;
           kB[q].x += dk;
         }
@@ -531,7 +531,7 @@ conv_pair_kernel(
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           const int k = i + q * NBL;
-          float2 kv = STAGE ? Kr[k] : __ldg(K2h + k);
+          float2 kv = STAGE ? Kr[k] : __ldcg(K2h + k);
           kv.x += dk;
           split_mul(z[sl][q], bufB[pad((n - k) & (n - 1))], kv, a0[sl][q], a1[sl][q]);
         }
@@ -686,7 +686,7 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
       dft<RB, false>(a[s]);
 #pragma unroll
       for (int q = 0; q < RB; ++q) {
-        float2 kv = __ldg(K2 + (size_t)h * n + i + q * NBL);
+        float2 kv = __ldcg(K2 + (size_t)h * n + i + q * NBL);
         kv.x += dk;
         a[s][q] = cmul(a[s][q], kv);
       }
@@ -749,7 +749,10 @@ static int grid_for(KernelT k, int threads, size_t smem, int ctas_needed) {
 
 // Launch with the programmatic-serialization attribute when `pdl` is set:
 // the kernel may start before the previous kernel on the stream finishes and
-// synchronises with it through pdl_wait().
+// synchronises with it through pdl_wait().  Such a kernel is running while
+// its predecessor writes, so it reads the predecessor's output through L2
+// (__ldcg, or bulk copies), never through the non-coherent read-only path
+// (__ldg): an SM's L1 may still hold that region from an earlier kernel.
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), int grid, int threads, size_t smem,
                                     cudaStream_t s, bool pdl, Args... args) {
