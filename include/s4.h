@@ -30,12 +30,15 @@
  *    status block at the start of `ws` and read with s4_get_status; when one
  *    is recorded, the affected output (K, or y) is written as all zeros.
  *    The block holds the flags, the generation they were set under and the
- *    generation of the last call.  s4_kernel_gen, s4_conv_fwd,
- *    s4_conv_fwd_real and s4_layer_fwd tag their flags with a fresh
- *    generation instead of clearing the block, so such a call is kernels only
- *    and chains to the kernel before it on the stream; s4_ctilde and
- *    s4_recurrent_fwd clear it (an enqueued memset).  Either way
- *    s4_get_status reports the last call only, whatever `ws` held before.
+ *    generation of the last call.  Called on a stream that is not being
+ *    captured, s4_kernel_gen, s4_conv_fwd, s4_conv_fwd_real and
+ *    s4_layer_fwd tag their flags with a fresh generation instead of
+ *    clearing the block, so such a call is kernels only and chains to the
+ *    kernel before it on the stream.  Captured into a CUDA graph (a captured
+ *    call would replay its generation), and for s4_ctilde and
+ *    s4_recurrent_fwd, a call clears the block first (an enqueued memset).
+ *    Either way s4_get_status reports the last call only, whatever `ws` held
+ *    before.
  *  - Concurrent calls that share one `ws` race; give each stream its own.
  *
  * Supported sizes: 1 <= H, 1 <= N <= 65536, 1 <= r <= 4, 1 <= L <= 65536,

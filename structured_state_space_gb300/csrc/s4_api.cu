@@ -63,7 +63,7 @@ s4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? S4_OK : S4_ERR_
 s4impl::St status_of(void* ws, unsigned gen) { return s4impl::St{static_cast<unsigned*>(ws), gen}; }
 constexpr size_t kStatusBlockBytes = 3 * sizeof(unsigned);
 
-// Generations of layer calls: 1, 2, ... (0 marks a status block reset by a memset).
+// Generations of calls: 1, 2, ... (0 marks a status block reset by a memset).
 unsigned next_generation() {
   static std::atomic<unsigned> g_gen{0};
   unsigned g;
@@ -71,6 +71,26 @@ unsigned next_generation() {
     g = g_gen.fetch_add(1u) + 1u;
   } while (g == 0u);
   return g;
+}
+
+// The status of a call on `s`: a fresh generation, with no reset of the block
+// and the call's first kernel chained to the previous kernel (`chain`) -- unless
+// `s` is being captured into a graph.  A captured call would replay its
+// generation every time the graph runs, so flags a replay sets would read as
+// current in the next replay; captured calls therefore reset the block with a
+// memset (generation 0) each time they run, and their first kernel is launched
+// normally.  Returns false if the memset cannot be enqueued.
+bool call_status(void* ws, cudaStream_t s, s4impl::St* st, bool* chain) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return false;
+  if (cs != cudaStreamCaptureStatusNone) {
+    *st = status_of(ws, 0u);
+    *chain = false;
+    return cudaMemsetAsync(ws, 0, kStatusBlockBytes, s) == cudaSuccess;
+  }
+  *st = status_of(ws, next_generation());
+  *chain = true;
+  return true;
 }
 
 cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
@@ -103,7 +123,7 @@ s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const
 }
 
 s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
-                    s4_c32* y, void* ws, s4impl::St st, cudaStream_t s) {
+                    s4_c32* y, void* ws, s4impl::St st, bool chain, cudaStream_t s) {
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
   const Layout lay = layout_for(H, L);
@@ -114,7 +134,7 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
   const int rows = batch * H;
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
-    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, false, /*pdl=*/true);
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, false, /*pdl=*/chain);
     // programmatic dependent: the convolution transforms its input rows while
     // the spectrum kernel finishes, and waits for it before reading K2
     if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s, /*pdl=*/true);
@@ -233,7 +253,10 @@ s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, status_of(ws, next_generation()), true, s);
+  s4impl::St st;
+  bool chain;
+  if (!call_status(ws, s, &st, &chain)) return S4_ERR_CUDA;
+  return gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, chain, s);
 }
 
 s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -245,7 +268,10 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch
   const s4_status wst = check_ws(ws, ws_bytes, H, L);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return conv_impl(u, K, D, batch, H, L, y, ws, status_of(ws, next_generation()), s);
+  s4impl::St st;
+  bool chain;
+  if (!call_status(ws, s, &st, &chain)) return S4_ERR_CUDA;
+  return conv_impl(u, K, D, batch, H, L, y, ws, st, chain, s);
 }
 
 s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int batch, int H, int L,
@@ -259,12 +285,14 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
   char* w = static_cast<char*>(ws);
-  const St st = status_of(ws, next_generation());
+  St st;
+  bool chain;
+  if (!call_status(ws, s, &st, &chain)) return S4_ERR_CUDA;
   float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L).k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
-    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true, /*pdl=*/true);
+    e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, /*realk=*/true, /*pdl=*/chain);
     if (e == cudaSuccess) e = launch_conv_real_rows(logn, u, k2, D, y, batch, H, L, st, s, /*pdl=*/true);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s, /*realk=*/true);
@@ -290,7 +318,9 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
   // No reset of the status block: this call's flags carry a fresh generation,
   // so the call is kernels only and its first kernel (root values) can be a
   // programmatic dependent of whatever kernel precedes it on the stream.
-  const s4impl::St st = status_of(ws, next_generation());
+  s4impl::St st;
+  bool chain;
+  if (!call_status(ws, s, &st, &chain)) return S4_ERR_CUDA;
   const int logM = ilog2_ceil(L);
   if (s4impl::kspec_supported(logM) && logM + 1 <= s4impl::kMaxLogConvRow) {
     // root values -> (K, kernel spectrum) in one launch -> convolution
@@ -298,7 +328,7 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
     char* w = static_cast<char*>(ws);
     float2* khat = reinterpret_cast<float2*>(w + lay.khat);
     float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
-    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, true, s);
+    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s);
     if (e == cudaSuccess)
       e = s4impl::launch_kspec_rows(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
     if (e == cudaSuccess)
@@ -306,9 +336,9 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
                                    /*pdl=*/true);
     return cuda_status(e);
   }
-  const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, true, s);
+  const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, chain, s);
   if (g != S4_OK) return g;
-  return conv_impl(u, K, D, batch, H, L, y, ws, st, s);
+  return conv_impl(u, K, D, batch, H, L, y, ws, st, /*chain=*/true, s);
 }
 
 s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const float* dt,

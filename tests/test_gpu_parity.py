@@ -290,6 +290,52 @@ def test_layer_calls_in_a_graph_match_eager():
     assert s4.s4_get_status(ws, s) == 0
 
 
+def test_graph_replay_after_a_flagged_replay():
+    # a replay whose inputs were fixed after a flagged replay must not see the
+    # earlier replay's flag: each execution of a captured call is a new call
+    w = W.WORKLOADS[1]
+    p = W.make_params(w)
+    d = dev(p)
+    u = torch.from_numpy(W.make_u(w, p)).cuda()
+    ws = s4.workspace(w.H, w.N, w.r, w.L, w.batch)
+    K_ref, y_ref = _layer(d, u, ws)
+    K_ref2 = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L, ws=ws)
+    y_ref2 = s4.s4_conv_fwd(u, K_ref2, d["D"], ws=ws)
+    torch.cuda.synchronize()
+    dt = d["dt"].clone()
+    K, y = torch.empty_like(K_ref), torch.empty_like(y_ref)
+    K2, y2 = torch.empty_like(K_ref2), torch.empty_like(y_ref2)
+    s = torch.cuda.Stream()
+
+    def calls():  # the layer call last: s4_get_status reports the last call
+        s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], dt, w.L, K=K2, ws=ws, stream=s)
+        s4.s4_conv_fwd(u, K2, d["D"], y=y2, ws=ws, stream=s)
+        with torch.cuda.stream(s):
+            _layer(d, u, ws, K=K, y=y, dt=dt)
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    for bad in (True, False, True, False):
+        dt.copy_(d["dt"])
+        if bad:
+            dt[7] = float("nan")
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        st = s4.s4_get_status(ws, s)
+        if bad:
+            assert st == s4.STATUS_CODE["S4_ERR_INVALID_STEP"]
+            assert torch.count_nonzero(y).item() == 0
+        else:
+            assert st == 0
+            assert torch.equal(K, K_ref) and torch.equal(y, y_ref)
+            assert torch.equal(K2, K_ref2) and torch.equal(y2, y_ref2)
+
+
 def test_entry_points_chained_in_a_graph_match_eager():
     # kernel generation and the two convolutions, alternating in one graph, each
     # call's first kernel a programmatic dependent of the previous call's last:
