@@ -163,7 +163,7 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
  *   stream capture.
  *   All calls share the one array: calls that can overlap on the GPU (work
  *   on streams not ordered with each other) race and must not be issued.
- *   A non-finite kernel spectrum writes y as zeros; no status word is exposed.
+ *   A non-finite kernel spectrum writes y as zeros; no status block is exposed.
  *   Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
  */
 #define S4_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -175,10 +175,12 @@ s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const float* D,
  * Page "Recurrent, LSTM, and structured state-space models": for a filter of
  * transform length M (least power of two >= L) the output vector is
  * C~ = (I - Abar^M)^* C; the filter procedure receives it as given data, and
- * this entry point forms it.  Computed as C - (Abar^*)^M C with M steps of
- * Abar^* w = 2 G^{-*} w - w (G = I - (Delta/2) A), each a rank-r Woodbury solve.
+ * this entry point forms it.  Computed as C - (Abar^*)^M C, Abar^* w =
+ * 2 G^{-*} w - w (G = I - (Delta/2) A) being a diagonal plus a rank-r term
+ * (the Woodbury form of G^{-*}); the kernel squares that form to Abar^{*p}
+ * (diagonal plus rank p r) and takes M/p steps of it.
  *   Lambda, P, Q, dt as for s4_kernel_gen; C [H][N] (input); Ctilde [H][N] (output).
- *   N <= 256.  ws: at least 256 bytes (the status word; see s4_get_status).
+ *   N <= 256.  ws: at least 256 bytes (the status block; see s4_get_status).
  * Device-detected statuses: S4_ERR_SINGULAR_BILINEAR, S4_ERR_INVALID_STEP (Ctilde zeros).
  */
 s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const float* dt,
@@ -195,7 +197,7 @@ s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, cons
  *   output vector (not C~).  u [batch][H][L] inputs; y [batch][H][L] outputs.
  *   x [batch][H][N]: the state x_{-1} on entry and x_{L-1} on return, so
  *   consecutive calls continue one sequence (zeros for a fresh sequence).
- *   N <= 256.  ws: at least 256 bytes (the status word).
+ *   N <= 256.  ws: at least 256 bytes (the status block).
  * Device-detected statuses: S4_ERR_SINGULAR_BILINEAR, S4_ERR_INVALID_STEP (y and x zeros).
  */
 s4_status s4_recurrent_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q,
