@@ -498,7 +498,7 @@ def run_ours(args):
         "kernels": kern,
         "profiled_pass": {"steps": S, "ms_per_step": ms_prof / S,
                           "how": "eager C-ABI calls with the library's launch events around each kernel"},
-        "launch": f"captured CUDA graph of {G} consecutive s4_layer_fwd calls ({launches_per_step} kernels each), replayed; remainder steps from single-call graphs",
+        "launch": f"captured CUDA graph of {G} consecutive s4_layer_fwd calls (a status-block memset and {launches_per_step} kernels each: captured calls reset the block), replayed; remainder steps from single-call graphs",
         "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(u_host.nbytes),
