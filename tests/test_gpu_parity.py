@@ -320,10 +320,10 @@ def test_graph_replay_after_a_flagged_replay():
     with torch.cuda.graph(g, stream=s):
         calls()
     for bad in (True, False, True, False):
-        dt.copy_(d["dt"])
-        if bad:
-            dt[7] = float("nan")
-        with torch.cuda.stream(s):
+        with torch.cuda.stream(s):  # the input update is ordered before the replay
+            dt.copy_(d["dt"])
+            if bad:
+                dt[7] = float("nan")
             g.replay()
         s.synchronize()
         st = s4.s4_get_status(ws, s)
