@@ -3,17 +3,19 @@ convolution) on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-A step is one s4_layer_fwd over one batch of the workload N=64, r=1, H=256,
-L=1024, batch 16 (synthetic inputs resident in HBM).  Input/output buffer sets
+A step is one s4_layer_fwd over one batch of the largest workload, N=256,
+r=1, H=1024, L=65536, batch 2 (synthetic inputs resident in HBM); --workload
+picks one of the smaller seeded workloads instead.  Input/output buffer sets
 rotate so that the bytes touched between two uses of the same buffer exceed
 twice the L2 size.  `value` is channel-samples per second (batch*H*L per step,
 summed over ranks / max time over ranks).  `e2e` times the same call with the
 input copied from pinned host memory and the output copied back every step.
 Each step replays a CUDA graph holding one captured s4_layer_fwd call (one
 graph per buffer set), so host launch overhead does not enter the timing.
-Per-kernel durations come from the library's launch events, captured as
-event-record nodes around every kernel of a separate multi-step graph.  The CPU baseline is the
-float64 oracle on the host cores.  `--impl reference` times that oracle alone.
+Per-kernel durations come from the library's launch events (CUDA events on
+the launch stream around every kernel) over eager C-ABI calls.  The CPU
+baseline is the float64 oracle on the host cores, on a stated sample of the
+workload's channels.  `--impl reference` times that oracle alone.
 """
 from __future__ import annotations
 
@@ -35,13 +37,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "S4 layer fwd channel-samples/s (B·H·L/s); Cauchy terms/s; % FP32 / HBM roofline"
 UNIT = "channel-samples/s"
-# The bench line is workload 1; --workload selects another of the seeded
-# workloads for per-workload measurement and profiling (its line then carries
-# no CPU baseline and no profiled traffic).  Spawned oracle workers read the
-# choice from the environment.
-WORKLOAD_INDEX = int(os.environ.get("S4_BENCH_WORKLOAD", "1"))
-SM_COUNT_NOMINAL = 152
+# The layer's bench line is the largest workload (index 4), the one that fits
+# one GPU with the most work; --workload selects another of the seeded
+# workloads.  The auxiliary paths (--path) default to workload 1.  Spawned
+# oracle workers read the choice from the environment.
+LAYER_WORKLOAD = 4
+PATH_WORKLOAD = 1
+WORKLOAD_INDEX = int(os.environ.get("S4_BENCH_WORKLOAD", str(LAYER_WORKLOAD)))
 FP32_LANES_PER_SM = 128
+
+
+def cauchy_flop(r):
+    """Algorithmic flop per (channel, root, pole) term of the root-value sums:
+    8 (r+1)^2 for the complex multiply-adds of the (r+1)^2 weighted
+    reciprocals, plus 10 for the denominator s - lambda_j and its reciprocal
+    (42 at rank 1, 82 at rank 2)."""
+    return 8 * (r + 1) ** 2 + 10
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -134,13 +145,13 @@ KERNEL_FILES = {
 }
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of that kernel; else None."""
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch on `workload` from the committed ncu summary, if
+    they were taken on the current source of that kernel; else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
-        e = d[kernel]
+        e = d[workload][kernel]
         if e.get("source_hash") != kernel_source_hash(KERNEL_FILES[kernel]):
             return None
         return e["dram_bytes_per_launch"]
@@ -159,18 +170,31 @@ def _oracle_init():
 
 
 def _oracle_channel(args):
-    """Oracle on one channel: its kernel and every batch row's convolution.
+    """Oracle on one channel: its kernel and the convolution of each of the
+    channel's input rows.  `args` carries the channel's parameters and rows
+    (sent by the parent, so workers never build the whole workload).
     Returns the channel-samples produced."""
-    h, = args
-    import numpy as np  # noqa: F401
+    lam, P, Q, B, Ct, dt, D, rows, L = args
     import oracle.s4_oracle as O
+    K = O.s4_kernel(lam, P, Q, B, Ct, dt, L)
+    for row in rows:
+        O.causal_conv(K, row, D)
+    return len(rows) * L
+
+
+def channel_units(p, u, chans, L):
+    """Work items of _oracle_channel for the listed channels (all batch rows)."""
+    import numpy as np
+    return [(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["Ctilde"][h], float(p["dt"][h]),
+             float(p["D"][h]), np.ascontiguousarray(u[:, h, :]), L) for h in chans]
+
+
+def baseline_channels(w):
+    """Channels of the CPU baseline's sample: every channel of the small
+    workloads, the stated 8-channel sample (first two, middle two, last, four
+    seeded) of the large ones."""
     from structured_state_space_gb300 import workloads as W
-    w = W.WORKLOADS[WORKLOAD_INDEX]
-    p, u = _oracle_data()
-    K = O.s4_kernel(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["Ctilde"][h], p["dt"][h], w.L)
-    for b in range(w.batch):
-        O.causal_conv(K, u[b, h], p["D"][h])
-    return w.batch * w.L
+    return list(range(w.H)) if w.batch * w.H * w.L <= (1 << 24) else W.sample_channels(w)
 
 
 _DATA = None
@@ -186,17 +210,21 @@ def _oracle_data():
     return _DATA
 
 
-def _worker_start():
-    _oracle_init()
-    _oracle_data()
+def _warm_unit():
+    """A tiny oracle work item: imports and first-call costs out of the timing."""
+    import numpy as np
+    N, L = 4, 64
+    lam = (-0.5 + 1j * np.pi * np.arange(N)).astype(np.complex64)
+    v = np.full(N, 0.1, np.complex64)
+    return (lam, v.reshape(N, 1), v.reshape(N, 1), v, v, 0.01, 0.5, np.ones((1, L), np.float32), L)
 
 
 def make_pool(procs):
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[k] = "1"
     ctx = mp.get_context("spawn")
-    pool = ctx.Pool(procs, initializer=_worker_start)
-    pool.map(_oracle_channel, [(0,)] * procs)  # warm: imports, data, caches
+    pool = ctx.Pool(procs, initializer=_oracle_init)
+    pool.map(_oracle_channel, [_warm_unit()] * procs)
     return pool
 
 
@@ -217,8 +245,8 @@ def timed_passes(pool, procs, fn, items, max_passes=50):
             return done, dt, passes
 
 
-def oracle_rate(pool, procs, channels):
-    samples, dt, passes = timed_passes(pool, procs, _oracle_channel, [(h,) for h in channels])
+def oracle_rate(pool, procs, units):
+    samples, dt, passes = timed_passes(pool, procs, _oracle_channel, units)
     return samples / dt, dt, samples, passes
 
 
@@ -259,10 +287,13 @@ def run_ours(args):
     from structured_state_space_gb300 import workloads as W
 
     rank, local_rank, world = dist_env()
-    # CPU baseline pool first: spawned before any GPU work
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    # CPU baseline pool first: spawned before any GPU work, one process per
+    # sampled channel up to the host's cores
     pool, procs = None, 0
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and WORKLOAD_INDEX == 1:
-        procs = max(1, os.cpu_count() or 1)
+    base_chans = baseline_channels(w)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        procs = max(1, min(os.cpu_count() or 1, len(base_chans)))
         pool = make_pool(procs)
 
     torch.cuda.set_device(local_rank)
@@ -274,7 +305,6 @@ def run_ours(args):
         dist.barrier()
     s4.load()
 
-    w = W.WORKLOADS[WORKLOAD_INDEX]
     H, N, r, L, Bsz, M = w.H, w.N, w.r, w.L, w.batch, w.M
     p = W.make_params(w)
     u_host = W.make_u(w, p)
@@ -437,53 +467,51 @@ def run_ours(args):
     e2e_value = multi.job_throughput(samples_step, e2e_steps_done, world, ms_e2e)
 
     peaks, peak_src = read_peaks()
-    # roofline of the dominant kernel
-    dom = max(kern, key=lambda k: kern[k]["avg_us"])
-    fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    if dom == "cauchy":
-        flops = H * M * N * (8 * (r + 1) ** 2 + 6)
-        ach = flops / (kern[dom]["avg_us"] * 1e-6) / 1e12
-        roof = {"kernel": "cauchy_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": ach / fp32_peak, "traffic": profiled_traffic("cauchy") if WORKLOAD_INDEX == 1 else None,
-                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
-                "algorithmic": f"{8 * (r + 1) ** 2 + 6} flop per (channel, root, pole)"}
-    else:
-        # algorithmic bytes of the named kernel per launch
-        if dom == "conv":
-            byts = Bsz * H * L * (4 + 8) + H * 2 * M * 8
-            desc = "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"
-        elif dom == "spectrum":
-            byts = H * L * 8 + H * 2 * M * 8
-            desc = "K 8 B per tap in, spectrum 8 B per 2M bin out"
-        elif dom == "kspec":
-            byts = H * M * 8 + H * L * 8 + H * 2 * M * 8
-            desc = "root values 8 B in, K 8 B out, spectrum 8 B per 2M bin out"
-        elif dom == "ifft":
-            byts = H * M * 8 + H * L * 8
-            desc = "root values 8 B in, K 8 B out"
+    sms = props.multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    peak_source = f"{sms} SMs (queried) x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x max SM clock"
+    lg2m = (2 * M).bit_length() - 1
+    # algorithmic work per launch of each kernel family: (bound, amount, description)
+    work = {
+        "cauchy": ("alu", H * M * N * cauchy_flop(r), f"{cauchy_flop(r)} flop per (channel, root, pole)"),
+        "conv": ("hbm", Bsz * H * L * (4 + 8) + H * 2 * M * 8,
+                 "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"),
+        "spectrum": ("hbm", H * L * 8 + H * 2 * M * 8, "K 8 B per tap in, spectrum 8 B per 2M bin out"),
+        "kspec": ("hbm", H * M * 8 + H * L * 8 + H * 2 * M * 8,
+                  "root values 8 B in, K 8 B out, spectrum 8 B per 2M bin out"),
+        "ifft": ("hbm", H * M * 8 + H * L * 8, "root values 8 B in, K 8 B out"),
+    }
+
+    def roof_of(name):
+        bound, amount, desc = work[name]
+        t = kern[name]["avg_us"] * 1e-6
+        if bound == "alu":
+            ach = amount / t / 1e12
+            e = {"kernel": f"{name}_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak,
+                 "unit": "TFLOP/s", "frac": ach / fp32_peak, "peak_source": peak_source}
         else:
-            byts = M * 8
-            desc = "table 8 B per root"
-        ach = byts / (kern[dom]["avg_us"] * 1e-6) / 1e9
-        roof = {"kernel": f"{dom}_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic(dom) if WORKLOAD_INDEX == 1 else None,
-                "algorithmic": desc}
-        if dom == "conv":
+            ach = amount / t / 1e9
+            e = {"kernel": f"{name}_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+        e["traffic"] = profiled_traffic(name, w.name)
+        e["algorithmic"] = desc
+        e["avg_us"] = kern[name]["avg_us"]
+        if name == "conv":
             # the transforms' arithmetic (about 15 flop per byte moved) is above the FP32/HBM
             # ridge (about 12 flop per byte), so the FP32 side is reported as well
-            lg = (2 * M).bit_length() - 1
-            cflops = Bsz * H * (15 * M * lg + 16 * M)
-            cach = cflops / (kern[dom]["avg_us"] * 1e-6) / 1e12
-            roof["fp32"] = {"achieved": cach, "peak": fp32_peak, "unit": "TFLOP/s", "frac": cach / fp32_peak,
-                            "algorithmic": "15 M log2(2M) + 16 M flop per batch row (real-input forward, "
-                                           "complex inverse, 5 n log2 n per transform)"}
+            cflops = Bsz * H * (15 * M * lg2m + 16 * M)
+            cach = cflops / t / 1e12
+            e["fp32"] = {"achieved": cach, "peak": fp32_peak, "unit": "TFLOP/s", "frac": cach / fp32_peak,
+                         "algorithmic": "15 M log2(2M) + 16 M flop per batch row (real-input forward, "
+                                        "complex inverse, 5 n log2 n per transform)"}
+        return e
+
+    # roofline of the dominant kernel, the other kernels of the step beside it
+    dom = max(kern, key=lambda k: kern[k]["avg_us"])
+    roof = roof_of(dom)
     roof["peak_kind"] = f"of {peak_src}"
     roof["fp32_probe"] = fp32_probe(dev, fp32_peak)
-    if dom != "cauchy" and kern.get("cauchy", {}).get("launches"):
-        # the root-value kernel's FP32 fraction, beside the dominant kernel's
-        cach = H * M * N * (8 * (r + 1) ** 2 + 6) / (kern["cauchy"]["avg_us"] * 1e-6) / 1e12
-        roof["cauchy_fp32"] = {"achieved": cach, "peak": fp32_peak, "unit": "TFLOP/s", "frac": cach / fp32_peak,
-                               "algorithmic": f"{8 * (r + 1) ** 2 + 6} flop per (channel, root, pole)"}
+    roof["others"] = {k: roof_of(k) for k in kern if k != dom and kern[k]["launches"]}
 
     launches_per_step = int(round(sum(v["launches"] for v in kern.values()) / S))
     line = {
@@ -506,11 +534,14 @@ def run_ours(args):
                 "how": "per step: H2D of u from pinned memory, the layer graph, D2H of y to pinned memory; three streams pipeline consecutive steps"},
     }
     if pool is not None:
-        # bounded sample: every channel of the workload, each with all batch rows
-        chans = list(range(H))
-        rate, secs, samples, passes = oracle_rate(pool, procs, chans)
+        # bounded sample: the sampled channels (every channel of a small
+        # workload), each with its kernel and all of its batch rows
+        units = channel_units(p, u_host, base_chans, L)
+        rate, secs, samples, passes = oracle_rate(pool, procs, units)
+        what = ("the whole workload" if len(base_chans) == H else
+                f"channels {base_chans} of {H}")
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": procs, "kind": "oracle",
-                                "sample": f"{passes} passes over the whole workload, {len(chans)} channels x {Bsz} rows "
+                                "sample": f"{passes} passes over {what}: {len(base_chans)} channels x {Bsz} rows "
                                           f"x L={L} ({samples} channel-samples, {secs:.1f} s wall, ~{secs * procs:.0f} CPU-s)"}
         pool.close()
     if rank == 0:
@@ -684,7 +715,9 @@ def run_path(args):
     per_call = H * M if args.path in ("ctilde", "kernel_gen") else Bsz * H * L
     value = per_call * K / (ms_total / 1e3)
     peaks, peak_src = read_peaks()
-    fp32_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    sms = props.multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    peak_source = f"{sms} SMs (queried) x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x max SM clock"
     if args.path in ("conv", "conv_real"):
         yb = 4 if args.path == "conv_real" else 8
         byts = Bsz * H * L * (4 + yb) + H * 2 * M * 8
@@ -694,12 +727,12 @@ def run_path(args):
                 "traffic": None,
                 "algorithmic": f"u 4 B + y {yb} B per channel-sample, kernel spectrum 16 B per channel-root once"}
     elif args.path == "kernel_gen":
-        flops = H * M * N * (8 * (r + 1) ** 2 + 6)
+        flops = H * M * N * cauchy_flop(r)
         ach = flops / (kern[dom]["avg_us"] * 1e-6) / 1e12
         roof = {"kernel": "cauchy_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
                 "frac": ach / fp32_peak, "traffic": None,
-                "algorithmic": f"{8 * (r + 1) ** 2 + 6} flop per (channel, root, pole)",
-                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+                "algorithmic": f"{cauchy_flop(r)} flop per (channel, root, pole)",
+                "peak_source": peak_source}
     else:
         steps = Bsz * H * L if args.path == "recurrent" else H * M
         flops = steps * N * (20 + 16 * r)
@@ -707,7 +740,7 @@ def run_path(args):
         roof = {"kernel": f"{dom}_kernel", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
                 "frac": ach / fp32_peak, "traffic": None,
                 "algorithmic": f"{20 + 16 * r} flop per (row or channel, step, state element)",
-                "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+                "peak_source": peak_source}
     roof["peak_kind"] = f"of {peak_src}"
     # end to end: input from pinned host memory, the call, output back, one stream
     e2e = None
@@ -756,12 +789,16 @@ def run_reference(args):
         return
     from structured_state_space_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD_INDEX]
-    procs = max(1, os.cpu_count() or 1)
+    procs = max(1, min(os.cpu_count() or 1, w.H))
     pool = make_pool(procs)
-    # one step = one channel per worker process, each with every batch row
+    p = W.make_params(w)
+    u = W.make_u(w, p)
+
+    # one step = one channel per worker process (its kernel and every batch
+    # row), channels taken in turn through the workload
     def step(i):
         chans = [((i * procs) + j) % w.H for j in range(procs)]
-        return sum(pool.map(_oracle_channel, [(h,) for h in chans]))
+        return sum(pool.map(_oracle_channel, channel_units(p, u, chans, w.L)))
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
@@ -777,7 +814,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {"workload": w.name, "N": w.N, "r": w.r, "H": w.H, "L": w.L, "M": w.M, "batch": w.batch},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
-                         "sample": f"per step {procs} channels x {w.batch} rows x L={w.L}"},
+                         "sample": f"per step {procs} channels (taken in turn) x {w.batch} rows x L={w.L}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -793,12 +830,14 @@ def main():
     ap.add_argument("--path", choices=["layer"] + sorted(PATHS), default="layer",
                     help="layer (the bench line) or a step either side of it")
     ap.add_argument("--workload", type=int, default=None,
-                    help="seeded workload index (default 1, the benchmark workload)")
+                    help=f"seeded workload index (default {LAYER_WORKLOAD} for the layer and the reference arm, "
+                         f"{PATH_WORKLOAD} for --path)")
     args = ap.parse_args()
-    if args.workload is not None:
-        global WORKLOAD_INDEX
-        WORKLOAD_INDEX = args.workload
-        os.environ["S4_BENCH_WORKLOAD"] = str(args.workload)
+    global WORKLOAD_INDEX
+    if args.workload is None:
+        args.workload = PATH_WORKLOAD if args.path != "layer" and args.impl != "reference" else LAYER_WORKLOAD
+    WORKLOAD_INDEX = args.workload
+    os.environ["S4_BENCH_WORKLOAD"] = str(args.workload)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

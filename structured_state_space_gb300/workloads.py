@@ -128,3 +128,16 @@ def scalar_example(L: int, u=None) -> dict:
         "C": np.ones((1, 1), np.complex64), "dt": np.ones(1, np.float32),
         "D": np.zeros(1, np.float32), "u": np.asarray(u, np.float32).reshape(1, 1, L),
     }
+
+
+def sample_channels(w: Workload, extra: int = 4, seed: int = 4242) -> list:
+    """Channels checked (and timed on the CPU) for workloads too large to take
+    whole: the first two, the two around the middle, the last, and `extra`
+    seeded others, sorted.  Small workloads (H <= 8) return every channel."""
+    if w.H <= 8:
+        return list(range(w.H))
+    fixed = {0, 1, w.H // 2 - 1, w.H - 1}
+    rest = np.array([h for h in range(w.H) if h not in fixed])
+    rng = np.random.default_rng(seed)
+    picked = rng.choice(rest, size=min(extra, rest.size), replace=False)
+    return sorted(fixed | {int(h) for h in picked})

@@ -10,13 +10,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_reference_arm_json_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference"
     assert line["unit"] == "channel-samples/s" and line["value"] > 0
-    assert line["steps"] == 2 and line["warmup"] == 3 and line["higher_is_better"] is True
-    assert line["config"]["workload"].startswith("s4-fwd N64 r1 H256 L1024 B16")
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "s4-fwd N256 r1 H1024 L65536 B2"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]

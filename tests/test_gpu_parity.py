@@ -55,16 +55,15 @@ def run_layer(p, u):
     return K.cpu().numpy(), y.cpu().numpy()
 
 
-# sampled channels per workload (all of them for the small ones)
+# sampled channels per workload: all of them for the small ones, else the
+# first two, the middle two, the last and `count - 4` seeded others
 def _channels(w, count):
     if w.H <= count:
         return list(range(w.H))
-    rng = np.random.default_rng(77)
-    extra = rng.choice(np.arange(2, w.H - 2), size=count - 4, replace=False)
-    return sorted(set([0, 1, w.H // 2, w.H - 1] + [int(x) for x in extra]))
+    return W.sample_channels(w, extra=count - 4)
 
 
-@pytest.mark.parametrize("wi,nch,full_rows", [(0, 2, True), (1, 256, True), (2, 16, True), (3, 6, True), (4, 4, False)])
+@pytest.mark.parametrize("wi,nch,full_rows", [(0, 2, True), (1, 256, True), (2, 16, True), (3, 8, True), (4, 8, False)])
 def test_layer_matches_oracle(wi, nch, full_rows):
     w = W.WORKLOADS[wi]
     p = W.make_params(w)
