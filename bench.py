@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -555,8 +556,8 @@ PATHS = {
     "kernel_gen": ("channel-roots/s", ["cauchy", "ifft"], "cauchy"),
     "conv": ("channel-samples/s", ["spectrum", "conv"], "conv"),
     "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
-    "recurrent": ("channel-samples/s", ["recurrent"], "recurrent"),
-    "ctilde": ("channel-steps/s", ["ctilde"], "ctilde"),
+    "recurrent": ("channel-samples/s", ["recurrent", "bordered"], "recurrent"),
+    "ctilde": ("channel-steps/s", ["ctilde", "bordered"], "ctilde"),
 }
 
 
@@ -829,6 +830,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["layer"] + sorted(PATHS), default="layer",
                     help="layer (the bench line) or a step either side of it")
+    ap.add_argument("--channels", type=int, default=None,
+                    help="layer only: run the workload with this many channels instead (a smaller copy "
+                         "for ncu captures; its line is not a bench line)")
     ap.add_argument("--workload", type=int, default=None,
                     help=f"seeded workload index (default {LAYER_WORKLOAD} for the layer and the reference arm, "
                          f"{PATH_WORKLOAD} for --path)")

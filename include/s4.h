@@ -64,9 +64,9 @@ typedef enum {
     S4_ERR_NONFINITE = 5,            /* a root value or spectrum entry is inf/nan */
     S4_ERR_INVALID_STEP = 6,         /* some Delta_h <= 0 or not finite */
     S4_ERR_CUDA = 7,                 /* a CUDA runtime call or launch failed */
-    S4_ERR_SINGULAR_BILINEAR = 8,    /* G = I - (Delta/2) A not solved: some d_j = 1 - (Delta/2) lambda_j
-                                        is exactly 0 (the bordered branch, not taken on the GPU)
-                                        or I_r + (Delta/2) Q^* D^{-1} P is exactly singular */
+    S4_ERR_SINGULAR_BILINEAR = 8,    /* G = I - (Delta/2) A not solved: I_r + (Delta/2) Q^* D^{-1} P is
+                                        exactly singular; or, where some d_j = 1 - (Delta/2) lambda_j is
+                                        exactly 0, more such d_j than r, or a singular bordered matrix */
     S4_ERR_TIMEOUT = 9               /* a kernel's bounded wait for an asynchronous copy into shared
                                         memory ran out (the affected output is zeros) */
 } s4_status;
@@ -178,7 +178,9 @@ s4_status s4_conv_fwd_noalloc(const float* u, const s4_c32* K, const float* D,
  * this entry point forms it.  Computed as C - (Abar^*)^M C, Abar^* w =
  * 2 G^{-*} w - w (G = I - (Delta/2) A) being a diagonal plus a rank-r term
  * (the Woodbury form of G^{-*}); the kernel squares that form to Abar^{*p}
- * (diagonal plus rank p r) and takes M/p steps of it.
+ * (diagonal plus rank p r) and takes M/p steps of it.  A channel with an
+ * exactly zero d_j = 1 - (Delta/2) lambda_j takes M single steps instead, each
+ * solving G^* by the conjugated bordered system of s4_recurrent_fwd.
  *   Lambda, P, Q, dt as for s4_kernel_gen; C [H][N] (input); Ctilde [H][N] (output).
  *   N <= 256.  ws: at least 256 bytes (the status block; see s4_get_status).
  * Device-detected statuses: S4_ERR_SINGULAR_BILINEAR, S4_ERR_INVALID_STEP (Ctilde zeros).
@@ -192,7 +194,10 @@ s4_status s4_ctilde(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, cons
  * Page "Recurrent, LSTM, and structured state-space models", section "DPLR
  * structured state-space parameterization", recurrent mode:
  *     b_t = (I + (Delta/2) A) x_{t-1} + Delta B u_t,   G x_t = b_t,   y_t = C^* x_t + D u_t,
- * G solved by the Woodbury inverse with D = diag(1 - (Delta/2) lambda_j).
+ * G solved by the Woodbury inverse with D = diag(1 - (Delta/2) lambda_j); in a
+ * channel where some of those d_j are exactly 0 in fp32 (the set Z, s = |Z| <= r),
+ * by the pages' bordered system of size r + s for (Q^* x, x_Z), with
+ * x_J = D_J^{-1}(b_J - (Delta/2) P_J Q^* x) on the other states.
  *   Lambda, P, Q, B, dt, D as for s4_layer_fwd; C [H][N] is the conventional
  *   output vector (not C~).  u [batch][H][L] inputs; y [batch][H][L] outputs.
  *   x [batch][H][N]: the state x_{-1} on entry and x_{L-1} on return, so
@@ -247,12 +252,24 @@ const char* s4_status_str(s4_status st);
  * library is bracketed by CUDA events recorded on its launch stream.
  * s4_timing_read syncs those events and returns, for the kernel family
  * `name` ("cauchy", "ifft", "spectrum", "kspec", "conv", "conv_real",
- * "recurrent", "ctilde"), the number of launches and their summed duration
+ * "recurrent", "ctilde", "bordered"), the number of launches and their summed duration
  * in milliseconds since the last reset.  Timing state is per process; it is
  * meant for benchmarks, not for use from several host threads at once. */
 void s4_timing_enable(int on);
 void s4_timing_reset(void);
 int  s4_timing_read(const char* name, int* launches, double* total_ms);
+
+/* Fault-detection test hook, outside the method: the number of polls a
+ * kernel's bounded wait on an asynchronous copy into shared memory makes
+ * before it gives up and records S4_ERR_TIMEOUT (default 4194304; polls < 0
+ * restores the default, 0 makes every such wait give up at once).  Only the
+ * staged kernels wait this way: the convolution of rows of 2M = 8192 points
+ * and the layer's kernel spectrum for M <= 1024.  A kernel whose wait gave up
+ * issues no further copies, reads the data from global memory instead, waits
+ * for the copy in flight once more (default limit) before it exits, and
+ * writes its output as zeros.  Library-wide and read at launch time; meant
+ * for tests of that path, not for concurrent use.  Returns S4_OK. */
+s4_status s4_set_wait_limit(int polls);
 
 /* Measurement aid, outside the method: an FP32 issue-rate probe.  Launches
  * `blocks` CTAs of 256 threads on `stream`; every thread runs `iters`

@@ -40,7 +40,7 @@ ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
     "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd", "s4_conv_fwd_real",
-    "s4_hippo_dplr", "s4_fp32_probe",
+    "s4_hippo_dplr", "s4_fp32_probe", "s4_set_wait_limit",
 ]
 
 HIPPO_KINDS = {"legs": 0, "legt": 1, "lagt": 2}
@@ -94,6 +94,8 @@ def load(path: str | None = None):
     lib.s4_hippo_dplr.restype = i32
     lib.s4_fp32_probe.argtypes = [vp, i32, i32, vp]
     lib.s4_fp32_probe.restype = i32
+    lib.s4_set_wait_limit.argtypes = [i32]
+    lib.s4_set_wait_limit.restype = i32
     _lib = lib
     return lib
 
@@ -310,6 +312,12 @@ def s4_fp32_probe(out, blocks: int, iters: int, stream=None) -> int:
     _check(load().s4_fp32_probe(ctypes.c_void_p(out.data_ptr()), int(blocks), int(iters), _stream(stream)),
            "s4_fp32_probe")
     return blocks * 256 * ((int(iters) + 7) // 8 * 8) * 16
+
+
+def s4_set_wait_limit(polls: int) -> None:
+    """Polls a kernel's bounded wait on an asynchronous copy makes before it
+    reports S4_ERR_TIMEOUT (negative: the default).  A test hook."""
+    _check(load().s4_set_wait_limit(int(polls)), "s4_set_wait_limit")
 
 
 def s4_get_status(ws, stream=None) -> int:

@@ -257,7 +257,7 @@ __host__ __device__ constexpr int kspec_min_blocks(int threads) {
 template <int LOGM>
 __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(RowCfg<LOGM + 1>::THREADS)) kspec_kernel(
     const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
-    float scale, St status) {
+    float scale, St status, int wait_limit) {
   using C = RowCfg<LOGM + 1>;
   constexpr int M = 1 << LOGM, n = C::n, T = C::T;
   constexpr bool STW = kspec_stage_tw(LOGM);
@@ -292,11 +292,11 @@ __global__ void __launch_bounds__(RowCfg<LOGM + 1>::THREADS, kspec_min_blocks(Ro
     const bool act = h < H;
     kspec_row<LOGM, STW>(Khat + (size_t)(act ? h : 0) * M, K + (size_t)(act ? h : 0) * L,
                          K2 + (size_t)(act ? h : 0) * n, L, scale, zero || stall, act, buf, lt, fin, twi,
-                         twf, &twbar, &stall);
+                         twf, &twbar, &stall, wait_limit);
   }
   if (!fin) st_flag(status, ST_NONFINITE);
   if constexpr (STW) {
-    if (stall) mbar_wait(&twbar, 0u);  // one more bounded wait for the copy in flight
+    if (stall) mbar_wait(&twbar, 0u);  // drain: one more wait, default limit, for the copy in flight
   }
   if (stall && threadIdx.x == 0) st_flag(status, ST_STALL);
 }
@@ -348,12 +348,17 @@ __device__ __forceinline__ int last_bfly(int sl, int lt) {
 // forward pass, used by the spectrum product) and the next pair's two input
 // rows (requested once the product has read K2, used by the next forward
 // pass 0), so neither global latency sits on the critical path.  Input rows
-// are staged only when L is a multiple of 4 (stage_u; 16-byte copies).
+// are staged only when L is a multiple of 4 (stage_u; 16-byte copies).  A
+// wait that gives up (after `wait_limit` polls) puts the CTA under the drain
+// rule of mbar_wait: the vote at the next barrier makes `stall` the same in
+// every thread, no copy is issued after it, staged data is read from global
+// memory instead, and the round in flight is waited for once more at the end.
+// The outputs are then zeros and the status is S4_ERR_TIMEOUT.
 template <int LOGN, bool STAGE>
 __global__ void __launch_bounds__(RowCfg<LOGN, true>::THREADS, conv_min_blocks(LOGN, RowCfg<LOGN, true>::THREADS))
 conv_pair_kernel(
     const float* __restrict__ u, const float2* __restrict__ K2, const float* __restrict__ D,
-    float2* __restrict__ y, int batch, int H, int L, St status, int stage_u) {
+    float2* __restrict__ y, int batch, int H, int L, St status, int stage_u, int wait_limit) {
   using C = RowCfg<LOGN, true>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
@@ -377,7 +382,8 @@ conv_pair_kernel(
   const float* stage_f = reinterpret_cast<const float*>(stage);
   __shared__ unsigned long long bar;
   unsigned ph = 0u;
-  bool stall = false;
+  unsigned last_ph = 0u;  // parity of the latest wait: the round in flight after a stall
+  bool stall = false;     // (STAGE) a wait gave up in this CTA; the same in every thread after a vote
   // one thread: announce and copy the two input rows of pair q into the stage
   auto issue_u = [&](int q) {
     const int hq = q % H, bq = 2 * (q / H);
@@ -411,11 +417,14 @@ conv_pair_kernel(
     const size_t row0 = (size_t)b0 * H + h, row1 = row0 + H;
     const float dk = act ? D[h] * (0.5f / n) : 0.f;
     const float2* K2h = K2 + (size_t)h * n;
-    const bool from_stage = STAGE && stage_u;
+    const bool from_stage = STAGE && stage_u && !stall;
+    bool got_u = true;
     if (from_stage) {  // this pair's input rows
-      stall |= !mbar_wait(&bar, ph);
+      got_u = mbar_wait(&bar, ph, wait_limit);
+      last_ph = ph;
       ph ^= 1u;
     }
+    const bool u_staged = from_stage && got_u;
     // forward pass 0: z = u_b + i u_{b+1}, zero-padded, global (or stage) -> shared
 #pragma unroll
     for (int s = 0; s < PER0; ++s) {
@@ -424,7 +433,7 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
-        if (from_stage)
+        if (u_staged)
           a[q] = make_float2(t < L ? stage_f[t] : 0.f, (has1 && t < L) ? stage_f[n + t] : 0.f);
         else
           a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
@@ -433,14 +442,18 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA; ++q) bufA[IXF0::wr(i, q)] = a[q];
     }
-    __syncthreads();
-    if (STAGE && waited && threadIdx.x == 0) issue_k2(K2h);  // the stage's inputs are consumed
+    if constexpr (STAGE) {
+      stall = __syncthreads_or(stall || !got_u);
+    } else {
+      __syncthreads();
+    }
+    if (STAGE && waited && !stall && threadIdx.x == 0) issue_k2(K2h);  // the stage's inputs are consumed
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(buf1, lt);
     if (!waited) {  // the forward transform of u needed nothing from the previous kernel
       pdl_wait();
       zero = st_bad(status);
       waited = true;
-      if (STAGE && threadIdx.x == 0) issue_k2(K2h);  // K2 comes from the previous kernel
+      if (STAGE && !stall && threadIdx.x == 0) issue_k2(K2h);  // K2 comes from the previous kernel
     }
     // forward last pass: Z in natural order, bin i + q NBL of butterfly i
     float2 z[PERL][RB];
@@ -458,11 +471,15 @@ conv_pair_kernel(
     // in registers; row b+1 goes to bufB at once (unused since the last
     // iteration), row b to bufA after every thread has read its last pass.
     float2 (&a0)[PERL][RB] = z;  // row b's products replace Z in place
-    if constexpr (STAGE) {  // the channel's K2 row
-      stall |= !mbar_wait(&bar, ph);
+    bool got_k = true;
+    const bool k_wait = STAGE && !stall;
+    if (k_wait) {  // the channel's K2 row
+      got_k = mbar_wait(&bar, ph, wait_limit);
+      last_ph = ph;
       ph ^= 1u;
     }
-    const float2* Kr = STAGE ? stage : K2h;
+    const bool k_staged = k_wait && got_k;
+    const float2* Kr = stage;
     if constexpr (MIRROR) {
 #pragma unroll
       for (int s = 0; s < PERL / 2; ++s) {
@@ -470,8 +487,8 @@ conv_pair_kernel(
         float2 kA[RB], kB[RB], a1A[RB], a1B[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          kA[q] = STAGE ? Kr[iA + q * NBL] : __ldcg(K2h + iA + q * NBL);
-          kB[q] = STAGE ? Kr[iB + q * NBL] : __ldcg(K2h + iB + q * NBL);
+          kA[q] = k_staged ? Kr[iA + q * NBL] : __ldcg(K2h + iA + q * NBL);
+          kB[q] = k_staged ? Kr[iB + q * NBL] : __ldcg(K2h + iB + q * NBL);
           kA[q].x += dk;
           kB[q].x += dk;
         }
@@ -513,8 +530,12 @@ conv_pair_kernel(
         dft<RB, true>(zA);
         dft<RB, true>(zB);
       }
-      __syncthreads();
-      if (STAGE && stage_u && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
+      if constexpr (STAGE) {
+        stall = __syncthreads_or(stall || !got_k);
+      } else {
+        __syncthreads();
+      }
+      if (STAGE && stage_u && !stall && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
     } else {
       // one butterfly per thread: the mirror bins sit in another thread
 #pragma unroll
@@ -531,15 +552,19 @@ conv_pair_kernel(
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           const int k = i + q * NBL;
-          float2 kv = STAGE ? Kr[k] : __ldcg(K2h + k);
+          float2 kv = k_staged ? Kr[k] : __ldcg(K2h + k);
           kv.x += dk;
           split_mul(z[sl][q], bufB[pad((n - k) & (n - 1))], kv, a0[sl][q], a1[sl][q]);
         }
         dft<RB, true>(a0[sl]);
         dft<RB, true>(a1[sl]);
       }
-      __syncthreads();
-      if (STAGE && stage_u && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
+      if constexpr (STAGE) {
+        stall = __syncthreads_or(stall || !got_k);
+      } else {
+        __syncthreads();
+      }
+      if (STAGE && stage_u && !stall && threadIdx.x == 0 && p0 + (int)gridDim.x < pairs) issue_u(p0 + gridDim.x);
 #pragma unroll
       for (int sl = 0; sl < PERL; ++sl) {
         const int i = last_bfly<T, NBL, PERL>(sl, lt);
@@ -581,6 +606,9 @@ conv_pair_kernel(
       }
     }
     __syncthreads();
+  }
+  if constexpr (STAGE) {
+    if (stall) mbar_wait(&bar, last_ph);  // drain: the round in flight, default limit
   }
   if (stall && threadIdx.x == 0) st_flag(status, ST_STALL);
 }
@@ -831,7 +859,7 @@ static cudaError_t conv_launch(const float* u, const float2* K2, const float* D,
     const int grid = grid_for(k, C::THREADS, smem, (pairs + C::ROWS - 1) / C::ROWS);
     TimedLaunch tl("conv", s);
     return launch_maybe_pdl(k, grid, C::THREADS, smem, s, pdl, u, K2, D, y, batch, H, L,
-                            st, (L % 4 == 0) ? 1 : 0);
+                            st, (L % 4 == 0) ? 1 : 0, wait_limit());
   }
   return cudaGetLastError();
 }
@@ -849,7 +877,7 @@ static cudaError_t kspec_launch(const float2* Khat, float2* K, float2* K2, int H
   if (e != cudaSuccess) return e;
   const int grid = grid_for(k, C::THREADS, smem, (H + C::ROWS - 1) / C::ROWS);
   TimedLaunch tl("kspec", s);
-  return launch_maybe_pdl(k, grid, C::THREADS, smem, s, true, Khat, K, K2, H, L, scale, st);
+  return launch_maybe_pdl(k, grid, C::THREADS, smem, s, true, Khat, K, K2, H, L, scale, st, wait_limit());
 }
 
 bool kspec_supported(int logM) { return logM >= 5 && logM <= 12; }

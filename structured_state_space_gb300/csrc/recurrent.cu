@@ -23,34 +23,24 @@
 // channel for C~): G = 16 for N <= 64 in the recurrent mode (two sequences per
 // warp, so each reduction takes four shuffle rounds for both), otherwise 32;
 // lane l of a group holds states j = l, l + G, ...  W^{-1} is formed once per
-// group.  An exactly zero d_j (the bordered branch of the pages' solver) or an
-// exactly singular W is reported as S4_ERR_SINGULAR_BILINEAR and the outputs
-// are zeros; this kernel does not take the bordered branch.
+// group.  An exactly singular W is reported as S4_ERR_SINGULAR_BILINEAR and the
+// outputs are zeros.
+//
+// The pages' solver has a second branch: when some d_j is exactly zero (the set
+// Z, s = |Z| <= r) the correction is replaced by the bordered system of size
+// r + s over (Q^* x, x_Z).  A channel with such a d_j (and a valid step) is
+// left alone by the two kernels above and taken by recurrent_bordered_kernel /
+// ctilde_bordered_kernel, one warp per sequence, a plain step at a time (the
+// branch is rare: it needs 1 - (Delta/2) lambda_j to round to exactly zero).
+// Both partitions use the same fp32 test of d_j, so every sequence is written
+// by exactly one kernel.
 #include <float.h>
 
 #include "s4_dev.cuh"
 #include "s4_internal.h"
+#include "s4_solve.cuh"
 
 namespace s4dev {
-
-__device__ __forceinline__ float2 cconj(float2 a) { return make_float2(a.x, -a.y); }
-
-__device__ __forceinline__ float2 cdiv_safe(float2 a, float2 b) {  // a / b, b != 0
-  const float s = __fdiv_rn(1.f, fmaf(b.x, b.x, b.y * b.y));
-  return make_float2((a.x * b.x + a.y * b.y) * s, (a.y * b.x - a.x * b.y) * s);
-}
-
-// Sum over the G lanes of a group (G = 16 or 32; every lane of the warp
-// takes part, offsets below G stay inside the group).
-template <int G = 32>
-__device__ __forceinline__ float2 warp_sum(float2 v) {
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) {
-    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-  }
-  return v;
-}
 
 // Sums over a 16-lane group of two complex values at once by recursive
 // halving: a (returned to every lane) and b (returned to lane 8 of the group,
@@ -104,57 +94,13 @@ __device__ __forceinline__ void group_sum_all(float (&v)[NF]) {
   for (int j = 0; j < NF; ++j) v[j] = __shfl_sync(0xffffffffu, w[0], j * (G / NF), G);
 }
 
-// Invert an r x r complex matrix in place (Gauss-Jordan, partial pivoting).
-// Returns false on an exactly zero pivot.
-template <int R>
-__device__ bool invert_small(float2 (&A)[R][R]) {
-  float2 I[R][R];
-#pragma unroll
-  for (int i = 0; i < R; ++i)
-#pragma unroll
-    for (int j = 0; j < R; ++j) I[i][j] = make_float2(i == j ? 1.f : 0.f, 0.f);
-#pragma unroll
-  for (int c = 0; c < R; ++c) {
-    int piv = c;
-    float best = fmaxf(fabsf(A[c][c].x), fabsf(A[c][c].y));
-#pragma unroll
-    for (int i = c + 1; i < R; ++i) {
-      const float m = fmaxf(fabsf(A[i][c].x), fabsf(A[i][c].y));
-      if (m > best) { best = m; piv = i; }
-    }
-    if (!(best > 0.f)) return false;
-#pragma unroll
-    for (int i = c + 1; i < R; ++i)
-      if (i == piv)
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          float2 t = A[c][j]; A[c][j] = A[i][j]; A[i][j] = t;
-          t = I[c][j]; I[c][j] = I[i][j]; I[i][j] = t;
-        }
-    const float2 inv = cdiv_safe(make_float2(1.f, 0.f), A[c][c]);
-#pragma unroll
-    for (int j = 0; j < R; ++j) { A[c][j] = cmul(A[c][j], inv); I[c][j] = cmul(I[c][j], inv); }
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      if (i == c) continue;
-      const float2 f = A[i][c];
-#pragma unroll
-      for (int j = 0; j < R; ++j) { A[i][j] = csub(A[i][j], cmul(f, A[c][j])); I[i][j] = csub(I[i][j], cmul(f, I[c][j])); }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < R; ++i)
-#pragma unroll
-    for (int j = 0; j < R; ++j) A[i][j] = I[i][j];
-  return true;
-}
-
 // Per-warp channel constants: dinv_j = 1/d_j, and W^{-1} (conjugate-transposed for C~).
 template <int RANK, int E>
 struct ChanConst {
   float2 dinv[E];
   float2 Winv[RANK][RANK];
   bool ok;
+  bool zero_d;  // some d_j of the channel is exactly zero (the bordered branch)
 };
 
 template <int RANK, int E, int G = 32>
@@ -172,7 +118,7 @@ __device__ void channel_constants(const float2* __restrict__ lam, const float2* 
     const int j = lane + G * e;
     cc.dinv[e] = make_float2(0.f, 0.f);
     if (j < N) {
-      const float2 d = make_float2(fmaf(-alpha, lam[j].x, 1.f), -alpha * lam[j].y);
+      const float2 d = dpl_diag(lam[j], alpha);
       if (d.x == 0.f && d.y == 0.f) {
         zero_d = true;
         continue;
@@ -198,6 +144,7 @@ __device__ void channel_constants(const float2* __restrict__ lam, const float2* 
 #pragma unroll
   for (int o = G / 2; o > 0; o >>= 1) zd |= __shfl_xor_sync(0xffffffffu, zd, o);
   zero_d = zd != 0;
+  cc.zero_d = zero_d;
   cc.ok = !zero_d && invert_small<RANK>(cc.Winv);
 }
 
@@ -230,6 +177,9 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
   ChanConst<RANK, E> cc;
   channel_constants<RANK, E, G>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
   const bool ok = cc.ok && !bad;
+  // a channel with an exactly zero d_j (and a valid step) belongs to
+  // recurrent_bordered_kernel: run along for the shuffles, store nothing
+  const bool mine = valid && !(cc.zero_d && !bad);
   // With w = D^{-1}(2 x + Delta B u) substituted, one step is
   //   s = sum_j h_j x_j + c0 u,  h_j = 2 conj(Q_j) / d_j,  c0 = sum_j conj(Q_j) Delta B_j / d_j,
   //   z = W^{-1} s,  x'_j = a_j x_j + e_j u - pd_j z,  a_j = 2/d_j - 1, e_j = Delta B_j / d_j,
@@ -305,14 +255,14 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     } else {
       yp = warp_sum<G>(yp);
     }
-    if (valid && lane == ylane) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
+    if (mine && lane == ylane) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
-    if (valid && j < N) x[(size_t)warp * N + j] = ok ? xs[e] : make_float2(0.f, 0.f);
+    if (mine && j < N) x[(size_t)warp * N + j] = ok ? xs[e] : make_float2(0.f, 0.f);
   }
-  if (valid && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+  if (mine && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
 
 // C~ = C - (Abar^*)^M C with Abar^* w = 2 G^{-*} w - w.
@@ -346,6 +296,8 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
   ChanConst<RANK, E> cc;
   channel_constants<RANK, E, G>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, cc);
   const bool ok = cc.ok && !bad;
+  // an exactly zero d_j (with a valid step): ctilde_bordered_kernel's channel
+  const bool mine = valid && !(cc.zero_d && !bad);
   // factors of Abar^*: columns 0..RANK-1 of U, V
   float2 av[E], w[E], c0[E], Uf[E][KP], Vf[E][KP];
 #pragma unroll
@@ -453,9 +405,9 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
-    if (valid && j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
+    if (mine && j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
   }
-  if (valid && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
+  if (mine && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
 
 }  // namespace s4dev
@@ -528,27 +480,44 @@ static cudaError_t ct_dispatch(const float2* Lam, const float2* P, const float2*
   return ct_launch_p<RANK, 8>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
 }
 
+template <int RANK>
+static cudaError_t rec_both(const float2* Lam, const float2* P, const float2* Q, const float2* B,
+                            const float2* C, const float* dt, const float* D, const float* u,
+                            int batch, int H, int N, int L, float2* x, float2* y, St st, cudaStream_t s) {
+  const cudaError_t e = rec_dispatch<RANK>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+  if (e != cudaSuccess) return e;
+  return launch_recurrent_bordered(RANK, Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+}
+
 cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q, const float2* B,
                              const float2* C, const float* dt, const float* D, const float* u,
                              int batch, int H, int N, int r, int L, float2* x, float2* y,
                              St st, cudaStream_t s) {
   switch (r) {
-    case 1: return rec_dispatch<1>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
-    case 2: return rec_dispatch<2>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
-    case 3: return rec_dispatch<3>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
-    case 4: return rec_dispatch<4>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+    case 1: return rec_both<1>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+    case 2: return rec_both<2>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+    case 3: return rec_both<3>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
+    case 4: return rec_both<4>(Lam, P, Q, B, C, dt, D, u, batch, H, N, L, x, y, st, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int RANK>
+static cudaError_t ct_both(const float2* Lam, const float2* P, const float2* Q, const float* dt,
+                           const float2* C, int H, int N, int M, float2* Ct, St st, cudaStream_t s) {
+  const cudaError_t e = ct_dispatch<RANK>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+  if (e != cudaSuccess) return e;
+  return launch_ctilde_bordered(RANK, Lam, P, Q, dt, C, H, N, M, Ct, st, s);
 }
 
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                           const float2* C, int H, int N, int r, int M, float2* Ct, St st,
                           cudaStream_t s) {
   switch (r) {
-    case 1: return ct_dispatch<1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-    case 2: return ct_dispatch<2>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-    case 3: return ct_dispatch<3>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
-    case 4: return ct_dispatch<4>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 1: return ct_both<1>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 2: return ct_both<2>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 3: return ct_both<3>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
+    case 4: return ct_both<4>(Lam, P, Q, dt, C, H, N, M, Ct, st, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -160,6 +160,12 @@ size_t g_used = 0;
 
 namespace s4impl {
 
+namespace {
+std::atomic<int> g_wait_limit{s4dev::kMbarWaitLimit};
+}  // namespace
+
+int wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -235,6 +241,11 @@ s4_status s4_fp32_probe(float* out, int blocks, int iters, void* stream) {
   if (!out || blocks < 1 || iters < 1) return S4_ERR_INVALID_ARG;
   s4impl::fp32_probe_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(out, (iters + 7) / 8);
   return cudaGetLastError() == cudaSuccess ? S4_OK : S4_ERR_CUDA;
+}
+
+s4_status s4_set_wait_limit(int polls) {
+  s4impl::g_wait_limit.store(polls >= 0 ? polls : s4dev::kMbarWaitLimit, std::memory_order_relaxed);
+  return S4_OK;
 }
 
 size_t s4_workspace_bytes(int H, int N, int r, int L, int batch) {

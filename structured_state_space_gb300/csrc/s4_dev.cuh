@@ -94,7 +94,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 // One thread announces the bytes of a round (mbar_expect_tx) and issues the
 // copies (bulk_g2s: 16-byte aligned addresses, sizes a multiple of 16); every
 // thread then waits for the round's phase.  The wait is bounded: it reports
-// false after kMbarWaitLimit polls instead of spinning forever.
+// false after `limit` polls (kMbarWaitLimit unless the library's wait limit
+// was changed, see s4_set_wait_limit) instead of spinning forever.
+//
+// Drain rule for a kernel whose wait gave up: the copy round it waited for
+// may still be writing into shared memory.  The CTA then issues no further
+// copies, reads what it would have staged straight from global memory, and
+// before it exits waits once more, with the default limit, for that round.
 constexpr int kMbarWaitLimit = 1 << 22;
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return (unsigned)__cvta_generic_to_shared(p);
@@ -119,8 +125,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
-  for (int it = 0; it < kMbarWaitLimit; ++it) {
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, int limit = kMbarWaitLimit) {
+  for (int it = 0; it < limit; ++it) {
     unsigned done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"

@@ -18,6 +18,10 @@ struct St {
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
+// Polls a kernel's bounded wait on an asynchronous copy makes before it gives
+// up (library-wide; s4_set_wait_limit changes it, for tests of that path).
+int wait_limit();
+
 // Optional event bracketing of kernel launches (see s4_timing_* in s4.h).
 // Construct right before a launch and let it go out of scope right after.
 class TimedLaunch {
@@ -96,6 +100,16 @@ cudaError_t launch_recurrent(const float2* Lam, const float2* P, const float2* Q
                              const float2* C, const float* dt, const float* D, const float* u,
                              int batch, int H, int N, int r, int L, float2* x, float2* y,
                              St st, cudaStream_t s);
+// The bordered branch (channels with an exactly zero d_j = 1 - (Delta/2) lambda_j):
+// launched after launch_recurrent's / launch_ctilde's own kernel, which leave
+// those channels to it; one warp per sequence, N <= 256.
+cudaError_t launch_recurrent_bordered(int r, const float2* Lam, const float2* P, const float2* Q,
+                                      const float2* B, const float2* C, const float* dt, const float* D,
+                                      const float* u, int batch, int H, int N, int L, float2* x, float2* y,
+                                      St st, cudaStream_t s);
+cudaError_t launch_ctilde_bordered(int r, const float2* Lam, const float2* P, const float2* Q,
+                                   const float* dt, const float2* C, int H, int N, int M, float2* Ct,
+                                   St st, cudaStream_t s);
 // C~ = (I - Abar^M)^* C, one warp per channel; N <= 256.
 cudaError_t launch_ctilde(const float2* Lam, const float2* P, const float2* Q, const float* dt,
                           const float2* C, int H, int N, int r, int M, float2* Ct, St st,

@@ -47,7 +47,8 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
                                           float2* __restrict__ K2row, int L, float scale, bool zero,
                                           bool act, float2* buf, int lt, bool& fin,
                                           const float2* twi = nullptr, const float2* twf = nullptr,
-                                          unsigned long long* twbar = nullptr, bool* stall = nullptr) {
+                                          unsigned long long* twbar = nullptr, bool* stall = nullptr,
+                                          int wait_limit = kMbarWaitLimit) {
   using KC = KspecCfg<LOGM>;
   constexpr int LOGN = KC::LOGN, M = KC::M, n = KC::n, T = KC::T, TI = KC::TI;
   static_assert(TI <= T, "thread split");
@@ -80,7 +81,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
   }
   __syncthreads();
   if constexpr (STW) {
-    if (!mbar_wait(twbar, 0u)) {  // tables missing: the row is written as zeros
+    if (!mbar_wait(twbar, 0u, wait_limit)) {  // tables missing: the row is written as zeros
       *stall = true;
       zero = true;
     }

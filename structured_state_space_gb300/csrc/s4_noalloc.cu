@@ -10,8 +10,9 @@
 // compiled into the library.  That array exists on every device that loads
 // the library and stays there until the process exits.
 //
-// The same launch sequence as s4_conv_fwd runs (spectrum, then fused
-// convolution); only the scratch pointer differs.
+// The same kernels as s4_conv_fwd run (spectrum, then fused convolution),
+// after a memset of the status word and without programmatic dependent launch,
+// so the convolution does not overlap the spectrum kernel as it does there.
 #include <stdint.h>
 
 #include <mutex>

@@ -110,17 +110,118 @@ def test_recurrent_equals_convolution_path():
     assert rel_l2(y_conv.cpu().numpy(), y_rec.cpu().numpy()) <= 2 * REL
 
 
-def test_singular_bilinear_status():
-    # lambda_0 = 2/Delta with Delta = 1/4: d_0 = 1 - (Delta/2) lambda_0 = 0 exactly.
-    c = lambda v: torch.tensor(v, dtype=torch.complex64, device="cuda")
+def _bordered_params(N, r, zero_sets, seed, indep=False, dt=0.25):
+    """One channel per entry of `zero_sets`: the states listed there get
+    lambda_j = 2/Delta, so d_j = 1 - (Delta/2) lambda_j is exactly zero in fp32
+    and in float64 (the bordered branch of the pages' recurrent solver); P_j is
+    large there so that A = Lambda - P Q^* stays stable.  An empty set is a
+    channel of the ordinary (Woodbury) branch."""
+    H = len(zero_sets)
+    rng = np.random.default_rng(seed)
+    lam = np.tile(-0.5 + 1j * np.pi * np.arange(N), (H, 1))
+    P = (rng.standard_normal((H, N, r)) + 1j * rng.standard_normal((H, N, r))) * 0.1
+    for h, zs in enumerate(zero_sets):
+        for i, j in enumerate(zs):
+            lam[h, j] = 2.0 / dt
+            P[h, j, i % r] = 4.0
+    Q = P.copy()
+    if indep:
+        Q = Q + (rng.standard_normal(P.shape) + 1j * rng.standard_normal(P.shape)) * 0.05
+    cn = lambda shape: (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)) / np.sqrt(2.0)
+    return {"Lambda": lam.astype(np.complex64), "P": P.astype(np.complex64), "Q": Q.astype(np.complex64),
+            "B": cn((H, N)).astype(np.complex64), "C": cn((H, N)).astype(np.complex64),
+            "dt": np.full(H, dt, np.float32), "D": rng.standard_normal(H).astype(np.float32)}
+
+
+# (N, r, zero states per channel, batch, L, Q independent of P): s = |Z| from 1
+# to r; channels of both branches in one call (two sequences per warp in the
+# recurrent kernel for N <= 64, where one may be the bordered kernel's)
+BORDERED_CASES = [
+    (4, 1, [[0], [], [2]], 2, 64, False),
+    (40, 1, [[3], []], 3, 100, True),
+    (80, 2, [[5, 70], [], [1]], 2, 50, False),
+    (33, 3, [[0, 1, 32]], 1, 40, False),
+    (16, 4, [[2], [0, 15]], 1, 30, True),
+]
+
+
+@pytest.mark.parametrize("N,r,zero_sets,batch,L,indep", BORDERED_CASES)
+def test_recurrent_bordered_branch_matches_oracle(N, r, zero_sets, batch, L, indep):
+    p = _bordered_params(N, r, zero_sets, seed=N + 10 * r, indep=indep)
+    H = len(zero_sets)
+    u = np.random.default_rng(N * L).standard_normal((batch, H, L)).astype(np.float32)
+    d = _dev(p, ["Lambda", "P", "Q", "B", "C", "dt", "D"])
+    ut = torch.from_numpy(u).cuda()
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    lam = c([[8.0, -0.5 + 1j]])
-    P = c([[[0.1], [0.2]]])
-    dt = torch.tensor([0.25], device="cuda")
-    u = torch.ones((1, 1, 4), device="cuda")
-    y, x = s4.s4_recurrent_fwd(lam, P, P, c([[1.0, 1.0]]), c([[1.0, 1.0]]), dt, torch.zeros(1, device="cuda"), u, ws=ws)
-    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
-    assert torch.count_nonzero(y).item() == 0 and torch.count_nonzero(x).item() == 0
-    Ct = s4.s4_ctilde(lam, P, P, dt, c([[1.0, 1.0]]), 4, ws=ws)
-    assert s4.s4_get_status(ws) == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
-    assert torch.count_nonzero(Ct).item() == 0
+    cut = L // 3  # the state carries over from the first call into the second
+    x = torch.zeros((batch, H, N), dtype=torch.complex64, device="cuda")
+    y1, x = s4.s4_recurrent_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["C"], d["dt"], d["D"],
+                                ut[:, :, :cut].contiguous(), x=x, ws=ws)
+    y2, x = s4.s4_recurrent_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["C"], d["dt"], d["D"],
+                                ut[:, :, cut:].contiguous(), x=x, ws=ws)
+    assert s4.s4_get_status(ws) == 0
+    y = torch.cat([y1, y2], dim=2).cpu().numpy()
+    ref = np.empty((batch, H, L), complex)
+    for h in range(H):
+        # the oracle's own solver takes the bordered branch on this channel
+        dd = 1.0 - (p["dt"][h] / 2.0) * p["Lambda"][h].astype(np.complex128)
+        assert (np.count_nonzero(dd == 0) > 0) == (len(zero_sets[h]) > 0)
+        _, Ab, Bb = O.bilinear(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["dt"][h])
+        for b in range(batch):
+            ref[b, h] = O.recurrence(Ab, Bb, p["C"][h], p["D"][h], u[b, h])
+    assert rel_l2(y, ref) <= REL, rel_l2(y, ref)
+
+
+@pytest.mark.parametrize("N,r,zero_sets,batch,L,indep", BORDERED_CASES)
+def test_ctilde_bordered_branch_matches_oracle(N, r, zero_sets, batch, L, indep):
+    p = _bordered_params(N, r, zero_sets, seed=N + 10 * r, indep=indep)
+    H = len(zero_sets)
+    d = _dev(p, ["Lambda", "P", "Q", "dt", "C"])
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    Ct = s4.s4_ctilde(d["Lambda"], d["P"], d["Q"], d["dt"], d["C"], L, ws=ws).cpu().numpy()
+    assert s4.s4_get_status(ws) == 0
+    M = O.transform_length(L)
+    ref = np.array([O.ctilde_from_c(O.bilinear(p["Lambda"][h], p["P"][h], p["Q"][h], p["B"][h], p["dt"][h])[1],
+                                    p["C"][h], M) for h in range(H)])
+    assert rel_l2(Ct, ref) <= REL, rel_l2(Ct, ref)
+
+
+def _status_case(p, L=4):
+    d = _dev(p, ["Lambda", "P", "Q", "B", "C", "dt", "D"])
+    H, N = p["Lambda"].shape
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    u = torch.ones((1, H, L), device="cuda")
+    y, x = s4.s4_recurrent_fwd(d["Lambda"], d["P"], d["Q"], d["B"], d["C"], d["dt"], d["D"], u, ws=ws)
+    st_rec = s4.s4_get_status(ws)
+    Ct = s4.s4_ctilde(d["Lambda"], d["P"], d["Q"], d["dt"], d["C"], L, ws=ws)
+    st_ct = s4.s4_get_status(ws)
+    return st_rec, st_ct, y.cpu().numpy(), x.cpu().numpy(), Ct.cpu().numpy(), u.cpu().numpy()
+
+
+def test_singular_bilinear_when_more_zero_diagonals_than_rank():
+    # s = 2 zero d_j at rank r = 1: the bordered system cannot be formed
+    # (singular-bilinear-matrix; the oracle raises the same status).  The
+    # second channel is ordinary and keeps its result.
+    p = _bordered_params(4, 1, [[0, 1], []], seed=21)
+    with pytest.raises(O.OracleStatus):
+        O.recurrent_solve_dplr(p["Lambda"][0], p["P"][0], p["Q"][0], p["dt"][0], np.ones(4))
+    st_rec, st_ct, y, x, Ct, u = _status_case(p)
+    assert st_rec == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
+    assert st_ct == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
+    assert not y[:, 0].any() and not x[:, 0].any() and not Ct[0].any()
+    _, Ab, Bb = O.bilinear(p["Lambda"][1], p["P"][1], p["Q"][1], p["B"][1], p["dt"][1])
+    assert rel_l2(y[0, 1], O.recurrence(Ab, Bb, p["C"][1], p["D"][1], u[0, 1])) <= REL
+
+
+def test_singular_bilinear_when_bordered_matrix_is_singular():
+    # s = 1 <= r = 1 but P_Z = 0: the bordered matrix [[W_J, -Q_Z^*], [alpha P_Z, 0]]
+    # (and G itself, whose row for the zero state vanishes) is singular.
+    p = _bordered_params(4, 1, [[0]], seed=22)
+    p["P"][0, 0, 0] = 0.0
+    p["Q"] = p["P"].copy()
+    with pytest.raises(O.OracleStatus):
+        O.recurrent_solve_dplr(p["Lambda"][0], p["P"][0], p["Q"][0], p["dt"][0], np.ones(4))
+    st_rec, st_ct, y, x, Ct, _ = _status_case(p)
+    assert st_rec == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
+    assert st_ct == s4.STATUS_CODE["S4_ERR_SINGULAR_BILINEAR"]
+    assert not y.any() and not x.any() and not Ct.any()

@@ -75,6 +75,52 @@ def test_two_calls_match_the_workspace_entry_point(lib):
     assert torch.isfinite(torch.view_as_real(y2)).all()
 
 
+@pytest.mark.parametrize("batch,H,L", [
+    (3, 64, 4096),    # rows of 8192 points: inputs and kernel spectrum staged by bulk copies
+    (2, 5, 3001),     # 8192 points, L not a multiple of 4: inputs read directly
+    (2, 16, 16384),   # 32768 points: a cluster of CTAs per pair of rows
+])
+def test_other_row_paths_match_the_workspace_entry_point(lib, batch, H, L):
+    # each fits the fixed scratch (256 + 16 H M bytes <= 8 MiB); two calls in a
+    # row, the second on the same inputs, must both match s4_conv_fwd
+    u, K, D = _inputs(batch, H, L, seed=L + H)
+    ref = s4.s4_conv_fwd(u, K, D)
+    for _ in range(2):
+        rc, y = _noalloc(lib, u, K, D)
+        assert rc == 0, s4.s4_status_str(rc)
+        assert _rel(y, ref) <= 1e-4
+
+
+def test_longest_rows_match_the_oracle(lib):
+    # L = 40000: M = 65536, rows of 131072 points over 8-CTA clusters (2 MiB of
+    # scratch for H = 2); sampled outputs against the direct causal sums
+    import oracle.s4_oracle as O
+    u, K, D = _inputs(1, 2, 40000, seed=5)
+    rc, y = _noalloc(lib, u, K, D)
+    assert rc == 0, s4.s4_status_str(rc)
+    un, Kn, Dn, yn = u.cpu().numpy(), K.cpu().numpy(), D.cpu().numpy(), y.cpu().numpy()
+    ts = [0, 1, 2, 999, 20000, 39998, 39999]
+    for h in range(2):
+        ref = O.causal_conv_at(Kn[h], un[0, h], Dn[h], ts)
+        got = yn[0, h, ts]
+        assert np.linalg.norm(got - ref) <= 1e-4 * np.linalg.norm(ref)
+    assert _rel(y, s4.s4_conv_fwd(u, K, D)) <= 1e-4
+
+
+def test_nonfinite_kernel_gives_zeros(lib):
+    # a NaN in one channel's kernel makes a non-finite spectrum: with no status
+    # block to read, the caller's signal is an all-zero y (and rc 0)
+    u, K, D = _inputs(2, 4, 1024, seed=6)
+    K[2, 17] = complex(float("nan"), 0.0)
+    rc, y = _noalloc(lib, u, K, D)
+    assert rc == 0
+    assert torch.count_nonzero(y).item() == 0
+    # the next call, on a finite kernel, is clean again
+    u2, K2, D2 = _inputs(2, 4, 1024, seed=7)
+    rc, y2 = _noalloc(lib, u2, K2, D2)
+    assert rc == 0 and _rel(y2, s4.s4_conv_fwd(u2, K2, D2)) <= 1e-4
+
+
 def test_too_large_is_refused(lib):
     # 256 + 16 * H * M bytes must fit 8 MiB: H = 600, L = 1024 needs ~9.4 MiB
     u, K, D = _inputs(1, 600, 1024, seed=3)
