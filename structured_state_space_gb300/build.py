@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libs4.so")
-SOURCES = ["s4_api.cu", "cauchy.cu", "fft_rows.cu", "fft_cluster.cu", "s4_noalloc.cu", "recurrent.cu", "bordered.cu",
+SOURCES = ["s4_api.cu", "cauchy.cu", "fft_rows.cu", "fft_cluster.cu", "fft_fourstep.cu", "s4_noalloc.cu", "recurrent.cu", "bordered.cu",
            "hippo.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

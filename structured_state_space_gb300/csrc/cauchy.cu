@@ -98,22 +98,34 @@ __device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
 // the pair w and w (-Re lambda_j).  With d = s - lambda_j = -Re lambda_j + i dim,
 //   w / d = (w (-Re lambda_j) - i dim w) / |d|^2
 // costs two FMAs for the numerator and two for the accumulation.
-template <int RANK>
+//
+// PACKED: two roots per packed fp32x2 instruction (__ffma2_rn / __fadd2_rn, the
+// same per-lane rounding as the scalar form, so the sums are bit-identical).
+// A packed instruction does two lanes' work for one issue slot, which matters
+// because the scalar loop is issue-bound (about 24 issued instructions per
+// term for 19 FMA-pipe ones).  The pole data is then staged as duplicated
+// pairs -- {-Im lambda, -Im lambda}, {(Re lambda)^2, ...}, and per weight
+// {w.y, w.y}, {w.x a, w.x a}, {-w.x, -w.x}, {w.y a, w.y a} with a = -Re lambda --
+// so one 16-byte shared load gives two packed operands.
+template <int RANK, bool PACKED = false>
 struct CauchyLayout {
   static constexpr int NW = (RANK + 1) * (RANK + 1);      // weight vectors
-  static constexpr int PS = (2 + 4 * NW + 3) / 4 * 4;     // floats per pole (float4-padded)
+  static constexpr int PS = PACKED ? 4 * (1 + 2 * NW)     // floats per pole (float4-padded)
+                                   : (2 + 4 * NW + 3) / 4 * 4;
   static constexpr int JT = PS <= 48 ? 128 : 64;          // poles staged at a time
 };
 
 // (4 roots per thread: compiled for 4 CTAs per SM, the schedule measured fastest;
 // left to itself the compiler picks a tighter, slower one)
-template <int RANK, int RPT, int T>
+template <int RANK, int RPT, int T, bool PACKED = false>
 __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
     float2* __restrict__ Khat, int N, int logM, int logC, St status) {
-  using Lay = CauchyLayout<RANK>;
+  using Lay = CauchyLayout<RANK, PACKED>;
   constexpr int NW = Lay::NW, PS = Lay::PS, JT = Lay::JT;
+  static_assert(!PACKED || RPT % 2 == 0, "packed roots come in pairs");
+  constexpr int NPR = RPT / 2;  // (PACKED) root pairs per thread
   __shared__ __align__(16) float par[JT * PS];
   __shared__ float2 red[T / 32 + 1];
 
@@ -153,6 +165,20 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
 #pragma unroll
     for (int w = 0; w < NW; ++w) acc[rr][w] = make_float2(0.f, 0.f);
   float2 cb = make_float2(0.f, 0.f);
+  // (PACKED) the accumulators of root pair pr: ax = {acc[2pr][w].x, acc[2pr+1][w].x}, ay likewise
+  float2 ax[PACKED ? NPR : 1][NW], ay[PACKED ? NPR : 1][NW], sh2[PACKED ? NPR : 1], sl2[PACKED ? NPR : 1];
+  if constexpr (PACKED) {
+#pragma unroll
+    for (int pr = 0; pr < NPR; ++pr) {
+      sh2[pr] = make_float2(shi[2 * pr], shi[2 * pr + 1]);
+      sl2[pr] = make_float2(slo[2 * pr], slo[2 * pr + 1]);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        ax[pr][w] = make_float2(0.f, 0.f);
+        ay[pr][w] = make_float2(0.f, 0.f);
+      }
+    }
+  }
 
   for (int j0 = 0; j0 < N; j0 += JT) {
     const int jn = min(JT, N - j0);
@@ -161,14 +187,24 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
       const size_t j = (size_t)h * N + j0 + jj;
       const float2 lam = Lambda[j], b = Bv[j], c = Ct[j];
       float* pp = par + jj * PS;
-      pp[0] = lam.y;
-      pp[1] = lam.x * lam.x;
       const float nre = -lam.x;
+      if constexpr (PACKED) {
+        reinterpret_cast<float4*>(pp)[0] = make_float4(-lam.y, -lam.y, lam.x * lam.x, lam.x * lam.x);
+      } else {
+        pp[0] = lam.y;
+        pp[1] = lam.x * lam.x;
+      }
       auto put = [&](int widx, float2 w) {
-        pp[2 + 4 * widx] = w.x;
-        pp[3 + 4 * widx] = w.y;
-        pp[4 + 4 * widx] = w.x * nre;
-        pp[5 + 4 * widx] = w.y * nre;
+        if constexpr (PACKED) {
+          float4* p4 = reinterpret_cast<float4*>(pp) + 1 + 2 * widx;
+          p4[0] = make_float4(w.y, w.y, w.x * nre, w.x * nre);
+          p4[1] = make_float4(-w.x, -w.x, w.y * nre, w.y * nre);
+        } else {
+          pp[2 + 4 * widx] = w.x;
+          pp[3 + 4 * widx] = w.y;
+          pp[4 + 4 * widx] = w.x * nre;
+          pp[5 + 4 * widx] = w.y * nre;
+        }
       };
       float2 w = conj_mul(c, b);
       cb = cadd(cb, w);
@@ -182,10 +218,41 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
 #pragma unroll
         for (int l = 0; l < RANK; ++l) put(1 + 2 * RANK + i * RANK + l, conj_mul(qi, Pm[j * RANK + l]));
       }
+      if constexpr (!PACKED) {
 #pragma unroll
-      for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
+        for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
+      }
     }
     __syncthreads();
+    if constexpr (PACKED) {
+#pragma unroll kCauchyUnroll
+      for (int jj = 0; jj < jn; ++jj) {
+        const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
+        const float4 pl = p4[0];
+        const float2 nim = make_float2(pl.x, pl.y), re2 = make_float2(pl.z, pl.w);
+        float2 dim[NPR], rn[NPR];
+#pragma unroll
+        for (int pr = 0; pr < NPR; ++pr) {
+          dim[pr] = __fadd2_rn(__fadd2_rn(sh2[pr], nim), sl2[pr]);
+          const float2 n2 = __ffma2_rn(dim[pr], dim[pr], re2);
+          rn[pr] = make_float2(rcp_approx(n2.x), rcp_approx(n2.y));
+        }
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float4 b4 = p4[1 + 2 * w], c4 = p4[2 + 2 * w];
+          const float2 wy = make_float2(b4.x, b4.y), wax = make_float2(b4.z, b4.w);
+          const float2 nwx = make_float2(c4.x, c4.y), way = make_float2(c4.z, c4.w);
+#pragma unroll
+          for (int pr = 0; pr < NPR; ++pr) {
+            const float2 tx = __ffma2_rn(dim[pr], wy, wax);
+            const float2 ty = __ffma2_rn(dim[pr], nwx, way);
+            ax[pr][w] = __ffma2_rn(rn[pr], tx, ax[pr][w]);
+            ay[pr][w] = __ffma2_rn(rn[pr], ty, ay[pr][w]);
+          }
+        }
+      }
+      continue;
+    }
 #pragma unroll kCauchyUnroll
     for (int jj = 0; jj < jn; ++jj) {
       float pr[PS];
@@ -213,6 +280,16 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
         }
       }
     }
+  }
+
+  if constexpr (PACKED) {
+#pragma unroll
+    for (int pr = 0; pr < NPR; ++pr)
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        acc[2 * pr][w] = make_float2(ax[pr][w].x, ay[pr][w].x);
+        acc[2 * pr + 1][w] = make_float2(ax[pr][w].y, ay[pr][w].y);
+      }
   }
 
   // C~^* B over all poles, for the root z = -1
@@ -304,9 +381,20 @@ using namespace s4dev;
 #ifndef S4_CAUCHY_RPT1_BIG
 #define S4_CAUCHY_RPT1_BIG 2
 #endif
+// Packed (fp32x2) root pairs at rank 1 on grids of two waves or more, 4 roots
+// (two pairs) per thread: 3.4 % faster than the scalar loop on the
+// N=256 H=1024 M=65536 grid and 3.5 % on N=64 H=512 M=4096; the scalar loop
+// stays faster on smaller grids (20.5 against 22.5 us on N=64 H=256 M=1024),
+// and 2 roots per thread packed was 35 % slower (two shared loads per term).
+#ifndef S4_CAUCHY_PACKED
+#define S4_CAUCHY_PACKED 1
+#endif
+#ifndef S4_CAUCHY_PRPT1_BIG
+#define S4_CAUCHY_PRPT1_BIG 4
+#endif
 
 
-template <int RANK, int RPT>
+template <int RANK, int RPT, bool PACKED = false>
 static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
                                  const float2* B, const float2* Ct, const float* dt,
                                  float2* Khat, int H, int N, int M, int logC, St status,
@@ -322,7 +410,7 @@ static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const fl
   // grid's first wave would only sit on the SMs beside the previous kernel's tail.
   static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
   if (pdl && per_sm < 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T>, T, 0) != cudaSuccess)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED>, T, 0) != cudaSuccess)
     per_sm = 0;
   pdl = pdl && (long long)grid.x * grid.y <= (long long)per_sm * num_sms();
   cudaLaunchConfig_t cfg = {};
@@ -334,8 +422,8 @@ static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const fl
   cfg.stream = s;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T>, Lambda, P, Q, B, Ct, dt, Khat, N, logM, logC,
-                            status);
+  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T, PACKED>, Lambda, P, Q, B, Ct, dt, Khat, N, logM,
+                            logC, status);
 }
 
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
@@ -347,8 +435,14 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
   const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
   switch (r) {
     case 1:
+#if S4_CAUCHY_PACKED
+      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<1, S4_CAUCHY_PRPT1_BIG, true>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s,
+                                                               pdl);
+#else
       return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
                    : cauchy_launch<1, S4_CAUCHY_RPT1_BIG>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
+#endif
     case 2:  // 4 roots per thread on large grids measured 2 % faster (8 at rank 1 was 11 % slower)
       return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
                    : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);

@@ -1,0 +1,312 @@
+// Fused causal convolution for long rows (2M = 2^14 .. 2^17 points) by a
+// four-step split through global memory, with ordinary CTAs (no clusters), so
+// that every SM takes part.
+//
+// "Recurrent, LSTM, and structured state-space models": y_t = sum_{j<=t} K_j
+// u_{t-j} + D u_t; section "Roots-of-unity orthogonality and radix-two FFT
+// cost": the product of two length-M polynomials by zero-padding to n = 2M.
+//
+// Two batch rows b, b+1 of a channel are one complex row z = u_b + i u_{b+1}.
+// With K^r and K^i the spectra of Re K and Im K (both Hermitian, formed from
+// the spectrum K^ of K as K^r[k] = (K^[k] + conj K^[-k])/2 and K^i[k] =
+// (K^[k] - conj K^[-k])/(2i)), the two inverse transforms
+//     a = iFFT(Z (K^r + D)) = (Re K * u_b + D u_b) + i (Re K * u_{b+1} + D u_{b+1})
+//     c = iFFT(Z K^i)       =  Im K * u_b + i Im K * u_{b+1}
+// give y_b = Re a + i Re c and y_{b+1} = Im a + i Im c, with no mirror of Z
+// (the skip term D u enters as D added to every bin of K^r: the spectrum of D
+// times the unit impulse).
+//
+// Split n = 16 m, t = m t1 + t2, k = k1 + 16 k2 (t1, k1 < 16; t2, k2 < m):
+//     Z[k1 + 16 k2] = sum_{t2} w_m^{t2 k2} (w_n^{t2 k1} sum_{t1} z[m t1 + t2] w_16^{t1 k1}),
+// w_n = exp(-2 pi i/n).  Three kernels:
+//   fs_forward_kernel  per (pair, t2): the 16-point DFT over t1 (inputs t1 >= 8
+//                      are the zero padding) and the twiddle w_n^{t2 k1} -> X[pair][k1][t2]
+//   fs_column_kernel   per (pair, k1): the m-point FFT over t2, the products with
+//                      K^r + D and K^i (scaled 1/n), two m-point inverse FFTs over k2
+//                      -> a and c in the (k1, t2) layout (a over X's storage)
+//   fs_inverse_kernel  per (pair, t2): the twiddle w_n^{-t2 k1} and the 16-point
+//                      inverse over k1 for t1 < 8 (t < M) -> y_b, y_{b+1}
+// The spectrum K^ comes from the cluster spectrum kernels in their blocked
+// order (bin k at (k mod C) n/C + k div C, C = 2^cluster_log(log n)).
+#include "s4_fft.cuh"
+#include "s4_internal.h"
+
+namespace s4dev {
+
+constexpr int kFsRadix = 16;
+constexpr int kFsThreads = 256;  // threads per CTA of the two across-column kernels
+
+// Rows of a pair: pair p = h pb + j (pb = ceil(batch / 2)) holds rows b0 = 2 j and b0 + 1.
+struct FsPair {
+  int h;
+  size_t row0, row1;
+  bool has1;
+};
+__device__ __forceinline__ FsPair fs_pair(int p, int pb, int batch, int H) {
+  FsPair q;
+  q.h = p / pb;
+  const int b0 = 2 * (p % pb);
+  q.row0 = (size_t)b0 * H + q.h;
+  q.row1 = q.row0 + H;
+  q.has1 = b0 + 1 < batch;
+  return q;
+}
+
+// w_n^{t2} = exp(-2 pi i t2 / n)
+__device__ __forceinline__ float2 fs_twiddle(int t2, int n) {
+  float s, c;
+  sincospif(2.0f * (float)t2 / (float)n, &s, &c);
+  return make_float2(c, -s);
+}
+
+template <int LOGN>
+__global__ void __launch_bounds__(kFsThreads) fs_forward_kernel(const float* __restrict__ u,
+                                                                float2* __restrict__ X, int batch, int H,
+                                                                int L, int pb) {
+  constexpr int n = 1 << LOGN, m = n / kFsRadix;
+  const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
+  const int p = (int)(gid / m), t2 = (int)(gid % m);
+  if (p >= pb * H) return;
+  const FsPair q = fs_pair(p, pb, batch, H);
+  float2 x[kFsRadix];
+#pragma unroll
+  for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
+    const int t = m * t1 + t2;
+    x[t1] = make_float2(t < L ? __ldcs(u + q.row0 * L + t) : 0.f,
+                        (q.has1 && t < L) ? __ldcs(u + q.row1 * L + t) : 0.f);
+  }
+  dft<kFsRadix, false, true>(x);
+  apply_twiddles<kFsRadix>(x, fs_twiddle(t2, n));
+  float2* xp = X + (size_t)p * n + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < kFsRadix; ++k1) xp[(size_t)k1 * m] = x[k1];
+}
+
+template <int LOGN>
+__global__ void __launch_bounds__(kFsThreads) fs_inverse_kernel(const float2* __restrict__ Ar,
+                                                                const float2* __restrict__ Ci,
+                                                                float2* __restrict__ y, int batch, int H,
+                                                                int L, int pb, St status) {
+  constexpr int n = 1 << LOGN, m = n / kFsRadix;
+  const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
+  const int p = (int)(gid / m), t2 = (int)(gid % m);
+  if (p >= pb * H) return;
+  const FsPair q = fs_pair(p, pb, batch, H);
+  const bool zero = st_bad(status);
+  float2 a[kFsRadix], c[kFsRadix];
+  const size_t base = (size_t)p * n + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < kFsRadix; ++k1) {
+    a[k1] = __ldcs(Ar + base + (size_t)k1 * m);
+    c[k1] = __ldcs(Ci + base + (size_t)k1 * m);
+  }
+  float2 w = fs_twiddle(t2, n);
+  w.y = -w.y;
+  apply_twiddles<kFsRadix>(a, w);
+  apply_twiddles<kFsRadix>(c, w);
+  dft<kFsRadix, true, false, true>(a);
+  dft<kFsRadix, true, false, true>(c);
+#pragma unroll
+  for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
+    const int t = m * t1 + t2;
+    if (t < L) {
+      __stcs(y + q.row0 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].x, c[t1].x));
+      if (q.has1) __stcs(y + q.row1 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].y, c[t1].y));
+    }
+  }
+}
+
+// Column transforms: one column (pair p, k1) of m = 2^LOGM points per row group.
+template <int LOGM>
+struct FsColCfg {
+  static constexpr int m = 1 << LOGM;
+  static constexpr int T = conv_row_threads(LOGM);  // one radix-16 butterfly per thread at m = 8192
+  static constexpr int ROWS = T >= 128 ? 1 : 128 / T;
+  static constexpr int THREADS = T * ROWS;
+  static constexpr int NP = plan_npass(LOGM);
+  static constexpr int RA = plan_radix(LOGM, 0, false);
+  static constexpr int RB = plan_radix(LOGM, NP - 1, false);
+  static constexpr int PADM = padded_len(m);
+};
+
+// K^ at natural bin k from the blocked layout of a cluster of 2^logC CTAs.
+__device__ __forceinline__ float2 fs_spec(const float2* __restrict__ K2h, int k, int n, int logC) {
+  const int C = 1 << logC;
+  return __ldcg(K2h + (size_t)(k & (C - 1)) * (n >> logC) + (k >> logC));
+}
+
+// 512 threads per SM at 128 registers (one CTA for m = 8192, more for shorter columns)
+template <int LOGM>
+__global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>::THREADS) fs_column_kernel(
+    float2* __restrict__ X, float2* __restrict__ Ci, const float2* __restrict__ K2,
+    const float* __restrict__ D, int H, int pb, int logC, St status) {
+  using C = FsColCfg<LOGM>;
+  constexpr int m = C::m, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
+  constexpr int n = m * kFsRadix;
+  constexpr int NB0 = m / RA, PER0 = NB0 / T, NBL = m / RB, PERL = NBL / T;
+  using IXF0 = PassIdx<m, RA, 1>;
+  using IXFL = PassIdx<m, RB, m / RB>;
+  using IXI0 = PassIdx<m, RB, 1>;
+  using IXIL = PassIdx<m, RA, m / RA>;
+  using TWFL = PassTw<LOGM, NP - 1, false>;
+  using TWIL = PassTw<LOGM, NP - 1, true>;
+  extern __shared__ float2 smem[];
+  const int slot = threadIdx.x / T, lt = threadIdx.x % T;
+  float2* bufA = smem + slot * 2 * C::PADM;
+  float2* bufB = bufA + C::PADM;
+  float2* const buf1[1] = {bufA};
+  float2* const buf2[2] = {bufA, bufB};
+  const bool zero = st_bad(status);
+  const int cols = pb * H * kFsRadix;
+  const float sc = 1.f / n;
+  for (int c0 = blockIdx.x * C::ROWS; c0 < cols; c0 += gridDim.x * C::ROWS) {
+    const int col = c0 + slot;
+    const bool act = col < cols;
+    const int p = act ? col / kFsRadix : 0, k1 = col % kFsRadix;
+    const int h = p / pb;
+    float2* xc = X + (size_t)p * n + (size_t)k1 * m;        // this column: X in, a out
+    float2* cc = Ci + (size_t)p * n + (size_t)k1 * m;       // c out
+    const float2* K2h = K2 + (size_t)h * n;
+    const float dv = act ? D[h] : 0.f;
+    // forward pass 0: global -> shared
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {
+      const int i = lt + s * T;
+      float2 a[RA];
+#pragma unroll
+      for (int qq = 0; qq < RA; ++qq) a[qq] = act ? __ldcs(xc + i + qq * NB0) : make_float2(0.f, 0.f);
+      dft<RA, false>(a);
+#pragma unroll
+      for (int qq = 0; qq < RA; ++qq) bufA[IXF0::wr(i, qq)] = a[qq];
+    }
+    __syncthreads();
+    passes_rows<LOGM, false, 1, NP - 2, T, 1>(buf1, lt);
+    // last forward pass in registers (bins k2 = i + q NBL), the two products,
+    // the first inverse pass (P = 1) in registers
+    float2 pa[PERL][RB], pc[PERL][RB];
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+      float2 z[RB], w[RB];
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq) z[qq] = bufA[IXFL::rd(i, qq)];
+      TWFL::load(w, i);
+      TWFL::apply(z, w);
+      dft<RB, false>(z);
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq) {
+        const int k2 = i + qq * NBL;
+        const int k = k1 + kFsRadix * k2;
+        const float2 kv = fs_spec(K2h, k, n, logC);
+        const float2 km = fs_spec(K2h, (n - k) & (n - 1), n, logC);
+        // (K^r + D)/n and K^i/n
+        const float2 kr = make_float2(fmaf(0.5f * sc, kv.x + km.x, dv * sc), 0.5f * sc * (kv.y - km.y));
+        const float2 ki = make_float2(0.5f * sc * (kv.y + km.y), 0.5f * sc * (km.x - kv.x));
+        pa[s][qq] = cmul(z[qq], kr);
+        pc[s][qq] = cmul(z[qq], ki);
+      }
+      dft<RB, true>(pa[s]);
+      dft<RB, true>(pc[s]);
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq) bufB[IXI0::wr(i, qq)] = pc[s][qq];
+    }
+    __syncthreads();  // every thread has read its last forward pass from bufA
+#pragma unroll
+    for (int s = 0; s < PERL; ++s) {
+      const int i = lt + s * T;
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq) bufA[IXI0::wr(i, qq)] = pa[s][qq];
+    }
+    __syncthreads();
+    passes_rows<LOGM, true, 1, NP - 2, T, 2>(buf2, lt);
+    // last inverse pass: every t2 of both products, back over X's column and into Ci
+#pragma unroll
+    for (int s = 0; s < PER0; ++s) {
+      const int i = lt + s * T;
+      float2 a[RA], c[RA], w[RA];
+#pragma unroll
+      for (int qq = 0; qq < RA; ++qq) {
+        a[qq] = bufA[IXIL::rd(i, qq)];
+        c[qq] = bufB[IXIL::rd(i, qq)];
+      }
+      TWIL::load(w, i);
+      TWIL::apply(a, w);
+      TWIL::apply(c, w);
+      dft<RA, true>(a);
+      dft<RA, true>(c);
+      if (act) {
+#pragma unroll
+        for (int qq = 0; qq < RA; ++qq) {
+          xc[i + qq * NB0] = zero ? make_float2(0.f, 0.f) : a[qq];
+          cc[i + qq * NB0] = zero ? make_float2(0.f, 0.f) : c[qq];
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace s4dev
+
+namespace s4impl {
+using namespace s4dev;
+
+size_t fs_scratch_bytes(int logn, int batch, int H) {
+  if (logn < kMinLogFourStep || logn > kMaxLogFourStep) return 0;
+  const size_t pairs = (size_t)((batch + 1) / 2) * (size_t)H;
+  return 2 * pairs * ((size_t)1 << logn) * sizeof(float2);
+}
+
+template <int LOGN>
+static cudaError_t fs_launch(const float* u, const float2* K2, const float* D, float2* y, int batch, int H,
+                             int L, float2* scratch, St st, cudaStream_t s) {
+  constexpr int n = 1 << LOGN, m = n / kFsRadix, LOGM = LOGN - 4;
+  using C = FsColCfg<LOGM>;
+  const int pb = (batch + 1) / 2;
+  const long long pairs = (long long)pb * H;
+  float2* X = scratch;
+  float2* Ci = scratch + (size_t)pairs * n;
+  const unsigned blocks = (unsigned)((pairs * m + kFsThreads - 1) / kFsThreads);
+  {
+    TimedLaunch tl("conv_fwd", s);
+    fs_forward_kernel<LOGN><<<blocks, kFsThreads, 0, s>>>(u, X, batch, H, L, pb);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(float2) * 2 * (size_t)C::ROWS * C::PADM;
+  auto k = fs_column_kernel<LOGM>;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, C::THREADS, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const long long cols = pairs * kFsRadix;
+  const long long need = (cols + C::ROWS - 1) / C::ROWS;
+  const int grid = (int)(need < (long long)per_sm * num_sms() ? need : (long long)per_sm * num_sms());
+  {
+    TimedLaunch tl("conv_col", s);
+    k<<<grid, C::THREADS, smem, s>>>(X, Ci, K2, D, H, pb, cluster_log(LOGN), st);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    TimedLaunch tl("conv_inv", s);
+    fs_inverse_kernel<LOGN><<<blocks, kFsThreads, 0, s>>>(X, Ci, y, batch, H, L, pb, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, const float* D, float2* y, int batch,
+                                 int H, int L, float2* scratch, St st, cudaStream_t s) {
+  switch (logn) {
+    case 14: return fs_launch<14>(u, K2, D, y, batch, H, L, scratch, st, s);
+    case 15: return fs_launch<15>(u, K2, D, y, batch, H, L, scratch, st, s);
+    case 16: return fs_launch<16>(u, K2, D, y, batch, H, L, scratch, st, s);
+    case 17: return fs_launch<17>(u, K2, D, y, batch, H, L, scratch, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace s4impl

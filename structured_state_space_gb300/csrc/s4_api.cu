@@ -27,17 +27,21 @@ int ilog2_ceil(int v) {
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Workspace: [status word | root values (H M) | kernel spectra (H 2M)]
+// Workspace: [status word | root values (H M) | kernel spectra (H 2M) |
+// long-row convolution scratch (two rows of 2M points per pair of batch rows,
+// only when 2M >= 2^14)].  `gen_total` is what kernel generation alone needs.
 struct Layout {
-  size_t khat, k2, total;
+  size_t khat, k2, fs, gen_total, total;
 };
 
-Layout layout_for(int H, int L) {
+Layout layout_for(int H, int L, int batch) {
   const size_t M = (size_t)1 << ilog2_ceil(L);
   Layout l;
   l.khat = 256;
   l.k2 = l.khat + round256(sizeof(float2) * M * (size_t)H);
-  l.total = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
+  l.fs = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
+  l.gen_total = l.fs;
+  l.total = l.fs + round256(s4impl::fs_scratch_bytes(ilog2_ceil(L) + 1, batch, H));
   return l;
 }
 
@@ -51,9 +55,11 @@ bool sizes_ok(int H, int N, int r, int L, int batch) {
   return true;
 }
 
-s4_status check_ws(const void* ws, size_t ws_bytes, int H, int L) {
+// batch = 0: kernel generation only (no convolution scratch)
+s4_status check_ws(const void* ws, size_t ws_bytes, int H, int L, int batch) {
   if (ws == nullptr || !aligned(ws, 256)) return S4_ERR_WORKSPACE;
-  if (ws_bytes < layout_for(H, L).total) return S4_ERR_WORKSPACE;
+  const Layout l = layout_for(H, L, batch > 0 ? batch : 1);
+  if (ws_bytes < (batch > 0 ? l.total : l.gen_total)) return S4_ERR_WORKSPACE;
   return S4_OK;
 }
 
@@ -102,7 +108,7 @@ cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   return launch_cauchy(reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
                        reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
                        reinterpret_cast<const float2*>(Ct), dt,
-                       reinterpret_cast<float2*>(w + layout_for(H, L).khat), H, N, r, 1 << logM,
+                       reinterpret_cast<float2*>(w + layout_for(H, L, 1).khat), H, N, r, 1 << logM,
                        khat_cluster_log(logM), st, s, pdl);
 }
 
@@ -111,7 +117,7 @@ s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const
                    void* ws, s4impl::St st, bool pdl, cudaStream_t s) {
   using namespace s4impl;
   const int logM = ilog2_ceil(L);
-  const Layout lay = layout_for(H, L);
+  const Layout lay = layout_for(H, L, 1);
   char* w = static_cast<char*>(ws);
   float2* khat = reinterpret_cast<float2*>(w + lay.khat);
   cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ct, dt, H, N, r, L, ws, st, pdl, s);
@@ -126,12 +132,11 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
                     s4_c32* y, void* ws, s4impl::St st, bool chain, cudaStream_t s) {
   using namespace s4impl;
   const int logn = ilog2_ceil(L) + 1;
-  const Layout lay = layout_for(H, L);
+  const Layout lay = layout_for(H, L, batch);
   char* w = static_cast<char*>(ws);
   float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   float2* yf = reinterpret_cast<float2*>(y);
-  const int rows = batch * H;
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
     e = launch_spectrum_rows(logn, Kf, k2, H, L, st, s, false, /*pdl=*/chain);
@@ -140,7 +145,8 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
     if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s, /*pdl=*/true);
   } else {
     e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
-    if (e == cudaSuccess) e = launch_conv_cluster(logn, u, k2, D, yf, rows, H, L, st, s);
+    if (e == cudaSuccess)
+      e = launch_conv_fourstep(logn, u, k2, D, yf, batch, H, L, reinterpret_cast<float2*>(w + lay.fs), st, s);
   }
   return cuda_status(e);
 }
@@ -250,7 +256,7 @@ s4_status s4_set_wait_limit(int polls) {
 
 size_t s4_workspace_bytes(int H, int N, int r, int L, int batch) {
   if (!sizes_ok(H, N, r, L, batch)) return 0;
-  return layout_for(H, L).total;
+  return layout_for(H, L, batch).total;
 }
 
 s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
@@ -261,7 +267,7 @@ s4_status s4_kernel_gen(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   if (!aligned(Lambda, 8) || !aligned(P, 8) || !aligned(Q, 8) || !aligned(B, 8) ||
       !aligned(Ctilde, 8) || !aligned(dt, 4) || !aligned(K, 16))
     return S4_ERR_INVALID_ARG;
-  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  const s4_status wst = check_ws(ws, ws_bytes, H, L, 0);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   s4impl::St st;
@@ -276,7 +282,7 @@ s4_status s4_conv_fwd(const float* u, const s4_c32* K, const float* D, int batch
   if (!sizes_ok(H, 1, 1, L, batch)) return S4_ERR_INVALID_ARG;
   if (!aligned(u, 16) || !aligned(K, 16) || !aligned(D, 4) || !aligned(y, 16))
     return S4_ERR_INVALID_ARG;
-  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  const s4_status wst = check_ws(ws, ws_bytes, H, L, batch);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   s4impl::St st;
@@ -290,7 +296,7 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   if (!u || !K || !D || !y) return S4_ERR_INVALID_ARG;
   if (!sizes_ok(H, 1, 1, L, batch)) return S4_ERR_INVALID_ARG;
   if (!aligned(u, 16) || !aligned(K, 16) || !aligned(D, 4) || !aligned(y, 16)) return S4_ERR_INVALID_ARG;
-  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  const s4_status wst = check_ws(ws, ws_bytes, H, L, 0);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   using namespace s4impl;
@@ -299,7 +305,7 @@ s4_status s4_conv_fwd_real(const float* u, const s4_c32* K, const float* D, int 
   St st;
   bool chain;
   if (!call_status(ws, s, &st, &chain)) return S4_ERR_CUDA;
-  float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L).k2);
+  float2* k2 = reinterpret_cast<float2*>(w + layout_for(H, L, 1).k2);
   const float2* Kf = reinterpret_cast<const float2*>(K);
   cudaError_t e;
   if (logn <= kMaxLogConvRow) {
@@ -323,7 +329,7 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
       !aligned(Ctilde, 8) || !aligned(dt, 4) || !aligned(D, 4) || !aligned(u, 16) ||
       !aligned(K, 16) || !aligned(y, 16))
     return S4_ERR_INVALID_ARG;
-  const s4_status wst = check_ws(ws, ws_bytes, H, L);
+  const s4_status wst = check_ws(ws, ws_bytes, H, L, batch);
   if (wst != S4_OK) return wst;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // No reset of the status block: this call's flags carry a fresh generation,
@@ -335,7 +341,7 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
   const int logM = ilog2_ceil(L);
   if (s4impl::kspec_supported(logM) && logM + 1 <= s4impl::kMaxLogConvRow) {
     // root values -> (K, kernel spectrum) in one launch -> convolution
-    const Layout lay = layout_for(H, L);
+    const Layout lay = layout_for(H, L, batch);
     char* w = static_cast<char*>(ws);
     float2* khat = reinterpret_cast<float2*>(w + lay.khat);
     float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
@@ -345,6 +351,20 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
     if (e == cudaSuccess)
       e = s4impl::launch_conv_rows(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L, st, s,
                                    /*pdl=*/true);
+    return cuda_status(e);
+  }
+  if (s4impl::kspec_cluster_supported(logM)) {
+    // long rows: root values -> (K, kernel spectrum) in one clustered launch -> convolution
+    const Layout lay = layout_for(H, L, batch);
+    char* w = static_cast<char*>(ws);
+    float2* khat = reinterpret_cast<float2*>(w + lay.khat);
+    float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
+    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s);
+    if (e == cudaSuccess)
+      e = s4impl::launch_kspec_cluster(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
+    if (e == cudaSuccess)
+      e = s4impl::launch_conv_fourstep(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L,
+                                       reinterpret_cast<float2*>(w + lay.fs), st, s);
     return cuda_status(e);
   }
   const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, chain, s);

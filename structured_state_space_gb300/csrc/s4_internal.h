@@ -85,6 +85,23 @@ cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const f
                              int batch, int H, int L, St st, cudaStream_t s,
                              bool pdl = false);
 
+// Layer path for M = 2^16 (kspec_cluster_supported): the inverse transform of
+// the root values (K out) and the kernel spectrum of 2M points in one launch,
+// one 8-CTA cluster per channel; K2 as from launch_spectrum_cluster.
+bool kspec_cluster_supported(int logM);
+cudaError_t launch_kspec_cluster(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
+                                 St st, cudaStream_t s);
+
+// Long-row convolution by a four-step split through global memory (2M =
+// 2^14 .. 2^17 points; K2 in the blocked order of the cluster spectrum
+// kernels): three launches, scratch of fs_scratch_bytes(logn, batch, H) bytes
+// (two complex rows of 2M points per pair of batch rows), 16-byte aligned.
+constexpr int kMinLogFourStep = 14;
+constexpr int kMaxLogFourStep = 17;
+size_t fs_scratch_bytes(int logn, int batch, int H);
+cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, const float* D, float2* y, int batch,
+                                 int H, int L, float2* scratch, St st, cudaStream_t s);
+
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,
                                 St st, cudaStream_t s);
