@@ -416,26 +416,33 @@ def run_ours(args):
     ms_prof = timed(prof_steps, S)
     s4.timing.enable(False)
     ms_prof -= timed(head_start, 0)
-    kern = {}
-    for name in ["cauchy", "ifft", "spectrum", "kspec", "conv", "conv_fwd", "conv_col", "conv_inv"]:
+    fams = ["cauchy", "ifft", "kspec_cross", "spectrum", "spec_fwd", "kspec", "conv", "conv_fwd", "conv_col",
+            "conv_inv"]
+    raw = {}
+    for name in fams:
         n, t = s4.timing.read(name)
-        kern[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1), "share": 0.0}
+        raw[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1)}
     s4.timing.reset()
-    # long rows: the convolution is three launches (across-column radix-16 step,
-    # column transforms, inverse across-column step); as one step of the path
-    # they count together as "conv"
-    four = ["conv_fwd", "conv_col", "conv_inv"]
-    if kern["conv_col"]["launches"]:
-        kern["conv"] = {"launches": kern["conv_col"]["launches"],
-                        "avg_us": sum(kern[k]["avg_us"] for k in four), "share": 0.0,
-                        "parts": {k: kern.pop(k) for k in four}}
-    else:
-        for k in four:
-            kern.pop(k)
+    launches_per_step = int(round(sum(v["launches"] for v in raw.values()) / S))
+    # the step's parts: the root values, the kernel spectrum (one launch on short
+    # rows; on long rows the column inverse transforms, the cross step that writes
+    # K, and the column spectra) and the convolution (one launch on short rows;
+    # on long rows the across-column step, the column transforms and the inverse
+    # across-column step); a part's time is the sum of its launches per step
+    groups = {"cauchy": ["cauchy"], "kspec": ["kspec", "ifft", "kspec_cross", "spectrum", "spec_fwd"],
+              "conv": ["conv", "conv_fwd", "conv_col", "conv_inv"]}
+    kern = {}
+    for g, members in groups.items():
+        used = [k for k in members if raw[k]["launches"]]
+        if not used:
+            continue
+        kern[g] = {"launches": max(raw[k]["launches"] for k in used),
+                   "avg_us": sum(raw[k]["avg_us"] * raw[k]["launches"] / S for k in used), "share": 0.0}
+        if len(used) > 1:
+            kern[g]["parts"] = {k: raw[k] for k in used}
     tot = sum(v["avg_us"] for v in kern.values())
     for v in kern.values():
         v["share"] = v["avg_us"] / tot if tot > 0 else 0.0
-    parts_per_step = sum(len(v.get("parts", {})) - 1 for v in kern.values() if v.get("parts"))
 
     # end to end through the public call: every step copies its input from
     # pinned host memory and its output back, pipelined over three streams
@@ -528,7 +535,6 @@ def run_ours(args):
     roof["fp32_probe"] = fp32_probe(dev, fp32_peak)
     roof["others"] = {k: roof_of(k) for k in kern if k != dom and kern[k]["launches"]}
 
-    launches_per_step = int(round(sum(v["launches"] for v in kern.values()) / S)) + parts_per_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -568,7 +574,7 @@ def run_ours(args):
 PATHS = {
     # path: (unit of the rate, timing families of the library, dominant family)
     "kernel_gen": ("channel-roots/s", ["cauchy", "ifft"], "cauchy"),
-    "conv": ("channel-samples/s", ["spectrum", "conv"], "conv"),
+    "conv": ("channel-samples/s", ["spec_fwd", "spectrum", "conv", "conv_fwd", "conv_col", "conv_inv"], "conv"),
     "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
     "recurrent": ("channel-samples/s", ["recurrent", "bordered"], "recurrent"),
     "ctilde": ("channel-steps/s", ["ctilde", "bordered"], "ctilde"),
@@ -722,11 +728,25 @@ def run_path(args):
 
     timed(prof, S)
     s4.timing.enable(False)
-    kern = {}
+    raw = {}
     for name in families:
         n, t = s4.timing.read(name)
-        kern[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1)}
+        raw[name] = {"launches": n, "avg_us": 1e3 * t / max(n, 1)}
     s4.timing.reset()
+    launches_per_call = int(round(sum(v["launches"] for v in raw.values()) / S))
+    # long rows: the convolution's three launches count as one part, the
+    # spectrum's two likewise (per-call time = the sum)
+    groups = {"conv": ["conv", "conv_fwd", "conv_col", "conv_inv"], "spectrum": ["spectrum", "spec_fwd"]}
+    kern = {}
+    for name in families:
+        g = next((k for k, v in groups.items() if name in v), name)
+        if g in kern or not (raw[name]["launches"] or name == g):
+            continue
+        used = [k for k in groups.get(g, [g]) if k in raw and raw[k]["launches"]] or [name]
+        kern[g] = {"launches": max(raw[k]["launches"] for k in used),
+                   "avg_us": sum(raw[k]["avg_us"] * raw[k]["launches"] / S for k in used)}
+        if len(used) > 1:
+            kern[g]["parts"] = {k: raw[k] for k in used}
     per_call = H * M if args.path in ("ctilde", "kernel_gen") else Bsz * H * L
     value = per_call * K / (ms_total / 1e3)
     peaks, peak_src = read_peaks()
@@ -781,7 +801,7 @@ def run_path(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; shapes and distributions of the workload)",
             "config": {"workload": w.name, "N": N, "r": r, "H": H, "L": L, "M": M, "batch": Bsz},
-            "gpu_launches": int(round(sum(v["launches"] for v in kern.values()) / S)) * K,
+            "gpu_launches": launches_per_call * K,
             "kernels": kern, "roofline": roof, "clocks": clocks, "e2e": e2e}
     if pool is not None:
         if args.path in ("ctilde", "kernel_gen"):

@@ -188,90 +188,6 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
   }
 }
 
-// Layer path for M = 2^16: the inverse transform of the root values and the
-// kernel spectrum in one launch, over one 8-CTA cluster per channel.  K (an
-// output of the layer) is written once as the inverse's last step, and the
-// spectrum's forward step reads it back through L2 right away: the inverse
-// holds K in the four-step order of an M-point row (8192 points per CTA), the
-// forward needs it in that of a 2M-point row (16384 per CTA), so the exchange
-// goes through the just-written global copy instead of a second HBM pass.
-template <int LOGM>
-__global__ void __launch_bounds__(ClusterCfg<LOGM, true>::T) kspec_cluster_kernel(
-    const float2* __restrict__ Khat, float2* __restrict__ K, float2* __restrict__ K2, int H, int L,
-    St status) {
-  using CI = ClusterCfg<LOGM, true>;  // inverse: M points (the paired shape: one radix-16 butterfly per thread)
-  using CF = ClusterCfg<LOGM + 1>;    // forward: 2M points, zero-padded
-  static_assert(CI::C == CF::C && CI::T == CF::T, "one cluster shape for both transforms");
-  constexpr int C = CI::C, T = CI::T;
-  constexpr int M = CI::n, mi = CI::m, NPI = CI::NP, LOGMI = CI::LOGM;
-  constexpr int n = CF::n, mf = CF::m, NPF = CF::NP, LOGMF = CF::LOGM;
-  constexpr int R0 = plan_radix(LOGMI, 0, true), NB0 = mi / R0, PER0 = NB0 / T;
-  using IX0 = PassIdx<mi, R0, 1>;
-  constexpr int RB = plan_radix(LOGMF, NPF - 1, false), NBL = mf / RB, PERL = NBL / T;
-  using IXL = PassIdx<mf, RB, mf / RB>;
-  using TWL = PassTw<LOGMF, NPF - 1, false>;
-  cg::cluster_group cl = cg::this_cluster();
-  const int c = (int)cl.block_rank();
-  extern __shared__ float2 smem[];
-  float2* twi = smem;              // cross twiddles of the inverse (CI::MI)
-  float2* twf = twi + CI::MI;      // ... of the forward (CF::MI)
-  float2* buf = twf + CF::MI;      // one row buffer of the larger (forward) length
-  float2* const bufs[1] = {buf};
-  const int lt = threadIdx.x;
-  fill_cross_twiddles(twi, c, CI::MI, M, lt, T);
-  fill_cross_twiddles(twf, c, CF::MI, n, lt, T);
-  const bool zero = st_bad(status);
-  __syncthreads();
-  cl.sync();
-  const float sc = 1.f / M;
-  bool fin = true;
-  const int ncl = gridDim.x / C;
-  for (int h = blockIdx.x / C; h < H; h += ncl) {
-    // ---- K = first L of (1/M) iFFT_M(Khat), blocked input order
-#pragma unroll
-    for (int s = 0; s < PER0; ++s) {
-      const int i = lt + s * T;
-      float2 a[R0];
-#pragma unroll
-      for (int q = 0; q < R0; ++q) a[q] = __ldcg(Khat + (size_t)h * M + (size_t)c * mi + i + q * NB0);
-      dft<R0, true>(a);
-#pragma unroll
-      for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
-    }
-    __syncthreads();
-    passes_rows<LOGMI, true, 1, NPI - 1, T, 1>(bufs, lt);
-    cl.sync();
-    cross_inverse<LOGM, false, true>(cl, buf, twi, c, lt, [&](int, int, int t, float2 v) {
-      if (t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(v, sc);
-    });
-    __threadfence();  // K visible to the other CTAs of the cluster before they read it
-    cl.sync();
-    // ---- K2 = FFT_2M(K zero-padded), blocked output order; K read back through L2
-    cross_forward<LOGM + 1>(cl, buf, twf, c, lt, [&](int, int, int t) {
-      return t < L ? __ldcg(K + (size_t)h * L + t) : make_float2(0.f, 0.f);
-    });
-    cl.sync();
-    passes_rows<LOGMF, false, 0, NPF - 2, T, 1>(bufs, lt);
-#pragma unroll
-    for (int s = 0; s < PERL; ++s) {
-      const int i = lt + s * T;
-      float2 a[RB], w[RB];
-#pragma unroll
-      for (int q = 0; q < RB; ++q) a[q] = buf[IXL::rd(i, q)];
-      TWL::load(w, i);
-      TWL::apply(a, w);
-      dft<RB, false>(a);
-#pragma unroll
-      for (int q = 0; q < RB; ++q) {
-        fin = fin && cfinite(a[q]);
-        K2[(size_t)h * n + (size_t)c * mf + i + q * NBL] = a[q];
-      }
-    }
-    cl.sync();
-  }
-  if (!fin) st_flag(status, ST_NONFINITE);
-}
-
 // Fused causal convolution for rows of n = 2M > 16384 points.  The skip term
 // enters as D added to every kernel-spectrum bin (the spectrum of D times the
 // unit impulse), so no input value stays live across the transforms.
@@ -595,24 +511,6 @@ static cudaError_t spectrum_cl(const float2* K, float2* K2, int H, int L, St st,
   const size_t smem = sizeof(float2) * (Cf::MI + (size_t)Cf::PADM);
   return launch_clustered(spectrum_cluster_kernel<LOGN>, Cf::C, Cf::T, smem, H, "spectrum", s, K, K2,
                           H, L, realk ? 1 : 0, st);
-}
-
-template <int LOGM>
-static cudaError_t kspec_cl(const float2* Khat, float2* K, float2* K2, int H, int L, St st, cudaStream_t s) {
-  using CI = ClusterCfg<LOGM, true>;
-  using CF = ClusterCfg<LOGM + 1>;
-  const size_t smem = sizeof(float2) * ((size_t)CI::MI + CF::MI + (size_t)CF::PADM);
-  return launch_clustered(kspec_cluster_kernel<LOGM>, CI::C, CI::T, smem, H, "kspec", s, Khat, K, K2, H, L, st);
-}
-
-bool kspec_cluster_supported(int logM) { return logM == 16; }
-
-cudaError_t launch_kspec_cluster(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
-                                 St st, cudaStream_t s) {
-  switch (logM) {
-    case 16: return kspec_cl<16>(Khat, K, K2, H, L, st, s);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 template <int LOGN>

@@ -26,8 +26,22 @@
 //                      -> a and c in the (k1, t2) layout (a over X's storage)
 //   fs_inverse_kernel  per (pair, t2): the twiddle w_n^{-t2 k1} and the 16-point
 //                      inverse over k1 for t1 < 8 (t < M) -> y_b, y_{b+1}
-// The spectrum K^ comes from the cluster spectrum kernels in their blocked
-// order (bin k at (k mod C) n/C + k div C, C = 2^cluster_log(log n)).
+// The spectrum K^ is read in a blocked order, bin k at (k mod C) n/C + k div C:
+// C = 16 ("column order", K^[k1][k2]) when it comes from the four-step spectrum
+// below, C = 2^cluster_log(log n) when it comes from the cluster spectrum kernels.
+//
+// The kernel spectrum itself, also in four steps:
+//   fs_kfwd_kernel   per (channel, t2): the radix-16 across-column step of the
+//                    2M-point transform of K (zero-padded) -> X[h][k1][t2];
+//                    the row spectrum kernel then transforms the 16 H columns of
+//                    2M/16 points (full transforms) -> K2 in column order, scaled 8/(2M).
+// and, on the layer path, from the root values Khat in column order
+// [k1][k2] (k = k1 + 16 k2 of the M-point grid):
+//   the row inverse-transform kernel: the 16 H columns of M/16 points, 1/(M/16)
+//   ks_cross_kernel  per (channel, t2 < M/16): the twiddle w_M^{-t2 k1} and the
+//                    16-point inverse over k1 (1/16) -> K[h][t], t = (M/16) t1 + t2
+//                    (written out), then the forward across-column step of the
+//                    2M transform for its two columns t2 and t2 + M/16 -> X[h][k1][.]
 #include "s4_fft.cuh"
 #include "s4_internal.h"
 
@@ -80,6 +94,73 @@ __global__ void __launch_bounds__(kFsThreads) fs_forward_kernel(const float* __r
   float2* xp = X + (size_t)p * n + t2;
 #pragma unroll
   for (int k1 = 0; k1 < kFsRadix; ++k1) xp[(size_t)k1 * m] = x[k1];
+}
+
+// Forward across-column step of the 2M-point spectrum of a complex kernel K
+// [H][L] (zero beyond L): X[h][k1][t2] = w_n^{t2 k1} sum_{t1 < 8} K[m t1 + t2] w_16^{t1 k1}.
+template <int LOGN>
+__global__ void __launch_bounds__(kFsThreads) fs_kfwd_kernel(const float2* __restrict__ K,
+                                                             float2* __restrict__ X, int H, int L,
+                                                             int realk) {
+  constexpr int n = 1 << LOGN, m = n / kFsRadix;
+  const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
+  const int h = (int)(gid / m), t2 = (int)(gid % m);
+  if (h >= H) return;
+  float2 x[kFsRadix];
+#pragma unroll
+  for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
+    const int t = m * t1 + t2;
+    x[t1] = t < L ? __ldg(K + (size_t)h * L + t) : make_float2(0.f, 0.f);
+    if (realk) x[t1].y = 0.f;
+  }
+  dft<kFsRadix, false, true>(x);
+  apply_twiddles<kFsRadix>(x, fs_twiddle(t2, n));
+  float2* xp = X + (size_t)h * n + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < kFsRadix; ++k1) xp[(size_t)k1 * m] = x[k1];
+}
+
+// Layer path: K from the column inverse transforms G[h][k1][t2] (M/16 points
+// each, already scaled 1/(M/16)), and the forward across-column step of its
+// 2M-point spectrum.  A thread owns t2 < M/16: K[(M/16) t1 + t2] for all t1 < 16,
+// which are the 8 nonzero inputs of the 2M step's columns t2 (t1 even) and
+// t2 + M/16 (t1 odd).
+template <int LOGM>
+__global__ void __launch_bounds__(kFsThreads) ks_cross_kernel(const float2* __restrict__ G,
+                                                              float2* __restrict__ K, float2* __restrict__ X,
+                                                              int H, int L, St status) {
+  constexpr int M = 1 << LOGM, mi = M / kFsRadix, n = 2 * M, mf = n / kFsRadix;
+  const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
+  const int h = (int)(gid / mi), t2 = (int)(gid % mi);
+  if (h >= H) return;
+  const bool zero = st_bad(status);
+  float2 g[kFsRadix];
+  const float2* gp = G + (size_t)h * M + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < kFsRadix; ++k1) g[k1] = __ldcs(gp + (size_t)k1 * mi);
+  float2 w = fs_twiddle(t2, M);
+  w.y = -w.y;
+  apply_twiddles<kFsRadix>(g, w);
+  dft<kFsRadix, true>(g);
+  float2 xa[kFsRadix], xb[kFsRadix];
+#pragma unroll
+  for (int t1 = 0; t1 < kFsRadix; ++t1) {
+    const int t = mi * t1 + t2;
+    const float2 v = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(g[t1], 1.f / kFsRadix);
+    if (t < L) K[(size_t)h * L + t] = v;
+    if (t1 % 2 == 0) xa[t1 / 2] = v;
+    else xb[t1 / 2] = v;
+  }
+  dft<kFsRadix, false, true>(xa);
+  dft<kFsRadix, false, true>(xb);
+  apply_twiddles<kFsRadix>(xa, fs_twiddle(t2, n));
+  apply_twiddles<kFsRadix>(xb, fs_twiddle(t2 + mi, n));
+  float2* xp = X + (size_t)h * n + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < kFsRadix; ++k1) {
+    xp[(size_t)k1 * mf] = xa[k1];
+    xp[(size_t)k1 * mf + mi] = xb[k1];
+  }
 }
 
 template <int LOGN>
@@ -139,7 +220,7 @@ __device__ __forceinline__ float2 fs_spec(const float2* __restrict__ K2h, int k,
 template <int LOGM>
 __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>::THREADS) fs_column_kernel(
     float2* __restrict__ X, float2* __restrict__ Ci, const float2* __restrict__ K2,
-    const float* __restrict__ D, int H, int pb, int logC, St status) {
+    const float* __restrict__ D, int H, int pb, int logC, float kscale, St status) {
   using C = FsColCfg<LOGM>;
   constexpr int m = C::m, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int n = m * kFsRadix;
@@ -199,9 +280,9 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
         const int k = k1 + kFsRadix * k2;
         const float2 kv = fs_spec(K2h, k, n, logC);
         const float2 km = fs_spec(K2h, (n - k) & (n - 1), n, logC);
-        // (K^r + D)/n and K^i/n
-        const float2 kr = make_float2(fmaf(0.5f * sc, kv.x + km.x, dv * sc), 0.5f * sc * (kv.y - km.y));
-        const float2 ki = make_float2(0.5f * sc * (kv.y + km.y), 0.5f * sc * (km.x - kv.x));
+        // (K^r + D)/n and K^i/n, the stored spectrum being K^ n kscale
+        const float2 kr = make_float2(fmaf(0.5f * kscale, kv.x + km.x, dv * sc), 0.5f * kscale * (kv.y - km.y));
+        const float2 ki = make_float2(0.5f * kscale * (kv.y + km.y), 0.5f * kscale * (km.x - kv.x));
         pa[s][qq] = cmul(z[qq], kr);
         pc[s][qq] = cmul(z[qq], ki);
       }
@@ -258,8 +339,8 @@ size_t fs_scratch_bytes(int logn, int batch, int H) {
 }
 
 template <int LOGN>
-static cudaError_t fs_launch(const float* u, const float2* K2, const float* D, float2* y, int batch, int H,
-                             int L, float2* scratch, St st, cudaStream_t s) {
+static cudaError_t fs_launch(const float* u, const float2* K2, int k2_logC, float k2_scale, const float* D,
+                             float2* y, int batch, int H, int L, float2* scratch, St st, cudaStream_t s) {
   constexpr int n = 1 << LOGN, m = n / kFsRadix, LOGM = LOGN - 4;
   using C = FsColCfg<LOGM>;
   const int pb = (batch + 1) / 2;
@@ -287,7 +368,7 @@ static cudaError_t fs_launch(const float* u, const float2* K2, const float* D, f
   const int grid = (int)(need < (long long)per_sm * num_sms() ? need : (long long)per_sm * num_sms());
   {
     TimedLaunch tl("conv_col", s);
-    k<<<grid, C::THREADS, smem, s>>>(X, Ci, K2, D, H, pb, cluster_log(LOGN), st);
+    k<<<grid, C::THREADS, smem, s>>>(X, Ci, K2, D, H, pb, k2_logC, k2_scale, st);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -298,13 +379,75 @@ static cudaError_t fs_launch(const float* u, const float2* K2, const float* D, f
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, const float* D, float2* y, int batch,
-                                 int H, int L, float2* scratch, St st, cudaStream_t s) {
+cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, int k2_logC, float k2_scale,
+                                 const float* D, float2* y, int batch, int H, int L, float2* scratch, St st,
+                                 cudaStream_t s) {
   switch (logn) {
-    case 14: return fs_launch<14>(u, K2, D, y, batch, H, L, scratch, st, s);
-    case 15: return fs_launch<15>(u, K2, D, y, batch, H, L, scratch, st, s);
-    case 16: return fs_launch<16>(u, K2, D, y, batch, H, L, scratch, st, s);
-    case 17: return fs_launch<17>(u, K2, D, y, batch, H, L, scratch, st, s);
+    case 14: return fs_launch<14>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
+    case 15: return fs_launch<15>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
+    case 16: return fs_launch<16>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
+    case 17: return fs_launch<17>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+size_t fs_spec_scratch_bytes(int logn, int H) {
+  if (logn < kMinLogFourStep || logn > kMaxLogFourStep) return 0;
+  return (size_t)H * ((size_t)1 << logn) * sizeof(float2);
+}
+
+// The 2M = 2^logn spectrum of K [H][L] in column order, scaled 1/(2 (2M/16)) (see above).
+template <int LOGN>
+static cudaError_t fs_spec_launch(const float2* K, float2* K2, int H, int L, float2* scratch, St st,
+                                  cudaStream_t s, bool realk) {
+  constexpr int n = 1 << LOGN, m = n / kFsRadix;
+  const unsigned blocks = (unsigned)(((long long)H * m + kFsThreads - 1) / kFsThreads);
+  {
+    TimedLaunch tl("spec_fwd", s);
+    fs_kfwd_kernel<LOGN><<<blocks, kFsThreads, 0, s>>>(K, scratch, H, L, realk ? 1 : 0);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // columns of m points, no padding; records the call's generation
+  return launch_spectrum_rows_full(LOGN - 4, scratch, K2, H * kFsRadix, 8.f / n, st, s);
+}
+
+cudaError_t launch_spectrum_fourstep(int logn, const float2* K, float2* K2, int H, int L, float2* scratch, St st,
+                                     cudaStream_t s, bool realk) {
+  switch (logn) {
+    case 14: return fs_spec_launch<14>(K, K2, H, L, scratch, st, s, realk);
+    case 15: return fs_spec_launch<15>(K, K2, H, L, scratch, st, s, realk);
+    case 16: return fs_spec_launch<16>(K, K2, H, L, scratch, st, s, realk);
+    case 17: return fs_spec_launch<17>(K, K2, H, L, scratch, st, s, realk);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Layer path: root values Khat in column order -> K (out) and the 2M spectrum in
+// column order.  G and X: scratch of H M and H 2M complex values.
+template <int LOGM>
+static cudaError_t ks_fs_launch(const float2* Khat, float2* K, float2* K2, int H, int L, float2* G, float2* X,
+                                St st, cudaStream_t s) {
+  constexpr int M = 1 << LOGM, mi = M / kFsRadix, n = 2 * M;
+  cudaError_t e = launch_ifft_rows(LOGM - 4, Khat, G, H * kFsRadix, mi, st, s);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)(((long long)H * mi + kFsThreads - 1) / kFsThreads);
+  {
+    TimedLaunch tl("kspec_cross", s);
+    ks_cross_kernel<LOGM><<<blocks, kFsThreads, 0, s>>>(G, K, X, H, L, st);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_spectrum_rows_full(LOGM + 1 - 4, X, K2, H * kFsRadix, 8.f / n, st, s);
+}
+
+cudaError_t launch_kspec_fourstep(int logM, const float2* Khat, float2* K, float2* K2, int H, int L, float2* G,
+                                  float2* X, St st, cudaStream_t s) {
+  switch (logM) {
+    case 13: return ks_fs_launch<13>(Khat, K, K2, H, L, G, X, st, s);
+    case 14: return ks_fs_launch<14>(Khat, K, K2, H, L, G, X, st, s);
+    case 15: return ks_fs_launch<15>(Khat, K, K2, H, L, G, X, st, s);
+    case 16: return ks_fs_launch<16>(Khat, K, K2, H, L, G, X, st, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -181,7 +181,9 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
 }
 
 // Spectrum of each channel's kernel zero-padded to n = 2M, natural order, times `scale`.
-template <int LOGN>
+// FULL: rows of n values with no padding (the column spectra of the four-step
+// long-row path), every input read.
+template <int LOGN, bool FULL = false>
 __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
     const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale, int realk,
     St status) {
@@ -207,12 +209,12 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
       const int i = lt + s * T;
       float2 a[RA];
 #pragma unroll
-      for (int q = 0; q < RA / 2; ++q) {
+      for (int q = 0; q < (FULL ? RA : RA / 2); ++q) {
         const int t = i + q * NB0;
         a[q] = (act && t < L) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
         if (realk) a[q].y = 0.f;
       }
-      dft<RA, false, true>(a);
+      dft<RA, false, !FULL>(a);
 #pragma unroll
       for (int q = 0; q < RA; ++q) buf[IX0::wr(i, q)] = a[q];
     }
@@ -956,6 +958,30 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
 #undef S4_CASE
     default:
       return cudaErrorInvalidValue;
+  }
+}
+
+template <int LOGN>
+static cudaError_t spectrum_full_launch(const float2* X, float2* K2, int rows, float scale, St st,
+                                        cudaStream_t s) {
+  using C = RowCfg<LOGN>;
+  const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
+  auto k = spectrum_kernel<LOGN, true>;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_for(k, C::THREADS, smem, (rows + C::ROWS - 1) / C::ROWS);
+  TimedLaunch tl("spectrum", s);
+  return launch_maybe_pdl(k, grid, C::THREADS, smem, s, false, X, K2, rows, 1 << LOGN, scale, 0, st);
+}
+
+cudaError_t launch_spectrum_rows_full(int logn, const float2* X, float2* K2, int rows, float scale, St st,
+                                      cudaStream_t s) {
+  switch (logn) {
+    case 10: return spectrum_full_launch<10>(X, K2, rows, scale, st, s);
+    case 11: return spectrum_full_launch<11>(X, K2, rows, scale, st, s);
+    case 12: return spectrum_full_launch<12>(X, K2, rows, scale, st, s);
+    case 13: return spectrum_full_launch<13>(X, K2, rows, scale, st, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

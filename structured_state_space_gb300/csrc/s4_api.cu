@@ -99,9 +99,11 @@ bool call_status(void* ws, cudaStream_t s, s4impl::St* st, bool* chain) {
   return true;
 }
 
+// Root values in the blocked order of 2^logC (logC < 0: the order the inverse
+// transform of s4_kernel_gen reads, khat_cluster_log).
 cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
                         const s4_c32* Ct, const float* dt, int H, int N, int r, int L, void* ws,
-                        s4impl::St st, bool pdl, cudaStream_t s) {
+                        s4impl::St st, bool pdl, cudaStream_t s, int logC = -1) {
   using namespace s4impl;
   const int logM = ilog2_ceil(L);
   char* w = static_cast<char*>(ws);
@@ -109,7 +111,7 @@ cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
                        reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
                        reinterpret_cast<const float2*>(Ct), dt,
                        reinterpret_cast<float2*>(w + layout_for(H, L, 1).khat), H, N, r, 1 << logM,
-                       khat_cluster_log(logM), st, s, pdl);
+                       logC >= 0 ? logC : khat_cluster_log(logM), st, s, pdl);
 }
 
 s4_status gen_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, const s4_c32* B,
@@ -144,9 +146,12 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
     // the spectrum kernel finishes, and waits for it before reading K2
     if (e == cudaSuccess) e = launch_conv_rows(logn, u, k2, D, yf, batch, H, L, st, s, /*pdl=*/true);
   } else {
-    e = launch_spectrum_cluster(logn, Kf, k2, H, L, st, s);
+    // long rows: the four-step spectrum (column order; its scratch is the start
+    // of the convolution's, free again before the convolution writes it)
+    float2* fs = reinterpret_cast<float2*>(w + lay.fs);
+    e = launch_spectrum_fourstep(logn, Kf, k2, H, L, fs, st, s);
     if (e == cudaSuccess)
-      e = launch_conv_fourstep(logn, u, k2, D, yf, batch, H, L, reinterpret_cast<float2*>(w + lay.fs), st, s);
+      e = launch_conv_fourstep(logn, u, k2, 4, kFsSpecScale, D, yf, batch, H, L, fs, st, s);
   }
   return cuda_status(e);
 }
@@ -353,18 +358,23 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
                                    /*pdl=*/true);
     return cuda_status(e);
   }
-  if (s4impl::kspec_cluster_supported(logM)) {
-    // long rows: root values -> (K, kernel spectrum) in one clustered launch -> convolution
+  if (logM + 1 >= s4impl::kMinLogFourStep) {
+    // long rows: root values in column order -> column inverse transforms -> K
+    // (out) and the across-column step of its spectrum -> column spectra ->
+    // four-step convolution.  The spectrum's scratch (H M + 2 H M values) lies
+    // in the convolution's, which is written only after it is consumed.
     const Layout lay = layout_for(H, L, batch);
     char* w = static_cast<char*>(ws);
     float2* khat = reinterpret_cast<float2*>(w + lay.khat);
     float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
-    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s);
+    float2* fs = reinterpret_cast<float2*>(w + lay.fs);
+    cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s, /*logC=*/4);
     if (e == cudaSuccess)
-      e = s4impl::launch_kspec_cluster(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, st, s);
+      e = s4impl::launch_kspec_fourstep(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, fs,
+                                        fs + ((size_t)H << logM), st, s);
     if (e == cudaSuccess)
-      e = s4impl::launch_conv_fourstep(logM + 1, u, k2, D, reinterpret_cast<float2*>(y), batch, H, L,
-                                       reinterpret_cast<float2*>(w + lay.fs), st, s);
+      e = s4impl::launch_conv_fourstep(logM + 1, u, k2, 4, s4impl::kFsSpecScale, D, reinterpret_cast<float2*>(y),
+                                       batch, H, L, fs, st, s);
     return cuda_status(e);
   }
   const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, chain, s);

@@ -73,6 +73,10 @@ cudaError_t launch_ifft_rows(int logM, const float2* Khat, float2* K, int H, int
 // dependent of the previous kernel on the stream (waited for before any access).
 cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, int L, St st,
                                  cudaStream_t s, bool realk = false, bool pdl = false);
+// Full (unpadded) forward transforms of `rows` rows of 2^logn points (logn =
+// 10..13), natural order, times `scale`; records the call's generation.
+cudaError_t launch_spectrum_rows_full(int logn, const float2* X, float2* K2, int rows, float scale, St st,
+                                      cudaStream_t s);
 // Layer path: inverse transform of the root values and the kernel spectrum in
 // one launch (rows of M = 2^logM with 2M <= 2^13; see kspec_supported),
 // launched as a programmatic dependent of the root-value kernel.
@@ -85,22 +89,31 @@ cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const f
                              int batch, int H, int L, St st, cudaStream_t s,
                              bool pdl = false);
 
-// Layer path for M = 2^16 (kspec_cluster_supported): the inverse transform of
-// the root values (K out) and the kernel spectrum of 2M points in one launch,
-// one 8-CTA cluster per channel; K2 as from launch_spectrum_cluster.
-bool kspec_cluster_supported(int logM);
-cudaError_t launch_kspec_cluster(int logM, const float2* Khat, float2* K, float2* K2, int H, int L,
-                                 St st, cudaStream_t s);
-
 // Long-row convolution by a four-step split through global memory (2M =
 // 2^14 .. 2^17 points; K2 in the blocked order of the cluster spectrum
 // kernels): three launches, scratch of fs_scratch_bytes(logn, batch, H) bytes
 // (two complex rows of 2M points per pair of batch rows), 16-byte aligned.
 constexpr int kMinLogFourStep = 14;
 constexpr int kMaxLogFourStep = 17;
+// K2 in the blocked order of 2^k2_logC (16: column order from the four-step
+// spectrum; cluster_log(logn): from the cluster spectrum kernels), stored as
+// the spectrum times n k2_scale.
 size_t fs_scratch_bytes(int logn, int batch, int H);
-cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, const float* D, float2* y, int batch,
-                                 int H, int L, float2* scratch, St st, cudaStream_t s);
+cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, int k2_logC, float k2_scale,
+                                 const float* D, float2* y, int batch, int H, int L, float2* scratch, St st,
+                                 cudaStream_t s);
+// The four-step kernel spectrum (2M = 2^logn, 2^14..2^17) of K [H][L], in
+// column order (k2_logC = 4) scaled 1/(2 (2M/16)) = 8/(2M) (k2_scale = 1/8);
+// scratch of fs_spec_scratch_bytes(logn, H) bytes.  Records the call's generation.
+constexpr float kFsSpecScale = 0.125f;
+size_t fs_spec_scratch_bytes(int logn, int H);
+cudaError_t launch_spectrum_fourstep(int logn, const float2* K, float2* K2, int H, int L, float2* scratch, St st,
+                                     cudaStream_t s, bool realk = false);
+// Layer path, M = 2^13 .. 2^16: root values in column order (the root-value
+// kernel with logC = 4) -> K (out) and its 2M spectrum as above; G: H M and X:
+// H 2M complex scratch.
+cudaError_t launch_kspec_fourstep(int logM, const float2* Khat, float2* K, float2* K2, int H, int L, float2* G,
+                                  float2* X, St st, cudaStream_t s);
 
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,

@@ -450,3 +450,20 @@ def test_fp32_probe_runs_and_counts_flop():
     torch.cuda.synchronize()
     assert flop == 2 * 256 * 16 * 16
     assert bool(torch.isfinite(out).all())
+
+
+def test_packed_root_values_equal_scalar_bitwise():
+    # The root-value kernel takes packed fp32x2 pairs of roots on large grids and
+    # the scalar loop on small ones; both do the same per-lane operations in the
+    # same order, so one channel alone (H = 1, scalar) and the same channel
+    # repeated 64 times (packed) give identical kernels, bit for bit.
+    w = W.custom(64, 1, 1, 16384, 1, seed=4242)
+    p = W.make_params(w)
+    rep = {k: np.repeat(p[k], 64, axis=0) for k in ["Lambda", "P", "Q", "B", "Ctilde", "dt"]}
+    d1, d64 = dev(p, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt")), dev(rep, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt"))
+    K1 = s4.s4_kernel_gen(d1["Lambda"], d1["P"], d1["Q"], d1["B"], d1["Ctilde"], d1["dt"], w.L).cpu().numpy()
+    K64 = s4.s4_kernel_gen(d64["Lambda"], d64["P"], d64["Q"], d64["B"], d64["Ctilde"], d64["dt"], w.L).cpu().numpy()
+    assert np.array_equal(K1[0].view(np.uint32), K64[0].view(np.uint32))
+    assert np.array_equal(K64[0].view(np.uint32), K64[63].view(np.uint32))
+    K_ref = O.s4_kernel_channels(p, w.L, [0])
+    assert rel_l2(K1, K_ref) <= REL_K
