@@ -271,6 +271,14 @@ int  s4_timing_read(const char* name, int* launches, double* total_ms);
  * for tests of that path, not for concurrent use.  Returns S4_OK. */
 s4_status s4_set_wait_limit(int polls);
 
+/* Test aid, outside the method: in a library built with -DS4_BOUNDS_CHECK
+ * (a separate build for tests), every global and shared-memory index of the
+ * instrumented kernels is compared with its buffer's extent, and an index outside
+ * it is counted and its access skipped (nothing traps).  Returns the number counted
+ * since the library was loaded (after synchronising the device), -2 if the counters
+ * cannot be read, and -1 in the normal build, which has no checks. */
+long long s4_bounds_violations(void);
+
 /* Measurement aid, outside the method: an FP32 issue-rate probe.  Launches
  * `blocks` CTAs of 256 threads on `stream`; every thread runs `iters`
  * iterations (rounded up to a multiple of 8) of 8 independent fused

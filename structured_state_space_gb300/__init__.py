@@ -40,7 +40,7 @@ ABI_FUNCTIONS = [
     "s4_workspace_bytes", "s4_kernel_gen", "s4_conv_fwd", "s4_layer_fwd", "s4_get_status",
     "s4_status_str", "s4_timing_enable", "s4_timing_reset", "s4_timing_read",
     "s4_conv_fwd_noalloc", "s4_ctilde", "s4_recurrent_fwd", "s4_conv_fwd_real",
-    "s4_hippo_dplr", "s4_fp32_probe", "s4_set_wait_limit",
+    "s4_hippo_dplr", "s4_fp32_probe", "s4_set_wait_limit", "s4_bounds_violations",
 ]
 
 HIPPO_KINDS = {"legs": 0, "legt": 1, "lagt": 2}
@@ -61,7 +61,8 @@ def load(path: str | None = None):
     global _lib
     if _lib is not None:
         return _lib
-    p = path or LIB_PATH
+    # S4_LIB: another build of the library (the bounds-checked one, for tests)
+    p = path or os.environ.get("S4_LIB") or LIB_PATH
     if not os.path.exists(p):
         raise RuntimeError(f"libs4 not built ({p} missing): run structured_state_space_gb300.build.build()")
     lib = ctypes.CDLL(p)
@@ -96,6 +97,8 @@ def load(path: str | None = None):
     lib.s4_fp32_probe.restype = i32
     lib.s4_set_wait_limit.argtypes = [i32]
     lib.s4_set_wait_limit.restype = i32
+    lib.s4_bounds_violations.argtypes = []
+    lib.s4_bounds_violations.restype = ctypes.c_longlong
     _lib = lib
     return lib
 
@@ -318,6 +321,11 @@ def s4_set_wait_limit(polls: int) -> None:
     """Polls a kernel's bounded wait on an asynchronous copy makes before it
     reports S4_ERR_TIMEOUT (negative: the default).  A test hook."""
     _check(load().s4_set_wait_limit(int(polls)), "s4_set_wait_limit")
+
+
+def s4_bounds_violations() -> int:
+    """Out-of-extent indices counted by a bounds-checked build (-1: normal build)."""
+    return int(load().s4_bounds_violations())
 
 
 def s4_get_status(ws, stream=None) -> int:

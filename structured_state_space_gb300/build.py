@@ -35,31 +35,39 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stale(extra_deps) -> bool:
-    if not os.path.exists(LIB):
+def _stale(extra_deps, lib=LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + extra_deps
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if needed) and return the path of libs4.so."""
+CHECKED_LIB = os.path.join(LIBDIR, "libs4_checked.so")
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, bounds_check: bool = False) -> str:
+    """Compile (if needed) and return the path of libs4.so; with bounds_check,
+    the separate test build libs4_checked.so (-DS4_BOUNDS_CHECK: every index of
+    the instrumented kernels compared with its buffer's extent)."""
     deps = [os.path.join(INCLUDE, "s4.h"), os.path.abspath(__file__),
             os.path.join(PKG, "gen_twiddles.py")]
-    if not force and not _stale(deps):
-        return LIB
+    lib_path = CHECKED_LIB if bounds_check else LIB
+    objdir = os.path.join(OBJDIR, "checked") if bounds_check else OBJDIR
+    if not force and not _stale(deps, lib_path):
+        return lib_path
     os.makedirs(LIBDIR, exist_ok=True)
     os.makedirs(GENDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     sys.path.insert(0, PKG)
     import gen_twiddles
     gen_twiddles.generate(os.path.join(GENDIR, "s4_twiddles.cuh"))
     gen_twiddles.generate_tan(os.path.join(GENDIR, "s4_tan.cuh"))
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DS4_BOUNDS_CHECK"] if bounds_check else [])
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -71,14 +79,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results], "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                bounds_check="--bounds-check" in sys.argv))

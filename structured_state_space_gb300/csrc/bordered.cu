@@ -269,10 +269,9 @@ __global__ void __launch_bounds__(128) recurrent_bordered_kernel(
   bool zero[E];
   if (bordered_find<RANK, E>(Lambda + pb, alpha, N, lane, zero, bd) == 0) return;
   bordered_build<RANK, E>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, false, zero, bd);
-  float2* yr = y + (size_t)warp * L;
   float2* xr = x + (size_t)warp * N;
   if (!bd.ok) {  // s > r, or the bordered matrix is singular
-    for (int t = lane; t < L; t += 32) yr[t] = make_float2(0.f, 0.f);
+    for (int t = lane; t < L; t += 32) st_chk(y, (long long)warp * L + t, (long long)batch * H * L, make_float2(0.f, 0.f));
     for (int j = lane; j < N; j += 32) xr[j] = make_float2(0.f, 0.f);
     if (lane == 0) st_flag(status, ST_SINGULAR);
     return;
@@ -287,9 +286,8 @@ __global__ void __launch_bounds__(128) recurrent_bordered_kernel(
     cc[e] = in ? cconj(Cv[pb + j]) : make_float2(0.f, 0.f);
   }
   const float dsk = Dskip[h];
-  const float* ur = u + (size_t)warp * L;
   for (int t = 0; t < L; ++t) {
-    const float ut = ur[t];
+    const float ut = ld_chk(u, (long long)warp * L + t, (long long)batch * H * L);
     float2 b[E], wv[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) b[e] = make_float2(fmaf(2.f, xs[e].x, eb[e].x * ut), fmaf(2.f, xs[e].y, eb[e].y * ut));
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(128) recurrent_bordered_kernel(
       yp = cadd(yp, cmul(cc[e], xs[e]));
     }
     yp = warp_sum<32>(yp);
-    if (lane == 0) yr[t] = make_float2(fmaf(dsk, ut, yp.x), yp.y);
+    if (lane == 0) st_chk(y, (long long)warp * L + t, (long long)batch * H * L, make_float2(fmaf(dsk, ut, yp.x), yp.y));
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -330,7 +328,7 @@ __global__ void __launch_bounds__(128) ctilde_bordered_kernel(
   if (bordered_find<RANK, E>(Lambda + pb, alpha, N, lane, zero, bd) == 0) return;
   bordered_build<RANK, E>(Lambda + pb, Pm + pb * RANK, Qm + pb * RANK, alpha, N, lane, true, zero, bd);
   if (!bd.ok) {
-    for (int j = lane; j < N; j += 32) Ct[pb + j] = make_float2(0.f, 0.f);
+    for (int j = lane; j < N; j += 32) st_chk(Ct, (long long)pb + j, (long long)H * N, make_float2(0.f, 0.f));
     if (lane == 0) st_flag(status, ST_SINGULAR);
     return;
   }
@@ -350,7 +348,7 @@ __global__ void __launch_bounds__(128) ctilde_bordered_kernel(
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + 32 * e;
-    if (j < N) Ct[pb + j] = csub(c0[e], w[e]);
+    if (j < N) st_chk(Ct, (long long)pb + j, (long long)H * N, csub(c0[e], w[e]));
   }
 }
 
@@ -358,6 +356,10 @@ __global__ void __launch_bounds__(128) ctilde_bordered_kernel(
 
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_bordered)
+#endif
 
 // The bordered branch: one warp per sequence; E = 2 covers N <= 64, E = 8 the rest.
 template <int RANK>

@@ -28,6 +28,10 @@
 #ifndef S4_CAUCHY_UNROLL
 #define S4_CAUCHY_UNROLL 2
 #endif
+// Packed loop: the per-root denominators in scalar instructions (1) or packed (0).
+#ifndef S4_CAUCHY_SCALAR_DEN
+#define S4_CAUCHY_SCALAR_DEN 0
+#endif
 
 namespace s4dev {
 
@@ -117,8 +121,11 @@ struct CauchyLayout {
 
 // (4 roots per thread: compiled for 4 CTAs per SM, the schedule measured fastest;
 // left to itself the compiler picks a tighter, slower one)
+#ifndef S4_CAUCHY_MINB
+#define S4_CAUCHY_MINB 4
+#endif
 template <int RANK, int RPT, int T, bool PACKED = false>
-__global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
+__global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
     float2* __restrict__ Khat, int N, int logM, int logC, St status) {
@@ -149,7 +156,8 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
     pos[rr] = (blockIdx.y * RPT + rr) * T + threadIdx.x;
     const bool valid = pos[rr] < M;
     const int k = valid ? (pos[rr] % Mc) * (1 << logC) + pos[rr] / Mc : 0;
-    const float2 tt = valid ? __ldg(g_tan + (k << (16 - logM))) : make_float2(0.f, 0.f);
+    const float2 tt = (valid && S4_IN(k << (16 - logM), 65536)) ? __ldg(g_tan + (k << (16 - logM)))
+                                                                 : make_float2(0.f, 0.f);
     zm1[rr] = valid && M >= 2 && 2 * k == M;
     const float p = a_hi * tt.x;
     const float perr = fmaf(a_hi, tt.x, -p);
@@ -185,6 +193,9 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
     __syncthreads();
     for (int jj = threadIdx.x; jj < jn; jj += T) {
       const size_t j = (size_t)h * N + j0 + jj;
+      const long long nj = (long long)gridDim.x * N;  // H N
+      if (!S4_IN(j, nj) || !S4_IN((long long)j * RANK + RANK - 1, nj * RANK) || !S4_IN(jj * PS + PS - 1, JT * PS))
+        continue;
       const float2 lam = Lambda[j], b = Bv[j], c = Ct[j];
       float* pp = par + jj * PS;
       const float nre = -lam.x;
@@ -233,9 +244,17 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
         float2 dim[NPR], rn[NPR];
 #pragma unroll
         for (int pr = 0; pr < NPR; ++pr) {
+#if S4_CAUCHY_SCALAR_DEN
+          // the denominators in scalar instructions, which may issue to the FMA
+          // pipe's other half while the packed products keep the first busy
+          dim[pr] = make_float2((sh2[pr].x + nim.x) + sl2[pr].x, (sh2[pr].y + nim.y) + sl2[pr].y);
+          rn[pr] = make_float2(rcp_approx(fmaf(dim[pr].x, dim[pr].x, re2.x)),
+                               rcp_approx(fmaf(dim[pr].y, dim[pr].y, re2.y)));
+#else
           dim[pr] = __fadd2_rn(__fadd2_rn(sh2[pr], nim), sl2[pr]);
           const float2 n2 = __ffma2_rn(dim[pr], dim[pr], re2);
           rn[pr] = make_float2(rcp_approx(n2.x), rcp_approx(n2.y));
+#endif
         }
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
             res = res || (fmaf(dim, dim, lam.x * lam.x) == 0.f);
           }
           flags |= res ? ST_RES_DIAG : ST_NONFINITE;
-          Khat[(size_t)h * M + pos[rr]] = Hk;
+          st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
           continue;
         }
         float2 Wm[RANK][RANK], z[RANK];
@@ -356,7 +375,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
         }
       }
     }
-    Khat[(size_t)h * M + pos[rr]] = Hk;
+    st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
   }
   if (flags) st_flag(status, flags);
 }
@@ -365,6 +384,10 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? 4 : 0) cauchy_kernel(
 
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_cauchy)
+#endif
 
 // Build-time tuning: threads per CTA and roots per thread for rank 1 on small
 // grids (block sizes 32..256 and 2..8 roots per thread measured within 3 %).

@@ -63,7 +63,7 @@ __device__ __forceinline__ void cross_forward(cg::cluster_group& cl, float2* buf
 #pragma unroll
     for (int q = 0; q < C; ++q) {
       float2* dst = cl.map_shared_rank(buf, q);
-      dst[pad(i)] = x[q];
+      st_chk(dst, pad(i), Cf::PADM, x[q]);
     }
   }
 }
@@ -82,7 +82,7 @@ __device__ __forceinline__ void cross_inverse(cg::cluster_group& cl, float2* buf
 #pragma unroll
     for (int q = 0; q < C; ++q) {
       const float2* src = cl.map_shared_rank(buf, q);
-      x[q] = src[pad(i)];
+      x[q] = ld_chk(src, pad(i), Cf::PADM);
     }
     float2 w = tw1[il];
     w.y = -w.y;
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
   const int ncl = gridDim.x / Cf::C;
   for (int h = blockIdx.x / Cf::C; h < H; h += ncl) {
     cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int, int, int t) {
-      float2 v = t < L ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+      float2 v = (t < L && S4_IN((long long)h * L + t, (long long)H * L)) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
       if (realk) v.y = 0.f;
       return v;
     });
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) spectrum_cluster_kernel(
 #pragma unroll
       for (int q = 0; q < RB; ++q) {
         fin = fin && cfinite(a[q]);
-        K2[(size_t)h * n + (size_t)c * m + i + q * NBL] = a[q];
+        st_chk(K2, (long long)h * n + (long long)c * m + i + q * NBL, (long long)H * n, a[q]);
       }
     }
     cl.sync();
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
       const int i = lt + s * T;
       float2 a[R0];
 #pragma unroll
-      for (int q = 0; q < R0; ++q) a[q] = Khat[(size_t)h * n + (size_t)c * m + i + q * NB0];
+      for (int q = 0; q < R0; ++q) a[q] = ld_chk(Khat, (long long)h * n + (long long)c * m + i + q * NB0, (long long)H * n);
       dft<R0, true>(a);
 #pragma unroll
       for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) ifft_cluster_kernel(
     passes_rows<LOGM, true, 1, NP - 1, T, 1>(bufs, lt);
     cl.sync();
     cross_inverse<LOGN, false>(cl, buf, tw1, c, lt, [&](int, int, int t, float2 v) {
-      if (t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(v, sc);
+      if (t < L) st_chk(K, (long long)h * L + t, (long long)H * L, zero ? make_float2(0.f, 0.f) : cscale(v, sc));
     });
     cl.sync();
   }
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
     }
     const float d = D[h];
     cross_forward<LOGN>(cl, buf, tw1, c, lt, [&](int, int, int t) {
-      return make_float2(t < L ? u[(size_t)row * L + t] : 0.f, 0.f);
+      return make_float2((t < L && S4_IN((long long)row * L + t, (long long)rows * L)) ? u[(size_t)row * L + t] : 0.f, 0.f);
     });
     cl.sync();
     passes_rows<LOGM, false, 0, NP - 2, T, 1>(bufs, lt);
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
         float2 kv[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          kv[q] = K2[(size_t)h * n + (size_t)c * m + i + q * NBL];
+          kv[q] = ld_chk(K2, (long long)h * n + (long long)c * m + i + q * NBL, (long long)H * n);
           kv[q].x += d;
         }
         float2 w[RB];
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_kernel(
     passes_rows<LOGM, true, 1, NP - 1, T, 1>(bufs, lt);
     cl.sync();
     cross_inverse<LOGN, true>(cl, buf, tw1, c, lt, [&](int, int, int t, float2 v) {
-      if (t < L) y[(size_t)row * L + t] = zero ? make_float2(0.f, 0.f) : cscale(v, sc);
+      if (t < L) st_chk(y, (long long)row * L + t, (long long)rows * L, zero ? make_float2(0.f, 0.f) : cscale(v, sc));
     });
     cl.sync();
   }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN, true>::T) conv_cluster_pair_k
         const int km = c == 0 ? ((m - k) & (m - 1)) : (m - 1 - k);
         float2 kv = K2c[k];
         kv.x += d;
-        split_mul(z[s][q], zpart[pad(km)], kv, z[s][q], a1[q]);
+        split_mul(z[s][q], ld_chk(zpart, pad(km), Cf::PADM), kv, z[s][q], a1[q]);
       }
       dft<RB, true>(z[s]);
       dft<RB, true>(a1);
@@ -466,6 +466,10 @@ __global__ void __launch_bounds__(ClusterCfg<LOGN>::T) conv_cluster_real_kernel(
 
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_cluster)
+#endif
 
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_clustered(void (*kern)(KArgs...), int C, int threads, size_t smem,

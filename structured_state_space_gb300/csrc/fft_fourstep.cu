@@ -86,14 +86,15 @@ __global__ void __launch_bounds__(kFsThreads) fs_forward_kernel(const float* __r
 #pragma unroll
   for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
     const int t = m * t1 + t2;
-    x[t1] = make_float2(t < L ? __ldcs(u + q.row0 * L + t) : 0.f,
-                        (q.has1 && t < L) ? __ldcs(u + q.row1 * L + t) : 0.f);
+    const long long nu = (long long)batch * H * L;
+    x[t1] = make_float2((t < L && S4_IN(q.row0 * L + t, nu)) ? __ldcs(u + q.row0 * L + t) : 0.f,
+                        (q.has1 && t < L && S4_IN(q.row1 * L + t, nu)) ? __ldcs(u + q.row1 * L + t) : 0.f);
   }
   dft<kFsRadix, false, true>(x);
   apply_twiddles<kFsRadix>(x, fs_twiddle(t2, n));
-  float2* xp = X + (size_t)p * n + t2;
+  const long long nx = (long long)pb * H * n;
 #pragma unroll
-  for (int k1 = 0; k1 < kFsRadix; ++k1) xp[(size_t)k1 * m] = x[k1];
+  for (int k1 = 0; k1 < kFsRadix; ++k1) st_chk(X, (long long)p * n + (long long)k1 * m + t2, nx, x[k1]);
 }
 
 // Forward across-column step of the 2M-point spectrum of a complex kernel K
@@ -110,14 +111,15 @@ __global__ void __launch_bounds__(kFsThreads) fs_kfwd_kernel(const float2* __res
 #pragma unroll
   for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
     const int t = m * t1 + t2;
-    x[t1] = t < L ? __ldg(K + (size_t)h * L + t) : make_float2(0.f, 0.f);
+    x[t1] = (t < L && S4_IN((long long)h * L + t, (long long)H * L)) ? __ldg(K + (size_t)h * L + t)
+                                                                    : make_float2(0.f, 0.f);
     if (realk) x[t1].y = 0.f;
   }
   dft<kFsRadix, false, true>(x);
   apply_twiddles<kFsRadix>(x, fs_twiddle(t2, n));
-  float2* xp = X + (size_t)h * n + t2;
 #pragma unroll
-  for (int k1 = 0; k1 < kFsRadix; ++k1) xp[(size_t)k1 * m] = x[k1];
+  for (int k1 = 0; k1 < kFsRadix; ++k1)
+    st_chk(X, (long long)h * n + (long long)k1 * m + t2, (long long)H * n, x[k1]);
 }
 
 // Layer path: K from the column inverse transforms G[h][k1][t2] (M/16 points
@@ -137,7 +139,9 @@ __global__ void __launch_bounds__(kFsThreads) ks_cross_kernel(const float2* __re
   float2 g[kFsRadix];
   const float2* gp = G + (size_t)h * M + t2;
 #pragma unroll
-  for (int k1 = 0; k1 < kFsRadix; ++k1) g[k1] = __ldcs(gp + (size_t)k1 * mi);
+  for (int k1 = 0; k1 < kFsRadix; ++k1)
+    g[k1] = S4_IN((long long)h * M + (long long)k1 * mi + t2, (long long)H * M) ? __ldcs(gp + (size_t)k1 * mi)
+                                                                               : make_float2(0.f, 0.f);
   float2 w = fs_twiddle(t2, M);
   w.y = -w.y;
   apply_twiddles<kFsRadix>(g, w);
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kFsThreads) ks_cross_kernel(const float2* __re
   for (int t1 = 0; t1 < kFsRadix; ++t1) {
     const int t = mi * t1 + t2;
     const float2 v = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(g[t1], 1.f / kFsRadix);
-    if (t < L) K[(size_t)h * L + t] = v;
+    if (t < L) st_chk(K, (long long)h * L + t, (long long)H * L, v);
     if (t1 % 2 == 0) xa[t1 / 2] = v;
     else xb[t1 / 2] = v;
   }
@@ -155,11 +159,10 @@ __global__ void __launch_bounds__(kFsThreads) ks_cross_kernel(const float2* __re
   dft<kFsRadix, false, true>(xb);
   apply_twiddles<kFsRadix>(xa, fs_twiddle(t2, n));
   apply_twiddles<kFsRadix>(xb, fs_twiddle(t2 + mi, n));
-  float2* xp = X + (size_t)h * n + t2;
 #pragma unroll
   for (int k1 = 0; k1 < kFsRadix; ++k1) {
-    xp[(size_t)k1 * mf] = xa[k1];
-    xp[(size_t)k1 * mf + mi] = xb[k1];
+    st_chk(X, (long long)h * n + (long long)k1 * mf + t2, (long long)H * n, xa[k1]);
+    st_chk(X, (long long)h * n + (long long)k1 * mf + mi + t2, (long long)H * n, xb[k1]);
   }
 }
 
@@ -176,10 +179,12 @@ __global__ void __launch_bounds__(kFsThreads) fs_inverse_kernel(const float2* __
   const bool zero = st_bad(status);
   float2 a[kFsRadix], c[kFsRadix];
   const size_t base = (size_t)p * n + t2;
+  const long long nx = (long long)pb * H * n;
 #pragma unroll
   for (int k1 = 0; k1 < kFsRadix; ++k1) {
-    a[k1] = __ldcs(Ar + base + (size_t)k1 * m);
-    c[k1] = __ldcs(Ci + base + (size_t)k1 * m);
+    const bool in = S4_IN((long long)base + (long long)k1 * m, nx);
+    a[k1] = in ? __ldcs(Ar + base + (size_t)k1 * m) : make_float2(0.f, 0.f);
+    c[k1] = in ? __ldcs(Ci + base + (size_t)k1 * m) : make_float2(0.f, 0.f);
   }
   float2 w = fs_twiddle(t2, n);
   w.y = -w.y;
@@ -190,9 +195,12 @@ __global__ void __launch_bounds__(kFsThreads) fs_inverse_kernel(const float2* __
 #pragma unroll
   for (int t1 = 0; t1 < kFsRadix / 2; ++t1) {
     const int t = m * t1 + t2;
+    const long long ny = (long long)batch * H * L;
     if (t < L) {
-      __stcs(y + q.row0 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].x, c[t1].x));
-      if (q.has1) __stcs(y + q.row1 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].y, c[t1].y));
+      if (S4_IN(q.row0 * L + t, ny))
+        __stcs(y + q.row0 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].x, c[t1].x));
+      if (q.has1 && S4_IN(q.row1 * L + t, ny))
+        __stcs(y + q.row1 * L + t, zero ? make_float2(0.f, 0.f) : make_float2(a[t1].y, c[t1].y));
     }
   }
 }
@@ -213,7 +221,8 @@ struct FsColCfg {
 // K^ at natural bin k from the blocked layout of a cluster of 2^logC CTAs.
 __device__ __forceinline__ float2 fs_spec(const float2* __restrict__ K2h, int k, int n, int logC) {
   const int C = 1 << logC;
-  return __ldcg(K2h + (size_t)(k & (C - 1)) * (n >> logC) + (k >> logC));
+  const long long i = (long long)(k & (C - 1)) * (n >> logC) + (k >> logC);
+  return S4_IN(i, n) ? __ldcg(K2h + i) : make_float2(0.f, 0.f);
 }
 
 // 512 threads per SM at 128 registers (one CTA for m = 8192, more for shorter columns)
@@ -255,10 +264,12 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       const int i = lt + s * T;
       float2 a[RA];
 #pragma unroll
-      for (int qq = 0; qq < RA; ++qq) a[qq] = act ? __ldcs(xc + i + qq * NB0) : make_float2(0.f, 0.f);
+      for (int qq = 0; qq < RA; ++qq)
+        a[qq] = (act && S4_IN((long long)p * n + (long long)k1 * m + i + qq * NB0, (long long)pb * H * n))
+                    ? __ldcs(xc + i + qq * NB0) : make_float2(0.f, 0.f);
       dft<RA, false>(a);
 #pragma unroll
-      for (int qq = 0; qq < RA; ++qq) bufA[IXF0::wr(i, qq)] = a[qq];
+      for (int qq = 0; qq < RA; ++qq) st_chk(bufA, IXF0::wr(i, qq), C::PADM, a[qq]);
     }
     __syncthreads();
     passes_rows<LOGM, false, 1, NP - 2, T, 1>(buf1, lt);
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       const int i = lt + s * T;
       float2 z[RB], w[RB];
 #pragma unroll
-      for (int qq = 0; qq < RB; ++qq) z[qq] = bufA[IXFL::rd(i, qq)];
+      for (int qq = 0; qq < RB; ++qq) z[qq] = ld_chk(bufA, IXFL::rd(i, qq), C::PADM);
       TWFL::load(w, i);
       TWFL::apply(z, w);
       dft<RB, false>(z);
@@ -289,14 +300,14 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       dft<RB, true>(pa[s]);
       dft<RB, true>(pc[s]);
 #pragma unroll
-      for (int qq = 0; qq < RB; ++qq) bufB[IXI0::wr(i, qq)] = pc[s][qq];
+      for (int qq = 0; qq < RB; ++qq) st_chk(bufB, IXI0::wr(i, qq), C::PADM, pc[s][qq]);
     }
     __syncthreads();  // every thread has read its last forward pass from bufA
 #pragma unroll
     for (int s = 0; s < PERL; ++s) {
       const int i = lt + s * T;
 #pragma unroll
-      for (int qq = 0; qq < RB; ++qq) bufA[IXI0::wr(i, qq)] = pa[s][qq];
+      for (int qq = 0; qq < RB; ++qq) st_chk(bufA, IXI0::wr(i, qq), C::PADM, pa[s][qq]);
     }
     __syncthreads();
     passes_rows<LOGM, true, 1, NP - 2, T, 2>(buf2, lt);
@@ -307,8 +318,8 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       float2 a[RA], c[RA], w[RA];
 #pragma unroll
       for (int qq = 0; qq < RA; ++qq) {
-        a[qq] = bufA[IXIL::rd(i, qq)];
-        c[qq] = bufB[IXIL::rd(i, qq)];
+        a[qq] = ld_chk(bufA, IXIL::rd(i, qq), C::PADM);
+        c[qq] = ld_chk(bufB, IXIL::rd(i, qq), C::PADM);
       }
       TWIL::load(w, i);
       TWIL::apply(a, w);
@@ -318,6 +329,7 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       if (act) {
 #pragma unroll
         for (int qq = 0; qq < RA; ++qq) {
+          if (!S4_IN((long long)p * n + (long long)k1 * m + i + qq * NB0, (long long)pb * H * n)) continue;
           xc[i + qq * NB0] = zero ? make_float2(0.f, 0.f) : a[qq];
           cc[i + qq * NB0] = zero ? make_float2(0.f, 0.f) : c[qq];
         }
@@ -331,6 +343,10 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
 
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_fourstep)
+#endif
 
 size_t fs_scratch_bytes(int logn, int batch, int H) {
   if (logn < kMinLogFourStep || logn > kMaxLogFourStep) return 0;

@@ -154,10 +154,11 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
       float2 a[R0];
 #pragma unroll
       for (int q = 0; q < R0; ++q)
-        a[q] = act ? __ldcg(Khat + (size_t)h * n + i + q * NB0) : make_float2(0.f, 0.f);
+        a[q] = (act && S4_IN((long long)h * n + i + q * NB0, (long long)H * n))
+                   ? __ldcg(Khat + (size_t)h * n + i + q * NB0) : make_float2(0.f, 0.f);
       dft<R0, true>(a);
 #pragma unroll
-      for (int q = 0; q < R0; ++q) buf[IX0::wr(i, q)] = a[q];
+      for (int q = 0; q < R0; ++q) st_chk(buf, IX0::wr(i, q), C::PADN, a[q]);
     }
     __syncthreads();
     passes_rows<LOGN, true, 1, NP - 2, T, 1>(bufs, lt);
@@ -166,14 +167,14 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
       const int i = lt + s * T;
       float2 a[RL], w[RL];
 #pragma unroll
-      for (int q = 0; q < RL; ++q) a[q] = buf[IXL::rd(i, q)];
+      for (int q = 0; q < RL; ++q) a[q] = ld_chk(buf, IXL::rd(i, q), C::PADN);
       TWL::load(w, i);
       TWL::apply(a, w);
       dft<RL, true>(a);
 #pragma unroll
       for (int q = 0; q < RL; ++q) {
         const int t = i + q * NBL;
-        if (act && t < L) K[(size_t)h * L + t] = zero ? make_float2(0.f, 0.f) : cscale(a[q], sc);
+        if (act && t < L) st_chk(K, (long long)h * L + t, (long long)H * L, zero ? make_float2(0.f, 0.f) : cscale(a[q], sc));
       }
     }
     __syncthreads();
@@ -211,12 +212,13 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
 #pragma unroll
       for (int q = 0; q < (FULL ? RA : RA / 2); ++q) {
         const int t = i + q * NB0;
-        a[q] = (act && t < L) ? K[(size_t)h * L + t] : make_float2(0.f, 0.f);
+        a[q] = (act && t < L && S4_IN((long long)h * L + t, (long long)H * L)) ? K[(size_t)h * L + t]
+                                                                             : make_float2(0.f, 0.f);
         if (realk) a[q].y = 0.f;
       }
       dft<RA, false, !FULL>(a);
 #pragma unroll
-      for (int q = 0; q < RA; ++q) buf[IX0::wr(i, q)] = a[q];
+      for (int q = 0; q < RA; ++q) st_chk(buf, IX0::wr(i, q), C::PADN, a[q]);
     }
     __syncthreads();
     passes_rows<LOGN, false, 1, NP - 2, T, 1>(bufs, lt);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
       const int i = lt + s * T;
       float2 a[RB], w[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) a[q] = buf[IXL::rd(i, q)];
+      for (int q = 0; q < RB; ++q) a[q] = ld_chk(buf, IXL::rd(i, q), C::PADN);
       TWL::load(w, i);
       TWL::apply(a, w);
       dft<RB, false>(a);
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           fin = fin && cfinite(a[q]);
-          K2[(size_t)h * n + i + q * NBL] = cscale(a[q], scale);
+          st_chk(K2, (long long)h * n + i + q * NBL, (long long)H * n, cscale(a[q], scale));
         }
       }
     }
@@ -391,6 +393,9 @@ conv_pair_kernel(
     const int hq = q % H, bq = 2 * (q / H);
     const unsigned bytes = (unsigned)L * 4u;
     const bool two = bq + 1 < batch;
+    // (checked build: the rows fit their halves of the stage and of u)
+    (void)S4_IN(L - 1, n);
+    (void)S4_IN(((long long)bq * H + hq + (two ? H : 0)) * L + L - 1, (long long)batch * H * L);
     fence_proxy_async();
     mbar_expect_tx(&bar, two ? 2u * bytes : bytes);
     const size_t r0 = (size_t)bq * H + hq;
@@ -435,14 +440,17 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
+        const long long nu = (long long)batch * H * L;
         if (u_staged)
-          a[q] = make_float2(t < L ? stage_f[t] : 0.f, (has1 && t < L) ? stage_f[n + t] : 0.f);
+          a[q] = make_float2((t < L && S4_IN(t, 2 * n)) ? stage_f[t] : 0.f,
+                             (has1 && t < L && S4_IN(n + t, 2 * n)) ? stage_f[n + t] : 0.f);
         else
-          a[q] = make_float2((act && t < L) ? u[row0 * L + t] : 0.f, (has1 && t < L) ? u[row1 * L + t] : 0.f);
+          a[q] = make_float2((act && t < L && S4_IN(row0 * L + t, nu)) ? u[row0 * L + t] : 0.f,
+                             (has1 && t < L && S4_IN(row1 * L + t, nu)) ? u[row1 * L + t] : 0.f);
       }
       dft<RA, false, true>(a);
 #pragma unroll
-      for (int q = 0; q < RA; ++q) bufA[IXF0::wr(i, q)] = a[q];
+      for (int q = 0; q < RA; ++q) st_chk(bufA, IXF0::wr(i, q), C::PADN, a[q]);
     }
     if constexpr (STAGE) {
       stall = __syncthreads_or(stall || !got_u);
@@ -464,7 +472,7 @@ conv_pair_kernel(
       const int i = last_bfly<T, NBL, PERL>(sl, lt);
       float2 w[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) z[sl][q] = bufA[IXFL::rd(i, q)];
+      for (int q = 0; q < RB; ++q) z[sl][q] = ld_chk(bufA, IXFL::rd(i, q), C::PADN);
       TWFL::load(w, i);
       TWFL::apply(z[sl], w);
       dft<RB, false>(z[sl]);
@@ -489,8 +497,11 @@ conv_pair_kernel(
         float2 kA[RB], kB[RB], a1A[RB], a1B[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          kA[q] = k_staged ? Kr[iA + q * NBL] : __ldcg(K2h + iA + q * NBL);
-          kB[q] = k_staged ? Kr[iB + q * NBL] : __ldcg(K2h + iB + q * NBL);
+          const long long nk = (long long)H * n, ha = (long long)h * n;
+          kA[q] = !S4_IN(ha + iA + q * NBL, nk) ? make_float2(0.f, 0.f)
+                  : k_staged ? ld_chk(Kr, iA + q * NBL, n) : __ldcg(K2h + iA + q * NBL);
+          kB[q] = !S4_IN(ha + iB + q * NBL, nk) ? make_float2(0.f, 0.f)
+                  : k_staged ? ld_chk(Kr, iB + q * NBL, n) : __ldcg(K2h + iB + q * NBL);
           kA[q].x += dk;
           kB[q].x += dk;
         }
@@ -526,8 +537,8 @@ conv_pair_kernel(
         dft<RB, true>(a1B);
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-          bufB[IXI0::wr(iA, q)] = a1A[q];
-          bufB[IXI0::wr(iB, q)] = a1B[q];
+          st_chk(bufB, IXI0::wr(iA, q), C::PADN, a1A[q]);
+          st_chk(bufB, IXI0::wr(iB, q), C::PADN, a1B[q]);
         }
         dft<RB, true>(zA);
         dft<RB, true>(zB);
@@ -544,7 +555,7 @@ conv_pair_kernel(
       for (int sl = 0; sl < PERL; ++sl) {
         const int i = last_bfly<T, NBL, PERL>(sl, lt);
 #pragma unroll
-        for (int q = 0; q < RB; ++q) bufB[IXFL::rd(i, q)] = z[sl][q];
+        for (int q = 0; q < RB; ++q) st_chk(bufB, IXFL::rd(i, q), C::PADN, z[sl][q]);
       }
       __syncthreads();
       float2 a1[PERL][RB];
@@ -554,9 +565,10 @@ conv_pair_kernel(
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           const int k = i + q * NBL;
-          float2 kv = k_staged ? Kr[k] : __ldcg(K2h + k);
+          float2 kv = !S4_IN((long long)h * n + k, (long long)H * n) ? make_float2(0.f, 0.f)
+                      : k_staged ? ld_chk(Kr, k, n) : __ldcg(K2h + k);
           kv.x += dk;
-          split_mul(z[sl][q], bufB[pad((n - k) & (n - 1))], kv, a0[sl][q], a1[sl][q]);
+          split_mul(z[sl][q], ld_chk(bufB, pad((n - k) & (n - 1)), C::PADN), kv, a0[sl][q], a1[sl][q]);
         }
         dft<RB, true>(a0[sl]);
         dft<RB, true>(a1[sl]);
@@ -571,7 +583,7 @@ conv_pair_kernel(
       for (int sl = 0; sl < PERL; ++sl) {
         const int i = last_bfly<T, NBL, PERL>(sl, lt);
 #pragma unroll
-        for (int q = 0; q < RB; ++q) bufB[IXI0::wr(i, q)] = a1[sl][q];
+        for (int q = 0; q < RB; ++q) st_chk(bufB, IXI0::wr(i, q), C::PADN, a1[sl][q]);
       }
     }
     if (stall) zero = true;
@@ -579,7 +591,7 @@ conv_pair_kernel(
     for (int sl = 0; sl < PERL; ++sl) {
       const int i = last_bfly<T, NBL, PERL>(sl, lt);
 #pragma unroll
-      for (int q = 0; q < RB; ++q) bufA[IXI0::wr(i, q)] = a0[sl][q];
+      for (int q = 0; q < RB; ++q) st_chk(bufA, IXI0::wr(i, q), C::PADN, a0[sl][q]);
     }
     __syncthreads();
     passes_rows<LOGN, true, 1, NP - 2, T, 2>(buf2, lt);
@@ -590,8 +602,8 @@ conv_pair_kernel(
       float2 c0[RA], c1[RA], w[RA];
 #pragma unroll
       for (int q = 0; q < RA; ++q) {
-        c0[q] = bufA[IXIL::rd(i, q)];
-        c1[q] = bufB[IXIL::rd(i, q)];
+        c0[q] = ld_chk(bufA, IXIL::rd(i, q), C::PADN);
+        c1[q] = ld_chk(bufB, IXIL::rd(i, q), C::PADN);
       }
       TWIL::load(w, i);
       TWIL::apply(c0, w);
@@ -601,9 +613,10 @@ conv_pair_kernel(
 #pragma unroll
       for (int q = 0; q < RA / 2; ++q) {
         const int t = i + q * NB0;
+        const long long ny = (long long)batch * H * L;
         if (t < L) {
-          if (act) __stcs(y + row0 * L + t, zero ? make_float2(0.f, 0.f) : c0[q]);
-          if (has1) __stcs(y + row1 * L + t, zero ? make_float2(0.f, 0.f) : c1[q]);
+          if (act && S4_IN(row0 * L + t, ny)) __stcs(y + row0 * L + t, zero ? make_float2(0.f, 0.f) : c0[q]);
+          if (has1 && S4_IN(row1 * L + t, ny)) __stcs(y + row1 * L + t, zero ? make_float2(0.f, 0.f) : c1[q]);
         }
       }
     }
@@ -760,6 +773,10 @@ conv_real_pair_kernel(const float* __restrict__ u, const float2* __restrict__ K2
 // ----------------------------------------------------------------------------
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_rows)
+#endif
 
 template <typename KernelT>
 static cudaError_t prepare(KernelT k, size_t smem) {

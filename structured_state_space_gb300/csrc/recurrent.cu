@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     const int j = lane + G * e;
     const bool in = j < N;
     const float2 di = cc.dinv[e];  // zero outside the states
-    xs[e] = in ? x[(size_t)warp * N + j] : make_float2(0.f, 0.f);
+    xs[e] = in ? ld_chk(x, (long long)warp * N + j, (long long)batch * H * N) : make_float2(0.f, 0.f);
     eb[e] = in ? cscale(cmul(di, Bv[pb + j]), delta) : make_float2(0.f, 0.f);
     av[e] = in ? make_float2(fmaf(2.f, di.x, -1.f), 2.f * di.y) : make_float2(0.f, 0.f);
     cc_[e] = in ? cconj(Cv[pb + j]) : make_float2(0.f, 0.f);
@@ -207,8 +207,6 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
 #pragma unroll
   for (int l = 0; l < RANK; ++l) c0[l] = warp_sum<G>(c0[l]);
   const float dsk = Dskip[h];
-  const float* ur = u + (size_t)warp * L;
-  float2* yr = y + (size_t)warp * L;
   float2 s[RANK];  // this lane's part of sum_j h_j x_j for the coming step
 #pragma unroll
   for (int l = 0; l < RANK; ++l) {
@@ -223,7 +221,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
   const int ylane = JOINT ? 8 : 0;  // the lane that holds the summed output
 #pragma unroll kRecurrentUnroll
   for (int t = 0; t < L; ++t) {
-    const float ut = ur[t];
+    const float ut = ld_chk(u, (long long)warp * L + t, (long long)batch * H * L);
     float2 z[RANK];
 #pragma unroll
     for (int l = 0; l < RANK; ++l) {
@@ -255,12 +253,14 @@ __global__ void __launch_bounds__(128) recurrent_kernel(
     } else {
       yp = warp_sum<G>(yp);
     }
-    if (mine && lane == ylane) yr[t] = ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f);
+    if (mine && lane == ylane)
+      st_chk(y, (long long)warp * L + t, (long long)batch * H * L,
+             ok ? make_float2(fmaf(dsk, ut, yp.x), yp.y) : make_float2(0.f, 0.f));
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
-    if (mine && j < N) x[(size_t)warp * N + j] = ok ? xs[e] : make_float2(0.f, 0.f);
+    if (mine && j < N) st_chk(x, (long long)warp * N + j, (long long)batch * H * N, ok ? xs[e] : make_float2(0.f, 0.f));
   }
   if (mine && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = lane + G * e;
-    if (mine && j < N) Ct[pb + j] = ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f);
+    if (mine && j < N) st_chk(Ct, (long long)pb + j, (long long)H * N, ok ? csub(c0[e], w[e]) : make_float2(0.f, 0.f));
   }
   if (mine && lane == 0 && !ok) st_flag(status, bad ? ST_BAD_STEP : ST_SINGULAR);
 }
@@ -414,6 +414,10 @@ __global__ void __launch_bounds__(128) ctilde_kernel(
 
 namespace s4impl {
 using namespace s4dev;
+
+#ifdef S4_BOUNDS_CHECK
+S4_OOB_COUNTER(oob_recurrent)
+#endif
 
 template <int RANK, int E, int G>
 static cudaError_t rec_launch(const float2* Lam, const float2* P, const float2* Q, const float2* B,

@@ -254,6 +254,22 @@ s4_status s4_fp32_probe(float* out, int blocks, int iters, void* stream) {
   return cudaGetLastError() == cudaSuccess ? S4_OK : S4_ERR_CUDA;
 }
 
+long long s4_bounds_violations(void) {
+#ifdef S4_BOUNDS_CHECK
+  if (cudaDeviceSynchronize() != cudaSuccess) return -2;
+  const unsigned long long c[] = {s4impl::oob_rows(), s4impl::oob_cluster(), s4impl::oob_fourstep(),
+                                  s4impl::oob_cauchy(), s4impl::oob_recurrent(), s4impl::oob_bordered()};
+  unsigned long long t = 0;
+  for (unsigned long long v : c) {
+    if (v == ~0ull) return -2;
+    t += v;
+  }
+  return (long long)t;
+#else
+  return -1;
+#endif
+}
+
 s4_status s4_set_wait_limit(int polls) {
   s4impl::g_wait_limit.store(polls >= 0 ? polls : s4dev::kMbarWaitLimit, std::memory_order_relaxed);
   return S4_OK;

@@ -22,6 +22,44 @@ constexpr unsigned ST_BAD_STEP = 8u;   // Delta <= 0 or not finite
 constexpr unsigned ST_SINGULAR = 16u;  // G = I - (Delta/2) A not solved (zero d_j or singular W)
 constexpr unsigned ST_STALL = 32u;     // a bounded wait on an asynchronous copy ran out
 
+// ---- bounds-checked build -------------------------------------------------------
+// With -DS4_BOUNDS_CHECK (a separate library, built for tests) every global and
+// shared-memory index of the instrumented kernels is compared with the extent of
+// its buffer; an index outside it is counted in this translation unit's device
+// counter and the access is skipped (a load gives zero).  No trap: the counter is
+// read by the host (s4_bounds_violations) after the kernels ran.  In the normal
+// build S4_IN is `true` and the helpers are plain accesses.
+#ifdef S4_BOUNDS_CHECK
+static __device__ unsigned long long g_s4_oob;
+static __device__ __noinline__ void s4_oob_hit() { atomicAdd(&g_s4_oob, 1ull); }
+static __device__ __forceinline__ bool s4_in(long long i, long long n) {
+  const bool ok = i >= 0 && i < n;
+  if (!ok) s4_oob_hit();
+  return ok;
+}
+#define S4_IN(i, n) ::s4dev::s4_in((long long)(i), (long long)(n))
+// host side: this translation unit's counter (defines a function `name`)
+#define S4_OOB_COUNTER(name)                                                   \
+  unsigned long long name() {                                                  \
+    unsigned long long v = 0;                                                  \
+    if (cudaMemcpyFromSymbol(&v, ::s4dev::g_s4_oob, sizeof(v)) != cudaSuccess) \
+      return ~0ull;                                                            \
+    return v;                                                                  \
+  }
+#else
+#define S4_IN(i, n) true
+#endif
+
+// checked loads and stores: p[i] with 0 <= i < n
+template <typename T>
+__device__ __forceinline__ T ld_chk(const T* p, long long i, long long n) {
+  return S4_IN(i, n) ? p[i] : T{};
+}
+template <typename T>
+__device__ __forceinline__ void st_chk(T* p, long long i, long long n, T v) {
+  if (S4_IN(i, n)) p[i] = v;
+}
+
 // ---- complex helpers ----------------------------------------------------------
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 __device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }

@@ -91,7 +91,7 @@ __device__ __forceinline__ void pass_rows(float2* const* bufs, int lt, const flo
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-      for (int q = 0; q < R; ++q) a[r][s][q] = bufs[r][IX::rd(i, q)];
+      for (int q = 0; q < R; ++q) a[r][s][q] = ld_chk(bufs[r], IX::rd(i, q), padded_len(N));
     if constexpr (P > 1) {
       float2 w[R];
       TW::template load<STW>(w, i & (P - 1), STW ? twsm + TW::REL : nullptr);
@@ -110,7 +110,7 @@ __device__ __forceinline__ void pass_rows(float2* const* bufs, int lt, const flo
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-      for (int q = 0; q < R; ++q) bufs[r][IX::wr(i, q)] = a[r][s][q];
+      for (int q = 0; q < R; ++q) st_chk(bufs[r], IX::wr(i, q), padded_len(N), a[r][s][q]);
   }
   }
   __syncthreads();

@@ -15,6 +15,16 @@ struct St {
   unsigned gen;
 };
 
+#ifdef S4_BOUNDS_CHECK
+// Out-of-extent indices counted by each translation unit's kernels (checked build).
+unsigned long long oob_rows();
+unsigned long long oob_cluster();
+unsigned long long oob_fourstep();
+unsigned long long oob_cauchy();
+unsigned long long oob_recurrent();
+unsigned long long oob_bordered();
+#endif
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 

@@ -73,10 +73,11 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       const int i = lt + s * TI;
       float2 a[RI0];
 #pragma unroll
-      for (int q = 0; q < RI0; ++q) a[q] = act ? __ldcg(khat + i + q * NBI0) : make_float2(0.f, 0.f);
+      for (int q = 0; q < RI0; ++q)
+        a[q] = (act && S4_IN(i + q * NBI0, M)) ? __ldcg(khat + i + q * NBI0) : make_float2(0.f, 0.f);
       dft<RI0, true>(a);
 #pragma unroll
-      for (int q = 0; q < RI0; ++q) buf[IXI0::wr(i, q)] = a[q];
+      for (int q = 0; q < RI0; ++q) st_chk(buf, IXI0::wr(i, q), padded_len(n), a[q]);
     }
   }
   __syncthreads();
@@ -94,7 +95,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       const int i = lt + s * TI;
       float2 w[RIL];
 #pragma unroll
-      for (int q = 0; q < RIL; ++q) kv[s][q] = buf[IXIL::rd(i, q)];
+      for (int q = 0; q < RIL; ++q) kv[s][q] = ld_chk(buf, IXIL::rd(i, q), padded_len(n));
       TWIL::template load<STW>(w, i, STW ? twi + TWIL::REL : nullptr);
       TWIL::apply(kv[s], w);
       dft<RIL, true>(kv[s]);
@@ -109,8 +110,8 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       for (int q = 0; q < RIL; ++q) {
         const int t = i + q * NBIL;
         const float2 v = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(kv[s][q], sc);
-        if (act && t < L) Krow[t] = v;
-        buf[pad(t)] = v;
+        if (act && t < L) st_chk(Krow, t, L, v);
+        st_chk(buf, pad(t), padded_len(n), v);
       }
     }
   }
@@ -122,7 +123,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       for (int s = 0; s < PER0; ++s) {
         const int i = lt + s * T;
 #pragma unroll
-        for (int q = 0; q < RA / 2; ++q) a[s][q] = buf[pad(i + q * NB0)];
+        for (int q = 0; q < RA / 2; ++q) a[s][q] = ld_chk(buf, pad(i + q * NB0), padded_len(n));
         dft<RA, false, true>(a[s]);
       }
     }
@@ -132,7 +133,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       for (int s = 0; s < PER0; ++s) {
         const int i = lt + s * T;
 #pragma unroll
-        for (int q = 0; q < RA; ++q) buf[IXF0::wr(i, q)] = a[s][q];
+        for (int q = 0; q < RA; ++q) st_chk(buf, IXF0::wr(i, q), padded_len(n), a[s][q]);
       }
     }
     __syncthreads();
@@ -144,7 +145,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
       const int i = lt + s * T;
       float2 a[RB], w[RB];
 #pragma unroll
-      for (int q = 0; q < RB; ++q) a[q] = buf[IXFL::rd(i, q)];
+      for (int q = 0; q < RB; ++q) a[q] = ld_chk(buf, IXFL::rd(i, q), padded_len(n));
       TWFL::template load<STW>(w, i, STW ? twf + TWFL::REL : nullptr);
       TWFL::apply(a, w);
       dft<RB, false>(a);
@@ -152,7 +153,7 @@ __device__ __forceinline__ void kspec_row(const float2* __restrict__ khat, float
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           fin = fin && cfinite(a[q]);
-          K2row[i + q * NBL] = cscale(a[q], scale);
+          st_chk(K2row, i + q * NBL, n, cscale(a[q], scale));
         }
       }
     }
