@@ -49,11 +49,52 @@ FP32_LANES_PER_SM = 128
 
 
 def cauchy_flop(r):
-    """Algorithmic flop per (channel, root, pole) term of the root-value sums:
-    8 (r+1)^2 for the complex multiply-adds of the (r+1)^2 weighted
+    """Algorithmic flop per (channel, root, pole) term of the direct root-value
+    sums: 8 (r+1)^2 for the complex multiply-adds of the (r+1)^2 weighted
     reciprocals, plus 10 for the denominator s - lambda_j and its reciprocal
     (42 at rank 1, 82 at rank 2)."""
     return 8 * (r + 1) ** 2 + 10
+
+
+FAR_TERMS = 24  # terms of the far-root series (the library's kFarTerms)
+
+
+def cauchy_work(p, w, sms):
+    """The root-value kernel's algorithmic flop for one call, as it splits the
+    roots: a CTA of consecutive roots with any root near its channel's poles
+    (|s - c| < 2 R) sums directly over the N poles (cauchy_flop per pole and
+    root, for every root of the CTA); the other roots evaluate the series,
+    (r+1)^2 (FAR_TERMS - 1) complex multiply-adds of 8 flop plus ~24 flop of
+    set-up each.  The split is replayed here in float64 from the parameters
+    (the kernel decides in fp32; the two can differ only at a CTA on the
+    boundary).  Returns (flop, fraction of roots summed directly)."""
+    import numpy as np
+    H, N, r, M = w.H, w.N, w.r, w.M
+    nw = (r + 1) ** 2
+    if M < 8192 or N < 48:  # the library takes the series only on rows of M >= 8192 roots, N >= 48 poles
+        return H * M * N * cauchy_flop(r), 1.0
+    big = H * M >= 512 * 5 * 2 * sms
+    cta = 128 * (4 if (big and r <= 2) else (2 if r <= 2 else 1))
+    k = np.arange(M)
+    t = np.tan(np.pi * k / M)
+    direct_roots = 0
+    for h in range(H):
+        lam = p["Lambda"][h].astype(np.complex128)
+        c = 0.5 * (lam.real.min() + lam.real.max()) + 0.5j * (lam.imag.min() + lam.imag.max())
+        R = np.abs(lam - c).max() or 1.0
+        a = 2.0 / float(p["dt"][h])
+        u = 1j * a * t - c
+        far = np.abs(u) ** 2 >= 4 * R * R
+        if M >= 2:
+            far[M // 2] = True
+        nb = -(-M // cta)
+        pad = np.ones(nb * cta, bool)
+        pad[:M] = far
+        direct_roots += int((~pad.reshape(nb, cta).all(axis=1)).sum()) * cta
+    direct_roots = min(direct_roots, H * M)
+    far_roots = H * M - direct_roots
+    flop = direct_roots * N * cauchy_flop(r) + far_roots * (nw * (FAR_TERMS - 1) * 8 + 24)
+    return flop, direct_roots / (H * M)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -416,8 +457,8 @@ def run_ours(args):
     ms_prof = timed(prof_steps, S)
     s4.timing.enable(False)
     ms_prof -= timed(head_start, 0)
-    fams = ["cauchy", "ifft", "kspec_cross", "spectrum", "spec_fwd", "kspec", "conv", "conv_fwd", "conv_col",
-            "conv_inv"]
+    fams = ["moments", "cauchy", "ifft", "kspec_cross", "spectrum", "spec_fwd", "kspec", "conv", "conv_fwd",
+            "conv_col", "conv_inv"]
     raw = {}
     for name in fams:
         n, t = s4.timing.read(name)
@@ -429,7 +470,7 @@ def run_ours(args):
     # K, and the column spectra) and the convolution (one launch on short rows;
     # on long rows the across-column step, the column transforms and the inverse
     # across-column step); a part's time is the sum of its launches per step
-    groups = {"cauchy": ["cauchy"], "kspec": ["kspec", "ifft", "kspec_cross", "spectrum", "spec_fwd"],
+    groups = {"cauchy": ["cauchy", "moments"], "kspec": ["kspec", "ifft", "kspec_cross", "spectrum", "spec_fwd"],
               "conv": ["conv", "conv_fwd", "conv_col", "conv_inv"]}
     kern = {}
     for g, members in groups.items():
@@ -494,8 +535,11 @@ def run_ours(args):
     peak_source = f"{sms} SMs (queried) x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x max SM clock"
     lg2m = (2 * M).bit_length() - 1
     # algorithmic work per launch of each kernel family: (bound, amount, description)
+    cflop, direct_frac = cauchy_work(p, w, sms)
     work = {
-        "cauchy": ("alu", H * M * N * cauchy_flop(r), f"{cauchy_flop(r)} flop per (channel, root, pole)"),
+        "cauchy": ("alu", cflop,
+                   f"{cauchy_flop(r)} flop per (channel, root, pole) on the {100 * direct_frac:.1f} % of roots summed "
+                   f"directly, {(r + 1) ** 2 * (FAR_TERMS - 1) * 8 + 24} flop per far root (series of {FAR_TERMS} terms)"),
         "conv": ("hbm", Bsz * H * L * (4 + 8) + H * 2 * M * 8,
                  "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"),
         "spectrum": ("hbm", H * L * 8 + H * 2 * M * 8, "K 8 B per tap in, spectrum 8 B per 2M bin out"),
@@ -542,7 +586,7 @@ def run_ours(args):
         "config": {"workload": w.name, "N": N, "r": r, "H": H, "L": L, "M": M, "batch": Bsz,
                    "parallelism": f"replica x{world} (channels independent, no collective)",
                    "l2": l2_note},
-        "cauchy_terms_per_s": H * M * N * (r + 1) ** 2 * world * K / (ms_total / 1e3),
+        "cauchy_terms_per_s_direct_equivalent": H * M * N * (r + 1) ** 2 * world * K / (ms_total / 1e3),
         "gpu_launches": launches_per_step * K,
         "kernels": kern,
         "profiled_pass": {"steps": S, "ms_per_step": ms_prof / S,
@@ -573,7 +617,7 @@ def run_ours(args):
 
 PATHS = {
     # path: (unit of the rate, timing families of the library, dominant family)
-    "kernel_gen": ("channel-roots/s", ["cauchy", "ifft"], "cauchy"),
+    "kernel_gen": ("channel-roots/s", ["moments", "cauchy", "ifft"], "cauchy"),
     "conv": ("channel-samples/s", ["spec_fwd", "spectrum", "conv", "conv_fwd", "conv_col", "conv_inv"], "conv"),
     "conv_real": ("channel-samples/s", ["spectrum", "conv_real"], "conv_real"),
     "recurrent": ("channel-samples/s", ["recurrent", "bordered"], "recurrent"),
@@ -736,7 +780,8 @@ def run_path(args):
     launches_per_call = int(round(sum(v["launches"] for v in raw.values()) / S))
     # long rows: the convolution's three launches count as one part, the
     # spectrum's two likewise (per-call time = the sum)
-    groups = {"conv": ["conv", "conv_fwd", "conv_col", "conv_inv"], "spectrum": ["spectrum", "spec_fwd"]}
+    groups = {"conv": ["conv", "conv_fwd", "conv_col", "conv_inv"], "spectrum": ["spectrum", "spec_fwd"],
+              "cauchy": ["cauchy", "moments"]}
     kern = {}
     for name in families:
         g = next((k for k, v in groups.items() if name in v), name)

@@ -12,6 +12,21 @@
 // value (Delta/2) C~^* B.  Statuses: an fp32 denominator |s - lambda_j|^2 equal
 // to zero is 'resonant-diagonal'; an exactly singular W is 'resonant-correction'.
 //
+// Far roots.  Most roots lie far from every pole: with c the centre of the
+// channel's poles and R = max_j |lambda_j - c|, a root with |s - c| >= 2 R has
+//     sum_j w_j / (s - lambda_j) = (1/(s - c)) sum_m mu_m (R/(s - c))^m,
+//     mu_m = sum_j w_j ((lambda_j - c)/R)^m,
+// each term's geometric series converging with ratio at most 1/2.  Truncated
+// after kFarTerms = 24 terms, every term of the Cauchy sum is kept to a relative
+// 2^-24 / (1 - 1/2) < 1.2e-7, below the fp32 rounding of the direct sum.  The
+// moments come from cauchy_moments_kernel, once per channel; a root is far when
+// |s - c|^2 >= 4 R^2 (in fp32), and a CTA whose roots are all far skips the pole
+// loop and evaluates the series by Horner's rule: (r+1)^2 (kFarTerms - 1) complex
+// multiply-adds per root instead of (r+1)^2 N.  Near roots keep the direct sum
+// (and the resonance statuses, which only they can meet).  This is an
+// epsilon-accurate evaluation of the same Cauchy sums, the kind the pages' cost
+// section allows for the filter; the oracle computes the exact definition.
+//
 // Arithmetic: s is carried as an fp32 (hi, lo) pair (tan(pi k/M) from a table
 // computed in float64 at build time, a = 2/Delta split exactly), so that the
 // difference s - lambda_j near a resonance keeps full fp32 relative accuracy.
@@ -97,6 +112,135 @@ __device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
   return true;
 }
 
+// ---- far-field constants of a channel ---------------------------------------------
+using s4impl::kFarTerms;   // series terms kept
+using s4impl::kFarStride;  // float2 entries per channel: [c, (R, 0), mu[w][m]]
+constexpr float kFarRadius2 = 4.f;  // far: |s - c|^2 >= 4 R^2
+
+__device__ __forceinline__ float2 far_weight(int widx, int RANKv, float2 c, float2 b, const float2* p,
+                                             const float2* q) {
+  // order: 0 (C~,B); 1+l (C~,P_l); 1+r+i (Q_i,B); 1+2r+i r+l (Q_i,P_l)
+  if (widx == 0) return conj_mul(c, b);
+  if (widx < 1 + RANKv) return conj_mul(c, p[widx - 1]);
+  if (widx < 1 + 2 * RANKv) return conj_mul(q[widx - 1 - RANKv], b);
+  const int t = widx - 1 - 2 * RANKv;
+  return conj_mul(q[t / RANKv], p[t % RANKv]);
+}
+
+// One CTA per channel: c (centre of the poles' bounding box), R, and the
+// moments mu[w][m] = sum_j w_j rho_j^m, rho_j = (lambda_j - c)/R (R = 1 when all
+// poles coincide: then every rho_j is 0).  The first kernel of a call: records
+// its generation.
+template <int RANK>
+__global__ void __launch_bounds__(256) cauchy_moments_kernel(
+    const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
+    const float2* __restrict__ Bv, const float2* __restrict__ Ct, int N, float2* __restrict__ mom, St status) {
+  constexpr int NW = (RANK + 1) * (RANK + 1), P = kFarTerms, JC = 32, T = 256;
+  constexpr int OWN = (NW * P + T - 1) / T;  // (w, m) pairs per thread
+  __shared__ float2 pw[JC][P];
+  __shared__ float2 wt[JC][NW];
+  __shared__ float red[T / 32][4];
+  __shared__ float cr[3];
+  pdl_wait();
+  st_record_gen(status);
+  pdl_launch_dependents();
+  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  const float2* lam = Lambda + (size_t)h * N;
+  // bounding box of the poles
+  float b0 = INFINITY, b1 = -INFINITY, b2 = INFINITY, b3 = -INFINITY;
+  for (int j = tid; j < N; j += T) {
+    const float2 l = ld_chk(lam, j, N);
+    b0 = fminf(b0, l.x); b1 = fmaxf(b1, l.x); b2 = fminf(b2, l.y); b3 = fmaxf(b3, l.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    b0 = fminf(b0, __shfl_xor_sync(0xffffffffu, b0, o));
+    b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, o));
+    b2 = fminf(b2, __shfl_xor_sync(0xffffffffu, b2, o));
+    b3 = fmaxf(b3, __shfl_xor_sync(0xffffffffu, b3, o));
+  }
+  if (lane == 0) { red[wp][0] = b0; red[wp][1] = b1; red[wp][2] = b2; red[wp][3] = b3; }
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 1; i < T / 32; ++i) {
+      b0 = fminf(b0, red[i][0]); b1 = fmaxf(b1, red[i][1]); b2 = fminf(b2, red[i][2]); b3 = fmaxf(b3, red[i][3]);
+    }
+    cr[0] = 0.5f * (b0 + b1);
+    cr[1] = 0.5f * (b2 + b3);
+  }
+  __syncthreads();
+  const float2 c = make_float2(cr[0], cr[1]);
+  float r2 = 0.f;
+  for (int j = tid; j < N; j += T) {
+    const float2 l = ld_chk(lam, j, N);
+    const float dx = l.x - c.x, dy = l.y - c.y;
+    r2 = fmaxf(r2, fmaf(dx, dx, dy * dy));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) r2 = fmaxf(r2, __shfl_xor_sync(0xffffffffu, r2, o));
+  __syncthreads();
+  if (lane == 0) red[wp][0] = r2;
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 1; i < T / 32; ++i) r2 = fmaxf(r2, red[i][0]);
+    const float R = sqrtf(r2);
+    cr[2] = (R > 0.f && R <= FLT_MAX) ? R : 1.f;
+  }
+  __syncthreads();
+  const float R = cr[2], invR = 1.f / R;
+  float2 acc[OWN];
+#pragma unroll
+  for (int o = 0; o < OWN; ++o) acc[o] = make_float2(0.f, 0.f);
+  for (int j0 = 0; j0 < N; j0 += JC) {
+    const int jn = min(JC, N - j0);
+    __syncthreads();
+    if (tid < jn) {  // weights and the powers rho^0 .. rho^(P-1) of pole j0 + tid
+      const size_t j = (size_t)h * N + j0 + tid;
+      const float2 l = ld_chk(Lambda, j, (long long)gridDim.x * N);
+      float2 pp[RANK], qq[RANK];
+#pragma unroll
+      for (int i = 0; i < RANK; ++i) {
+        pp[i] = ld_chk(Pm, (long long)j * RANK + i, (long long)gridDim.x * N * RANK);
+        qq[i] = ld_chk(Qm, (long long)j * RANK + i, (long long)gridDim.x * N * RANK);
+      }
+      const float2 bj = ld_chk(Bv, j, (long long)gridDim.x * N), cj = ld_chk(Ct, j, (long long)gridDim.x * N);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) wt[tid][w] = far_weight(w, RANK, cj, bj, pp, qq);
+      const float2 rho = make_float2((l.x - c.x) * invR, (l.y - c.y) * invR);
+      float2 pwr = make_float2(1.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < P; ++m) {
+        pw[tid][m] = pwr;
+        pwr = cmul(pwr, rho);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int o = 0; o < OWN; ++o) {
+      const int t = tid + o * T;
+      if (t < NW * P) {
+        const int w = t / P, m = t % P;
+        float2 a = acc[o];
+        for (int jj = 0; jj < jn; ++jj) {
+          const float2 x = wt[jj][w], y = pw[jj][m];
+          a = make_float2(fmaf(x.x, y.x, fmaf(-x.y, y.y, a.x)), fmaf(x.x, y.y, fmaf(x.y, y.x, a.y)));
+        }
+        acc[o] = a;
+      }
+    }
+  }
+  float2* out = mom + (size_t)h * kFarStride;
+  if (tid == 0) {
+    out[0] = c;
+    out[1] = make_float2(R, 0.f);
+  }
+#pragma unroll
+  for (int o = 0; o < OWN; ++o) {
+    const int t = tid + o * T;
+    if (t < NW * P) out[2 + t] = acc[o];
+  }
+}
+
 // Per pole j in shared memory: Im lambda_j, (Re lambda_j)^2, then for each
 // weight w (order 0: (C~,B); 1+l: (C~,P_l); 1+r+i: (Q_i,B); 1+2r+i r+l: (Q_i,P_l))
 // the pair w and w (-Re lambda_j).  With d = s - lambda_j = -Re lambda_j + i dim,
@@ -124,22 +268,31 @@ struct CauchyLayout {
 #ifndef S4_CAUCHY_MINB
 #define S4_CAUCHY_MINB 4
 #endif
-template <int RANK, int RPT, int T, bool PACKED = false>
+// FAR: the far-root series is compiled in (it is used when `far_on` and the
+// constants are given); without it the kernel is the direct sum alone.
+template <int RANK, int RPT, int T, bool PACKED = false, bool FAR = false>
 __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
-    float2* __restrict__ Khat, int N, int logM, int logC, St status) {
+    float2* __restrict__ Khat, const float2* __restrict__ mom, int far_on, int N, int logM, int logC,
+    St status) {
   using Lay = CauchyLayout<RANK, PACKED>;
   constexpr int NW = Lay::NW, PS = Lay::PS, JT = Lay::JT;
   static_assert(!PACKED || RPT % 2 == 0, "packed roots come in pairs");
   constexpr int NPR = RPT / 2;  // (PACKED) root pairs per thread
+  constexpr int FP = kFarTerms;
   __shared__ __align__(16) float par[JT * PS];
+  __shared__ float2 mus[2 + NW * FP];  // c, (R, 0), mu[w][m] of this channel
   __shared__ float2 red[T / 32 + 1];
 
-  pdl_wait();  // (a programmatic launch) the previous kernel on the stream is done
-  st_record_gen(status);
+  if constexpr (!FAR) far_on = 0;
+  pdl_wait();  // the moments kernel (and whatever ran before it) is done
+  if (!far_on) st_record_gen(status);  // (else the moments kernel, this call's first, did)
   pdl_launch_dependents();  // the next kernel may start; it waits for this grid before reading
   const int h = blockIdx.x;
+  if (far_on)
+    for (int i = threadIdx.x; i < 2 + NW * FP; i += T)
+      mus[i] = ld_chk(mom, (long long)h * kFarStride + i, (long long)gridDim.x * kFarStride);
   const int M = 1 << logM;
   const float delta = dt[h];
   const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
@@ -148,14 +301,17 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
   const float a_hi = bad ? 0.f : __fdiv_rn(2.f, delta);
   const float a_lo = bad ? 0.f : __fdiv_rn(fmaf(-a_hi, delta, 2.f), delta);
 
+  // a CTA takes RPT T consecutive roots k (so that near and far roots fall in
+  // separate CTAs) and stores root k at position (k mod C) M/C + k div C
   int pos[RPT];
   bool zm1[RPT];
   float shi[RPT], slo[RPT], th[RPT];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
-    pos[rr] = (blockIdx.y * RPT + rr) * T + threadIdx.x;
-    const bool valid = pos[rr] < M;
-    const int k = valid ? (pos[rr] % Mc) * (1 << logC) + pos[rr] / Mc : 0;
+    const int kr = (blockIdx.y * RPT + rr) * T + threadIdx.x;
+    const bool valid = kr < M;
+    const int k = valid ? kr : 0;
+    pos[rr] = valid ? (k & ((1 << logC) - 1)) * Mc + (k >> logC) : M;
     const float2 tt = (valid && S4_IN(k << (16 - logM), 65536)) ? __ldg(g_tan + (k << (16 - logM)))
                                                                  : make_float2(0.f, 0.f);
     zm1[rr] = valid && M >= 2 && 2 * k == M;
@@ -166,13 +322,29 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     slo[rr] = zm1[rr] ? 0.f : lo;
     th[rr] = tt.x;
   }
+  // far roots: |s - c|^2 >= 4 R^2 with u = s - c (s = i (shi + slo)); the z = -1
+  // root and positions past M need no sums.  A CTA takes the series only when all
+  // its roots are far; otherwise every root takes the direct sum.
+  const float2 fc = far_on ? mus[0] : make_float2(0.f, 0.f);
+  const float fR = far_on ? mus[1].x : 0.f;
+  float2 fu[RPT];
+  bool all_far = far_on != 0;
+  if constexpr (FAR) {
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) {
+      fu[rr] = make_float2(-fc.x, (shi[rr] - fc.y) + slo[rr]);
+      const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
+      all_far = all_far && (pos[rr] >= M || zm1[rr] || (n2u >= kFarRadius2 * fR * fR && n2u > 0.f));
+    }
+    all_far = __syncthreads_and(all_far) != 0;  // (also orders the far constants' loads)
+  }
 
   float2 acc[RPT][NW];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr)
 #pragma unroll
     for (int w = 0; w < NW; ++w) acc[rr][w] = make_float2(0.f, 0.f);
-  float2 cb = make_float2(0.f, 0.f);
+  float2 cb = make_float2(0.f, 0.f);  // this thread's part of C~^* B (pole loop)
   // (PACKED) the accumulators of root pair pr: ax = {acc[2pr][w].x, acc[2pr+1][w].x}, ay likewise
   float2 ax[PACKED ? NPR : 1][NW], ay[PACKED ? NPR : 1][NW], sh2[PACKED ? NPR : 1], sl2[PACKED ? NPR : 1];
   if constexpr (PACKED) {
@@ -188,7 +360,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     }
   }
 
-  for (int j0 = 0; j0 < N; j0 += JT) {
+  for (int j0 = 0; j0 < (all_far ? 0 : N); j0 += JT) {
     const int jn = min(JT, N - j0);
     __syncthreads();
     for (int jj = threadIdx.x; jj < jn; jj += T) {
@@ -217,9 +389,9 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
           pp[5 + 4 * widx] = w.y * nre;
         }
       };
-      float2 w = conj_mul(c, b);
-      cb = cadd(cb, w);
-      put(0, w);
+      const float2 w0 = conj_mul(c, b);
+      cb = cadd(cb, w0);
+      put(0, w0);
 #pragma unroll
       for (int l = 0; l < RANK; ++l) put(1 + l, conj_mul(c, Pm[j * RANK + l]));
 #pragma unroll
@@ -311,21 +483,54 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
       }
   }
 
-  // C~^* B over all poles, for the root z = -1
+  // far roots: the series by Horner's rule, x = R/u, S_w = (1/u) sum_m mu[w][m] x^m
+  if (FAR && all_far) {
+    float2 iu[RPT], xx[RPT];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cb.x += __shfl_xor_sync(0xffffffffu, cb.x, o);
-    cb.y += __shfl_xor_sync(0xffffffffu, cb.y, o);
+    for (int rr = 0; rr < RPT; ++rr) {
+      const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
+      const float r = n2u > 0.f ? __fdiv_rn(1.f, n2u) : 0.f;
+      iu[rr] = make_float2(fu[rr].x * r, -fu[rr].y * r);
+      xx[rr] = cscale(iu[rr], fR);
+    }
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      float2 hw[RPT];
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + FP - 1];
+#pragma unroll 4
+      for (int m = FP - 2; m >= 0; --m) {
+        const float2 mu = mus[2 + w * FP + m];
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr)
+          hw[rr] = make_float2(fmaf(hw[rr].x, xx[rr].x, fmaf(-hw[rr].y, xx[rr].y, mu.x)),
+                               fmaf(hw[rr].x, xx[rr].y, fmaf(hw[rr].y, xx[rr].x, mu.y)));
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) acc[rr][w] = cmul(hw[rr], iu[rr]);
+    }
   }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cb;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float2 t = make_float2(0.f, 0.f);
-    for (int i = 0; i < T / 32; ++i) t = cadd(t, red[i]);
-    red[T / 32] = t;
+  // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
+  // when the pole loop was skipped, else the loop's sum
+  float2 cb_all;
+  if (FAR && all_far) {
+    cb_all = mus[2];
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cb.x += __shfl_xor_sync(0xffffffffu, cb.x, o);
+      cb.y += __shfl_xor_sync(0xffffffffu, cb.y, o);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cb;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float2 t = make_float2(0.f, 0.f);
+      for (int i = 0; i < T / 32; ++i) t = cadd(t, red[i]);
+      red[T / 32] = t;
+    }
+    __syncthreads();
+    cb_all = red[T / 32];
   }
-  __syncthreads();
-  const float2 cb_all = red[T / 32];
 
   unsigned flags = bad ? ST_BAD_STEP : 0u;
 #pragma unroll
@@ -417,11 +622,11 @@ S4_OOB_COUNTER(oob_cauchy)
 #endif
 
 
-template <int RANK, int RPT, bool PACKED = false>
-static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
-                                 const float2* B, const float2* Ct, const float* dt,
-                                 float2* Khat, int H, int N, int M, int logC, St status,
-                                 cudaStream_t s, bool pdl) {
+template <int RANK, int RPT, bool PACKED, bool FAR>
+static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, const float2* Q,
+                                     const float2* B, const float2* Ct, const float* dt,
+                                     float2* Khat, const float2* mom, int H, int N, int M, int logC, St status,
+                                     cudaStream_t s, bool pdl) {
   constexpr int T = S4_CAUCHY_T;
   const int tiles = (M + T * RPT - 1) / (T * RPT);
   dim3 grid(H, tiles);
@@ -433,7 +638,8 @@ static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const fl
   // grid's first wave would only sit on the SMs beside the previous kernel's tail.
   static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
   if (pdl && per_sm < 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED>, T, 0) != cudaSuccess)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, T, 0) !=
+          cudaSuccess)
     per_sm = 0;
   pdl = pdl && (long long)grid.x * grid.y <= (long long)per_sm * num_sms();
   cudaLaunchConfig_t cfg = {};
@@ -445,13 +651,66 @@ static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const fl
   cfg.stream = s;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T, PACKED>, Lambda, P, Q, B, Ct, dt, Khat, N, logM,
-                            logC, status);
+  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, Lambda, P, Q, B, Ct, dt, Khat, mom,
+                            mom ? 1 : 0, N, logM, logC, status);
+}
+
+// the far-root series compiled in only where its constants are given
+template <int RANK, int RPT, bool PACKED = false>
+static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
+                                 const float2* B, const float2* Ct, const float* dt,
+                                 float2* Khat, const float2* mom, int H, int N, int M, int logC, St status,
+                                 cudaStream_t s, bool pdl) {
+  if (mom != nullptr)
+    return cauchy_launch_far<RANK, RPT, PACKED, true>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s,
+                                                      pdl);
+  return cauchy_launch_far<RANK, RPT, PACKED, false>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s,
+                                                     pdl);
+}
+
+template <int RANK>
+static cudaError_t moments_launch(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
+                                  const float2* Ct, float2* mom, int H, int N, St status, cudaStream_t s,
+                                  bool pdl) {
+  TimedLaunch tl("moments", s);
+  static int per_sm = -1;
+  if (pdl && per_sm < 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_moments_kernel<RANK>, 256, 0) != cudaSuccess)
+    per_sm = 0;
+  pdl = pdl && (long long)H <= (long long)per_sm * num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(H);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, cauchy_moments_kernel<RANK>, Lambda, P, Q, B, Ct, N, mom, status);
 }
 
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
-                          const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
+                          const float2* Ct, const float* dt, float2* Khat, float2* mom, int H, int N, int r,
                           int M, int logC, St status, cudaStream_t s, bool pdl) {
+  // the far-field constants first (this call's first kernel), then the root values,
+  // a programmatic dependent that waits for them.  Only on rows of M >= 8192 roots
+  // and N >= 48 poles: on shorter rows every CTA of roots holds near roots, and
+  // with few poles the series is not shorter than the sum, so the extra launch
+  // would not pay (measured slower on N=64 M=1024 and M=4096).
+  if (M < 8192 || N < 48) mom = nullptr;
+  if (mom != nullptr) {
+    cudaError_t e;
+    switch (r) {
+      case 1: e = moments_launch<1>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
+      case 2: e = moments_launch<2>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
+      case 3: e = moments_launch<3>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
+      case 4: e = moments_launch<4>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
+      default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    pdl = true;
+  }
   // roots per thread: rank 1 takes 2 on every grid (S4_CAUCHY_RPT1_BIG); rank 2
   // takes 4 (512 per CTA) once the grid holds at least two waves of such CTAs
   // and 2 below that, to keep enough warps resident
@@ -459,20 +718,20 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
   switch (r) {
     case 1:
 #if S4_CAUCHY_PACKED
-      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
-                   : cauchy_launch<1, S4_CAUCHY_PRPT1_BIG, true>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s,
+      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<1, S4_CAUCHY_PRPT1_BIG, true>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s,
                                                                pdl);
 #else
-      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
-                   : cauchy_launch<1, S4_CAUCHY_RPT1_BIG>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
+      return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<1, S4_CAUCHY_RPT1_BIG>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl);
 #endif
     case 2:  // 4 roots per thread on large grids measured 2 % faster (8 at rank 1 was 11 % slower)
-      return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl)
-                   : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
+      return small ? cauchy_launch<2, 2>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl)
+                   : cauchy_launch<2, 4>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl);
     case 3:
-      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
+      return cauchy_launch<3, 1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl);
     case 4:
-      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, Khat, H, N, M, logC, status, s, pdl);
+      return cauchy_launch<4, 1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl);
     default:
       return cudaErrorInvalidValue;
   }

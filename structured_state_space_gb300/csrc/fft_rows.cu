@@ -183,12 +183,13 @@ __global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) ifft_kernel(
 
 // Spectrum of each channel's kernel zero-padded to n = 2M, natural order, times `scale`.
 // FULL: rows of n values with no padding (the column spectra of the four-step
-// long-row path), every input read.
+// long-row path), every input read; one radix-16 butterfly per thread at 8192
+// points (the convolution's thread count: at two per thread this form spilled).
 template <int LOGN, bool FULL = false>
-__global__ void __launch_bounds__(RowCfg<LOGN>::THREADS) spectrum_kernel(
+__global__ void __launch_bounds__(RowCfg<LOGN, FULL>::THREADS) spectrum_kernel(
     const float2* __restrict__ K, float2* __restrict__ K2, int H, int L, float scale, int realk,
     St status) {
-  using C = RowCfg<LOGN>;
+  using C = RowCfg<LOGN, FULL>;
   constexpr int n = C::n, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int NB0 = n / RA, PER0 = NB0 / T, NBL = n / RB, PERL = NBL / T;
   using IX0 = PassIdx<n, RA, 1>;
@@ -981,7 +982,7 @@ cudaError_t launch_spectrum_rows(int logn, const float2* K, float2* K2, int H, i
 template <int LOGN>
 static cudaError_t spectrum_full_launch(const float2* X, float2* K2, int rows, float scale, St st,
                                         cudaStream_t s) {
-  using C = RowCfg<LOGN>;
+  using C = RowCfg<LOGN, true>;
   const size_t smem = sizeof(float2) * (size_t)C::ROWS * C::PADN;
   auto k = spectrum_kernel<LOGN, true>;
   cudaError_t e = prepare(k, smem);

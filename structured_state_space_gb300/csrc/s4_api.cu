@@ -27,17 +27,19 @@ int ilog2_ceil(int v) {
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Workspace: [status word | root values (H M) | kernel spectra (H 2M) |
-// long-row convolution scratch (two rows of 2M points per pair of batch rows,
-// only when 2M >= 2^14)].  `gen_total` is what kernel generation alone needs.
+// Workspace: [status word | far-field constants of the root values (H
+// kFarStride) | root values (H M) | kernel spectra (H 2M) | long-row convolution
+// scratch (two rows of 2M points per pair of batch rows, only when 2M >= 2^14)].
+// `gen_total` is what kernel generation alone needs.
 struct Layout {
-  size_t khat, k2, fs, gen_total, total;
+  size_t mom, khat, k2, fs, gen_total, total;
 };
 
 Layout layout_for(int H, int L, int batch) {
   const size_t M = (size_t)1 << ilog2_ceil(L);
   Layout l;
-  l.khat = 256;
+  l.mom = 256;
+  l.khat = l.mom + round256(sizeof(float2) * (size_t)s4impl::kFarStride * (size_t)H);
   l.k2 = l.khat + round256(sizeof(float2) * M * (size_t)H);
   l.fs = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
   l.gen_total = l.fs;
@@ -110,7 +112,8 @@ cudaError_t cauchy_impl(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, 
   return launch_cauchy(reinterpret_cast<const float2*>(Lambda), reinterpret_cast<const float2*>(P),
                        reinterpret_cast<const float2*>(Q), reinterpret_cast<const float2*>(B),
                        reinterpret_cast<const float2*>(Ct), dt,
-                       reinterpret_cast<float2*>(w + layout_for(H, L, 1).khat), H, N, r, 1 << logM,
+                       reinterpret_cast<float2*>(w + layout_for(H, L, 1).khat),
+                       reinterpret_cast<float2*>(w + layout_for(H, L, 1).mom), H, N, r, 1 << logM,
                        logC >= 0 ? logC : khat_cluster_log(logM), st, s, pdl);
 }
 

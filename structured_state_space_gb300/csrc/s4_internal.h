@@ -65,13 +65,20 @@ __host__ __device__ constexpr int khat_cluster_log(int logM) {
   return logM <= kMaxLogRowCta ? 0 : cluster_log(logM);
 }
 
+// Far-field constants of the root-value sums, per channel: the centre c and
+// radius R of the poles and the moments of the (r+1)^2 weight vectors, kFarTerms
+// of each; kFarStride complex values per channel (room for rank 4).
+constexpr int kFarTerms = 24;
+constexpr int kFarStride = 2 + 25 * kFarTerms;
+
 // Root values Khat[h][p] for every channel, in the blocked root order
-// (position p -> root (p mod M/C) C + p div M/C, C = 2^logC).  The kernel
-// records the call's generation (it is a call's first kernel); `pdl`: launch
-// it as a programmatic dependent of the previous kernel on the stream, which
-// it waits for before any memory access.
+// (position p -> root (p mod M/C) C + p div M/C, C = 2^logC), after the far-field
+// constants of every channel (into `mom`, H kFarStride complex values).  Two
+// launches; the first records the call's generation (it is a call's first
+// kernel); `pdl`: launch it as a programmatic dependent of the previous kernel on
+// the stream, which it waits for before any memory access.
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
-                          const float2* Ct, const float* dt, float2* Khat, int H, int N, int r,
+                          const float2* Ct, const float* dt, float2* Khat, float2* mom, int H, int N, int r,
                           int M, int logC, St status, cudaStream_t s, bool pdl = false);
 
 // Single-CTA row transforms (log sizes up to kMaxLogRowCta).

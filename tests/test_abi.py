@@ -35,11 +35,16 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_workspace_bytes(lib):
-    # [256 status | H M root values | H 2M spectra], each 256-aligned
+    # [256 status | H x 602 far-field constants | H M root values | H 2M spectra
+    # | long rows only: 2 x 2M per pair of batch rows], each 256-aligned
+    r256 = lambda b: (b + 255) // 256 * 256
+    far = lambda H: r256(8 * 602 * H)
     H, L = 256, 1024
     M = 1024
-    assert s4.s4_workspace_bytes(H, 64, 1, L, 16) == 256 + 8 * H * M + 16 * H * M
-    assert s4.s4_workspace_bytes(3, 4, 1, 100, 1) == 256 + 3072 + 6144  # M = 128
+    assert s4.s4_workspace_bytes(H, 64, 1, L, 16) == 256 + far(H) + 8 * H * M + 16 * H * M
+    assert s4.s4_workspace_bytes(3, 4, 1, 100, 1) == 256 + far(3) + 3072 + 6144  # M = 128
+    # 2M = 2^15: the four-step scratch, 2 rows of 2M complex per pair (batch 3 -> 2 pairs per channel)
+    assert s4.s4_workspace_bytes(2, 4, 1, 16384, 3) == 256 + far(2) + 8 * 2 * 16384 + 16 * 2 * 16384 + 2 * 4 * 32768 * 8
     for bad in [(0, 4, 1, 8, 1), (1, 0, 1, 8, 1), (1, 4, 0, 8, 1), (1, 4, 5, 8, 1), (1, 4, 1, 0, 1),
                 (1, 4, 1, 65537, 1), (1, 4, 1, 8, 0), (1, 65537, 1, 8, 1)]:
         assert s4.s4_workspace_bytes(*bad) == 0, bad

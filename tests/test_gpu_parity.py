@@ -456,8 +456,10 @@ def test_packed_root_values_equal_scalar_bitwise():
     # The root-value kernel takes packed fp32x2 pairs of roots on large grids and
     # the scalar loop on small ones; both do the same per-lane operations in the
     # same order, so one channel alone (H = 1, scalar) and the same channel
-    # repeated 64 times (packed) give identical kernels, bit for bit.
-    w = W.custom(64, 1, 1, 16384, 1, seed=4242)
+    # repeated 64 times (packed) give identical kernels, bit for bit.  (N = 32
+    # poles: the far-root series is not used below 48 poles, so every root takes
+    # the direct sum in both.)
+    w = W.custom(32, 1, 1, 16384, 1, seed=4242)
     p = W.make_params(w)
     rep = {k: np.repeat(p[k], 64, axis=0) for k in ["Lambda", "P", "Q", "B", "Ctilde", "dt"]}
     d1, d64 = dev(p, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt")), dev(rep, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt"))
@@ -467,3 +469,19 @@ def test_packed_root_values_equal_scalar_bitwise():
     assert np.array_equal(K64[0].view(np.uint32), K64[63].view(np.uint32))
     K_ref = O.s4_kernel_channels(p, w.L, [0])
     assert rel_l2(K1, K_ref) <= REL_K
+
+
+@pytest.mark.parametrize("r,dt", [(1, 1e-4), (1, 1e-2), (2, 1e-3)])
+def test_far_root_series_against_the_definition(r, dt):
+    # Channels whose roots are almost all far from the poles (N = 256 poles spread
+    # over 800 along the imaginary axis, a = 2/Delta >= 200): nearly every CTA
+    # of roots takes the truncated series instead of the direct sum.  The kernel
+    # must still match the definition K_j = C^* Abar^j Bbar, here to 1e-5 (ten
+    # times tighter than the parity tolerance), in one call that mixes the two
+    # forms (the CTAs around z = 1 stay direct).
+    w = W.custom(256, r, 4, 32768, 1, seed=77 + r, dt_lo=dt, dt_hi=dt)
+    p = W.make_params(w)
+    d = dev(p, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt"))
+    K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L).cpu().numpy()
+    K_ref = O.s4_kernel_channels(p, w.L, [0, 3])
+    assert rel_l2(K[[0, 3]], K_ref) <= 1e-5, rel_l2(K[[0, 3]], K_ref)
