@@ -56,16 +56,16 @@ def cauchy_flop(r):
     return 8 * (r + 1) ** 2 + 10
 
 
-FAR_TERMS = 24  # terms of the far-root series (the library's kFarTerms)
+FAR_TERMS = 42  # the far-root series' largest number of terms (the library's kFarTerms)
 
 
 def cauchy_work(p, w, sms):
     """The root-value kernel's algorithmic flop for one call, as it splits the
     roots: a CTA of consecutive roots with any root near its channel's poles
-    (|s - c| < 2 R) sums directly over the N poles (cauchy_flop per pole and
+    (|s - c| < 1.5 R) sums directly over the N poles (cauchy_flop per pole and
     root, for every root of the CTA); the other roots evaluate the series,
-    (r+1)^2 (FAR_TERMS - 1) complex multiply-adds of 8 flop plus ~24 flop of
-    set-up each.  The split is replayed here in float64 from the parameters
+    (r+1)^2 (P - 1) complex multiply-adds of 8 flop plus ~24 flop of set-up
+    each, P the terms their warp takes.  The split is replayed here in float64 from the parameters
     (the kernel decides in fp32; the two can differ only at a CTA on the
     boundary).  Returns (flop, fraction of roots summed directly)."""
     import numpy as np
@@ -78,22 +78,33 @@ def cauchy_work(p, w, sms):
     k = np.arange(M)
     t = np.tan(np.pi * k / M)
     direct_roots = 0
+    far_terms = 0
     for h in range(H):
         lam = p["Lambda"][h].astype(np.complex128)
         c = 0.5 * (lam.real.min() + lam.real.max()) + 0.5j * (lam.imag.min() + lam.imag.max())
         R = np.abs(lam - c).max() or 1.0
         a = 2.0 / float(p["dt"][h])
         u = 1j * a * t - c
-        far = np.abs(u) ** 2 >= 4 * R * R
+        far = np.abs(u) ** 2 >= 2.25 * R * R
         if M >= 2:
             far[M // 2] = True
         nb = -(-M // cta)
         pad = np.ones(nb * cta, bool)
         pad[:M] = far
-        direct_roots += int((~pad.reshape(nb, cta).all(axis=1)).sum()) * cta
+        blk_far = pad.reshape(nb, cta).all(axis=1)
+        direct_roots += int((~blk_far).sum()) * cta
+        # terms of the series per root, as the kernel takes them (the warp's largest)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ax = np.abs(R / u)
+            need = np.where((ax > 0) & np.isfinite(ax), 23 / -np.log2(ax), 1) + 2
+        need = np.clip(np.nan_to_num(need, nan=1.0), 1, FAR_TERMS).astype(int)
+        padn = np.ones(nb * cta, int)
+        padn[:M] = need
+        warp = padn.reshape(-1, 32).max(axis=1).repeat(32).reshape(nb, cta)
+        far_terms += int(warp[blk_far].sum())
     direct_roots = min(direct_roots, H * M)
     far_roots = H * M - direct_roots
-    flop = direct_roots * N * cauchy_flop(r) + far_roots * (nw * (FAR_TERMS - 1) * 8 + 24)
+    flop = direct_roots * N * cauchy_flop(r) + nw * 8 * max(far_terms - far_roots, 0) + 24 * far_roots
     return flop, direct_roots / (H * M)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -539,7 +550,7 @@ def run_ours(args):
     work = {
         "cauchy": ("alu", cflop,
                    f"{cauchy_flop(r)} flop per (channel, root, pole) on the {100 * direct_frac:.1f} % of roots summed "
-                   f"directly, {(r + 1) ** 2 * (FAR_TERMS - 1) * 8 + 24} flop per far root (series of {FAR_TERMS} terms)"),
+                   f"directly, 8 (r+1)^2 (P - 1) + 24 flop per far root (series of P <= {FAR_TERMS} terms)"),
         "conv": ("hbm", Bsz * H * L * (4 + 8) + H * 2 * M * 8,
                  "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"),
         "spectrum": ("hbm", H * L * 8 + H * 2 * M * 8, "K 8 B per tap in, spectrum 8 B per 2M bin out"),

@@ -13,15 +13,18 @@
 // to zero is 'resonant-diagonal'; an exactly singular W is 'resonant-correction'.
 //
 // Far roots.  Most roots lie far from every pole: with c the centre of the
-// channel's poles and R = max_j |lambda_j - c|, a root with |s - c| >= 2 R has
-//     sum_j w_j / (s - lambda_j) = (1/(s - c)) sum_m mu_m (R/(s - c))^m,
+// channel's poles and R = max_j |lambda_j - c|, a root with |s - c| >= 1.5 R has
+//     sum_j w_j / (s - lambda_j) = (1/(s - c)) sum_m mu_m x^m,   x = R/(s - c),
 //     mu_m = sum_j w_j ((lambda_j - c)/R)^m,
-// each term's geometric series converging with ratio at most 1/2.  Truncated
-// after kFarTerms = 24 terms, every term of the Cauchy sum is kept to a relative
-// 2^-24 / (1 - 1/2) < 1.2e-7, below the fp32 rounding of the direct sum.  The
+// each term's geometric series converging with ratio |y_j| <= |x| <= 2/3,
+// y_j = (lambda_j - c)/(s - c).  Truncated after P terms, term j of the Cauchy
+// sum is off by the factor 1 - y_j^P: a relative error of at most |x|^P, held to
+// 2^-23 (1.2e-7, the level of the fp32 rounding of the direct sum).  P is at most
+// kFarTerms = 42 (at |x| = 2/3) and falls quickly with |x| (8 terms at |x| = 0.1);
+// a warp takes the largest P its roots need.  The
 // moments come from cauchy_moments_kernel, once per channel; a root is far when
-// |s - c|^2 >= 4 R^2 (in fp32), and a CTA whose roots are all far skips the pole
-// loop and evaluates the series by Horner's rule: (r+1)^2 (kFarTerms - 1) complex
+// |s - c|^2 >= 2.25 R^2 (in fp32), and a CTA whose roots are all far skips the
+// pole loop and evaluates the series by Horner's rule: (r+1)^2 (P - 1) complex
 // multiply-adds per root instead of (r+1)^2 N.  Near roots keep the direct sum
 // (and the resonance statuses, which only they can meet).  This is an
 // epsilon-accurate evaluation of the same Cauchy sums, the kind the pages' cost
@@ -113,9 +116,9 @@ __device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
 }
 
 // ---- far-field constants of a channel ---------------------------------------------
-using s4impl::kFarTerms;   // series terms kept
+using s4impl::kFarTerms;   // series terms kept at most
 using s4impl::kFarStride;  // float2 entries per channel: [c, (R, 0), mu[w][m]]
-constexpr float kFarRadius2 = 4.f;  // far: |s - c|^2 >= 4 R^2
+constexpr float kFarRadius2 = 2.25f;  // far: |s - c|^2 >= (1.5 R)^2
 
 __device__ __forceinline__ float2 far_weight(int widx, int RANKv, float2 c, float2 b, const float2* p,
                                              const float2* q) {
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     slo[rr] = zm1[rr] ? 0.f : lo;
     th[rr] = tt.x;
   }
-  // far roots: |s - c|^2 >= 4 R^2 with u = s - c (s = i (shi + slo)); the z = -1
+  // far roots: |s - c|^2 >= 2.25 R^2 with u = s - c (s = i (shi + slo)); the z = -1
   // root and positions past M need no sums.  A CTA takes the series only when all
   // its roots are far; otherwise every root takes the direct sum.
   const float2 fc = far_on ? mus[0] : make_float2(0.f, 0.f);
@@ -483,23 +486,32 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
       }
   }
 
-  // far roots: the series by Horner's rule, x = R/u, S_w = (1/u) sum_m mu[w][m] x^m
+  // far roots: the series by Horner's rule, x = R/u, S_w = (1/u) sum_m mu[w][m] x^m,
+  // with the terms this warp's roots need: P >= 23 / -log2|x| (one more for the
+  // approximate logarithm), at most FP
   if (FAR && all_far) {
     float2 iu[RPT], xx[RPT];
+    int pneed = 1;
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) {
       const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
       const float r = n2u > 0.f ? __fdiv_rn(1.f, n2u) : 0.f;
       iu[rr] = make_float2(fu[rr].x * r, -fu[rr].y * r);
       xx[rr] = cscale(iu[rr], fR);
+      const float ax2 = fR * fR * r;  // |x|^2 <= 1/2.25 on a far root
+      if (pos[rr] < M && !zm1[rr] && ax2 > 0.f) {
+        const float p = 23.f / (-0.5f * __log2f(ax2));
+        pneed = max(pneed, min(FP, (int)p + 2));
+      }
     }
+    const int P = __reduce_max_sync(0xffffffffu, (unsigned)pneed);
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       float2 hw[RPT];
 #pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + FP - 1];
+      for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + P - 1];
 #pragma unroll 4
-      for (int m = FP - 2; m >= 0; --m) {
+      for (int m = P - 2; m >= 0; --m) {
         const float2 mu = mus[2 + w * FP + m];
 #pragma unroll
         for (int rr = 0; rr < RPT; ++rr)

@@ -68,7 +68,7 @@ __host__ __device__ constexpr int khat_cluster_log(int logM) {
 // Far-field constants of the root-value sums, per channel: the centre c and
 // radius R of the poles and the moments of the (r+1)^2 weight vectors, kFarTerms
 // of each; kFarStride complex values per channel (room for rank 4).
-constexpr int kFarTerms = 24;
+constexpr int kFarTerms = 42;
 constexpr int kFarStride = 2 + 25 * kFarTerms;
 
 // Root values Khat[h][p] for every channel, in the blocked root order
@@ -112,15 +112,18 @@ cudaError_t launch_conv_rows(int logn, const float* u, const float2* K2, const f
 // (two complex rows of 2M points per pair of batch rows), 16-byte aligned.
 constexpr int kMinLogFourStep = 14;
 constexpr int kMaxLogFourStep = 17;
-// K2 in the blocked order of 2^k2_logC (16: column order from the four-step
-// spectrum; cluster_log(logn): from the cluster spectrum kernels), stored as
-// the spectrum times n k2_scale.
+// Across-column radix 2^fs_log_radix(logn) of the four-step split: 16 up to
+// 2^16 points, 32 at 2^17 (columns of 4096 points).
+constexpr int fs_log_radix(int logn) { return logn >= 17 ? 5 : 4; }
+// K2 in the blocked order of 2^k2_logC (fs_log_radix(logn): column order from
+// the four-step spectrum; cluster_log(logn): from the cluster spectrum
+// kernels), stored as the spectrum times n k2_scale.
 size_t fs_scratch_bytes(int logn, int batch, int H);
 cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, int k2_logC, float k2_scale,
                                  const float* D, float2* y, int batch, int H, int L, float2* scratch, St st,
                                  cudaStream_t s);
 // The four-step kernel spectrum (2M = 2^logn, 2^14..2^17) of K [H][L], in
-// column order (k2_logC = 4) scaled 1/(2 (2M/16)) = 8/(2M) (k2_scale = 1/8);
+// column order (k2_logC = fs_log_radix(logn)) scaled 8/(2M) (k2_scale = 1/8);
 // scratch of fs_spec_scratch_bytes(logn, H) bytes.  Records the call's generation.
 constexpr float kFsSpecScale = 0.125f;
 size_t fs_spec_scratch_bytes(int logn, int H);
