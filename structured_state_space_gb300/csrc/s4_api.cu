@@ -154,7 +154,7 @@ s4_status conv_impl(const float* u, const s4_c32* K, const float* D, int batch, 
     float2* fs = reinterpret_cast<float2*>(w + lay.fs);
     e = launch_spectrum_fourstep(logn, Kf, k2, H, L, fs, st, s);
     if (e == cudaSuccess)
-      e = launch_conv_fourstep(logn, u, k2, 4, kFsSpecScale, D, yf, batch, H, L, fs, st, s);
+      e = launch_conv_fourstep(logn, u, k2, fs_log_radix(logn), kFsSpecScale, D, yf, batch, H, L, fs, st, s);
   }
   return cuda_status(e);
 }
@@ -392,8 +392,8 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
       e = s4impl::launch_kspec_fourstep(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, fs,
                                         fs + ((size_t)H << logM), st, s);
     if (e == cudaSuccess)
-      e = s4impl::launch_conv_fourstep(logM + 1, u, k2, 4, s4impl::kFsSpecScale, D, reinterpret_cast<float2*>(y),
-                                       batch, H, L, fs, st, s);
+      e = s4impl::launch_conv_fourstep(logM + 1, u, k2, s4impl::fs_log_radix(logM + 1), s4impl::kFsSpecScale, D,
+                                       reinterpret_cast<float2*>(y), batch, H, L, fs, st, s);
     return cuda_status(e);
   }
   const s4_status g = gen_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, K, ws, st, chain, s);

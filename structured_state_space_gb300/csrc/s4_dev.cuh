@@ -182,30 +182,37 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned pari
 __device__ __forceinline__ int pad(int w) { return w + (w >> 4); }
 __host__ __device__ constexpr int padded_len(int n) { return n + (n >> 4) + 1; }
 
-// ---- cos/sin of 2 pi e / 16 ----------------------------------------------------------
-__host__ __device__ constexpr float cos16(int e) {
-  constexpr float c1 = 0.92387953251128674f, s1 = 0.38268343236508978f, h = 0.70710678118654752f;
-  e &= 15;
-  return e == 0 ? 1.f : e == 1 ? c1 : e == 2 ? h : e == 3 ? s1 : e == 4 ? 0.f : e == 5 ? -s1
-       : e == 6 ? -h : e == 7 ? -c1 : e == 8 ? -1.f : e == 9 ? -c1 : e == 10 ? -h : e == 11 ? -s1
-       : e == 12 ? 0.f : e == 13 ? s1 : e == 14 ? h : c1;
+// ---- cos/sin of 2 pi e / 32 ----------------------------------------------------------
+__host__ __device__ constexpr float cos32(int e) {
+  // cos(k pi/16), k = 0..8, and the symmetries of the cosine
+  constexpr float c[9] = {1.f,
+                          0.98078528040323044f,
+                          0.92387953251128674f,
+                          0.83146961230254524f,
+                          0.70710678118654752f,
+                          0.55557023301960222f,
+                          0.38268343236508978f,
+                          0.19509032201612826f,
+                          0.f};
+  e &= 31;
+  return e <= 8 ? c[e] : e <= 16 ? -c[16 - e] : e <= 24 ? -c[e - 16] : c[32 - e];
 }
-__host__ __device__ constexpr float sin16(int e) { return cos16(e - 4); }  // sin x = cos(x - pi/2)
+__host__ __device__ constexpr float sin32(int e) { return cos32(e - 8); }  // sin x = cos(x - pi/2)
 
-// a <- a + w b, b <- a - w b, with w = exp(-+ 2 pi i e/16) (forward / inverse).
+// a <- a + w b, b <- a - w b, with w = exp(-+ 2 pi i e/32) (forward / inverse).
 template <bool INV>
 __device__ __forceinline__ void bfly(float2& a, float2& b, int e) {
   if (e == 0) {
     const float2 t = b;
     b = csub(a, t);
     a = cadd(a, t);
-  } else if (e == 4) {  // w = -i (forward) or +i (inverse)
+  } else if (e == 8) {  // w = -i (forward) or +i (inverse)
     const float2 t = INV ? make_float2(-b.y, b.x) : make_float2(b.y, -b.x);
     b = csub(a, t);
     a = cadd(a, t);
   } else {
-    const float c = cos16(e);
-    const float s = INV ? sin16(e) : -sin16(e);  // w = c + i s
+    const float c = cos32(e);
+    const float s = INV ? sin32(e) : -sin32(e);  // w = c + i s
     const float yx = fmaf(b.x, c, fmaf(-b.y, s, a.x));
     const float yy = fmaf(b.x, s, fmaf(b.y, c, a.y));
     b = make_float2(fmaf(2.f, a.x, -yx), fmaf(2.f, a.y, -yy));
@@ -218,16 +225,16 @@ template <bool INV>
 __device__ __forceinline__ void bfly_top(float2& a, const float2 b, int e) {
   if (e == 0) {
     a = cadd(a, b);
-  } else if (e == 4) {
+  } else if (e == 8) {
     a = cadd(a, INV ? make_float2(-b.y, b.x) : make_float2(b.y, -b.x));
   } else {
-    const float c = cos16(e);
-    const float s = INV ? sin16(e) : -sin16(e);
+    const float c = cos32(e);
+    const float s = INV ? sin32(e) : -sin32(e);
     a = make_float2(fmaf(b.x, c, fmaf(-b.y, s, a.x)), fmaf(b.x, s, fmaf(b.y, c, a.y)));
   }
 }
 
-// In-register DFT of length R (1, 2, 4, 8, 16) by the even/odd split of the
+// In-register DFT of length R (1, 2, 4, 8, 16, 32) by the even/odd split of the
 // radix-two recursion.  HALFZERO: inputs R/2..R-1 are known zero.  HALFOUT:
 // only outputs 0..R/2-1 are needed.
 template <int R, bool INV, bool HALFZERO = false, bool HALFOUT = false>
@@ -254,10 +261,10 @@ __device__ __forceinline__ void dft(float2* a) {
 #pragma unroll
     for (int k = 0; k < R / 2; ++k) {
       if constexpr (HALFOUT) {
-        bfly_top<INV>(ev[k], od[k], (16 / R) * k);
+        bfly_top<INV>(ev[k], od[k], (32 / R) * k);
         a[k] = ev[k];
       } else {
-        bfly<INV>(ev[k], od[k], (16 / R) * k);
+        bfly<INV>(ev[k], od[k], (32 / R) * k);
         a[k] = ev[k];
         a[k + R / 2] = od[k];
       }
