@@ -271,10 +271,15 @@ struct CauchyLayout {
 #ifndef S4_CAUCHY_MINB
 #define S4_CAUCHY_MINB 4
 #endif
+// (rank >= 2 with the far-root series compiled in: resident CTAs per SM)
+#ifndef S4_CAUCHY_MINB_FAR2
+#define S4_CAUCHY_MINB_FAR2 3
+#endif
 // FAR: the far-root series is compiled in (it is used when `far_on` and the
 // constants are given); without it the kernel is the direct sum alone.
 template <int RANK, int RPT, int T, bool PACKED = false, bool FAR = false>
-__global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kernel(
+__global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MINB_FAR2 : S4_CAUCHY_MINB) : 0)
+    cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
     float2* __restrict__ Khat, const float2* __restrict__ mom, int far_on, int N, int logM, int logC,
@@ -304,19 +309,40 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
   const float a_hi = bad ? 0.f : __fdiv_rn(2.f, delta);
   const float a_lo = bad ? 0.f : __fdiv_rn(fmaf(-a_hi, delta, 2.f), delta);
 
-  // a CTA takes RPT T consecutive roots k (so that near and far roots fall in
-  // separate CTAs) and stores root k at position (k mod C) M/C + k div C
+  // A tile is RPT T consecutive roots k (so that near and far roots fall in
+  // separate tiles); root k is stored at position (k mod C) M/C + k div C.  The
+  // CTA takes the tiles of its channel numbered v = blockIdx.y, blockIdx.y +
+  // gridDim.y, ..., tile v/2 for even v and tiles - 1 - v/2 for odd v: the roots
+  // near the poles lie at the two ends of the range (s = i a tan(pi k/M) small),
+  // so their costly direct tiles start first instead of forming the grid's tail.
+  // The next tile's tan values are loaded while the current one is computed.
+  const int tiles = (M + RPT * T - 1) / (RPT * T);
+  auto tile_of = [&](int v) { return (v & 1) ? tiles - 1 - (v >> 1) : (v >> 1); };
+  auto tan_of = [&](int tile, int rr) {
+    const int kr = (tile * RPT + rr) * T + threadIdx.x;
+    return (kr < M && S4_IN(kr << (16 - logM), 65536)) ? __ldg(g_tan + (kr << (16 - logM)))
+                                                      : make_float2(0.f, 0.f);
+  };
+  float2 tnext[FAR ? RPT : 1];
+  if constexpr (FAR) {
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) tnext[rr] = tan_of(tile_of(blockIdx.y), rr);
+  }
+  unsigned flags = bad ? ST_BAD_STEP : 0u;
+  for (int v = blockIdx.y; v < tiles; v += gridDim.y) {
+  const int tile = tile_of(v);
   int pos[RPT];
   bool zm1[RPT];
   float shi[RPT], slo[RPT], th[RPT];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
-    const int kr = (blockIdx.y * RPT + rr) * T + threadIdx.x;
+    const int kr = (tile * RPT + rr) * T + threadIdx.x;
     const bool valid = kr < M;
     const int k = valid ? kr : 0;
     pos[rr] = valid ? (k & ((1 << logC) - 1)) * Mc + (k >> logC) : M;
-    const float2 tt = (valid && S4_IN(k << (16 - logM), 65536)) ? __ldg(g_tan + (k << (16 - logM)))
-                                                                 : make_float2(0.f, 0.f);
+    float2 tt;
+    if constexpr (FAR) tt = tnext[rr];
+    else tt = tan_of(tile, rr);
     zm1[rr] = valid && M >= 2 && 2 * k == M;
     const float p = a_hi * tt.x;
     const float perr = fmaf(a_hi, tt.x, -p);
@@ -324,6 +350,10 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     shi[rr] = zm1[rr] ? 0.f : p;
     slo[rr] = zm1[rr] ? 0.f : lo;
     th[rr] = tt.x;
+  }
+  if (FAR && v + (int)gridDim.y < tiles) {
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) tnext[FAR ? rr : 0] = tan_of(tile_of(v + gridDim.y), rr);
   }
   // far roots: |s - c|^2 >= 2.25 R^2 with u = s - c (s = i (shi + slo)); the z = -1
   // root and positions past M need no sums.  A CTA takes the series only when all
@@ -495,31 +525,72 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) {
       const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
-      const float r = n2u > 0.f ? __fdiv_rn(1.f, n2u) : 0.f;
+      // 1/|u|^2 to within an ulp or two (the approximate reciprocal), which the
+      // series inherits as a relative error of the same size
+      const float r = n2u > 0.f ? rcp_approx(n2u) : 0.f;
       iu[rr] = make_float2(fu[rr].x * r, -fu[rr].y * r);
       xx[rr] = cscale(iu[rr], fR);
       const float ax2 = fR * fR * r;  // |x|^2 <= 1/2.25 on a far root
       if (pos[rr] < M && !zm1[rr] && ax2 > 0.f) {
-        const float p = 23.f / (-0.5f * __log2f(ax2));
+        const float p = 23.f * rcp_approx(-0.5f * __log2f(ax2));
         pneed = max(pneed, min(FP, (int)p + 2));
       }
     }
     const int P = __reduce_max_sync(0xffffffffu, (unsigned)pneed);
+    if constexpr (PACKED) {
+      // root pairs in packed fp32x2: hx = {Re h of root 2pr, of root 2pr+1}, hy likewise;
+      // each step is the scalar step below, operation for operation
+      float2 x2x[NPR], x2y[NPR], n2y[NPR];
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      float2 hw[RPT];
-#pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + P - 1];
-#pragma unroll 4
-      for (int m = P - 2; m >= 0; --m) {
-        const float2 mu = mus[2 + w * FP + m];
-#pragma unroll
-        for (int rr = 0; rr < RPT; ++rr)
-          hw[rr] = make_float2(fmaf(hw[rr].x, xx[rr].x, fmaf(-hw[rr].y, xx[rr].y, mu.x)),
-                               fmaf(hw[rr].x, xx[rr].y, fmaf(hw[rr].y, xx[rr].x, mu.y)));
+      for (int pr = 0; pr < NPR; ++pr) {
+        x2x[pr] = make_float2(xx[2 * pr].x, xx[2 * pr + 1].x);
+        x2y[pr] = make_float2(xx[2 * pr].y, xx[2 * pr + 1].y);
+        n2y[pr] = make_float2(-x2y[pr].x, -x2y[pr].y);
       }
 #pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) acc[rr][w] = cmul(hw[rr], iu[rr]);
+      for (int w = 0; w < NW; ++w) {
+        float2 hx[NPR], hy[NPR];
+        const float2 top = mus[2 + w * FP + P - 1];
+#pragma unroll
+        for (int pr = 0; pr < NPR; ++pr) {
+          hx[pr] = make_float2(top.x, top.x);
+          hy[pr] = make_float2(top.y, top.y);
+        }
+#pragma unroll 4
+        for (int m = P - 2; m >= 0; --m) {
+          const float2 mu = mus[2 + w * FP + m];
+          const float2 mx = make_float2(mu.x, mu.x), my = make_float2(mu.y, mu.y);
+#pragma unroll
+          for (int pr = 0; pr < NPR; ++pr) {
+            const float2 nx = __ffma2_rn(hx[pr], x2x[pr], __ffma2_rn(hy[pr], n2y[pr], mx));
+            const float2 ny = __ffma2_rn(hx[pr], x2y[pr], __ffma2_rn(hy[pr], x2x[pr], my));
+            hx[pr] = nx;
+            hy[pr] = ny;
+          }
+        }
+#pragma unroll
+        for (int pr = 0; pr < NPR; ++pr) {
+          acc[2 * pr][w] = cmul(make_float2(hx[pr].x, hy[pr].x), iu[2 * pr]);
+          acc[2 * pr + 1][w] = cmul(make_float2(hx[pr].y, hy[pr].y), iu[2 * pr + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        float2 hw[RPT];
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + P - 1];
+#pragma unroll 4
+        for (int m = P - 2; m >= 0; --m) {
+          const float2 mu = mus[2 + w * FP + m];
+#pragma unroll
+          for (int rr = 0; rr < RPT; ++rr)
+            hw[rr] = make_float2(fmaf(hw[rr].x, xx[rr].x, fmaf(-hw[rr].y, xx[rr].y, mu.x)),
+                                 fmaf(hw[rr].x, xx[rr].y, fmaf(hw[rr].y, xx[rr].x, mu.y)));
+        }
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr) acc[rr][w] = cmul(hw[rr], iu[rr]);
+      }
     }
   }
   // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
@@ -544,7 +615,6 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     cb_all = red[T / 32];
   }
 
-  unsigned flags = bad ? ST_BAD_STEP : 0u;
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
     if (pos[rr] >= M) continue;
@@ -553,9 +623,12 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
       if (zm1[rr]) {
         Hk = cscale(cb_all, 0.5f * delta);
       } else {
+        // (far tiles cannot meet a resonance: a non-finite value there shows in Hk)
         bool fin = true;
+        if (!(FAR && all_far)) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
+          for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
+        }
         if (!fin) {
           // an exactly zero denominator gives inf/nan; tell it apart from overflow
           bool res = false;
@@ -594,6 +667,8 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? S4_CAUCHY_MINB : 0) cauchy_kerne
     }
     st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
   }
+  if constexpr (!FAR) break;  // one tile per CTA
+  }  // tiles
   if (flags) st_flag(status, flags);
 }
 
@@ -632,6 +707,9 @@ S4_OOB_COUNTER(oob_cauchy)
 #ifndef S4_CAUCHY_PRPT1_BIG
 #define S4_CAUCHY_PRPT1_BIG 4
 #endif
+#ifndef S4_CAUCHY_FAR_TILES
+#define S4_CAUCHY_FAR_TILES 4
+#endif
 
 
 template <int RANK, int RPT, bool PACKED, bool FAR>
@@ -641,18 +719,30 @@ static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, cons
                                      cudaStream_t s, bool pdl) {
   constexpr int T = S4_CAUCHY_T;
   const int tiles = (M + T * RPT - 1) / (T * RPT);
-  dim3 grid(H, tiles);
+  static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
+  if (per_sm < 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, T, 0) !=
+          cudaSuccess)
+    per_sm = 0;
+  // With the far-root series, a CTA loops over up to S4_CAUCHY_FAR_TILES tiles of
+  // its channel (most of them cheap series tiles, which would otherwise each pay a
+  // CTA's set-up), as long as the grid keeps 16 CTAs per resident slot for the
+  // balance of the costly direct tiles (measured: 1511 -> 1394 us on N=256 H=1024
+  // M=65536 at 4 tiles, where 8 was no faster; 184 -> 198 us on N=64 H=256
+  // M=16384 at 4, whose grid is 16 times smaller).  The direct sum alone keeps one
+  // tile per CTA.
+  long long per_cta = 1;
+  if (FAR && per_sm > 0) {
+    per_cta = (long long)H * tiles / (16LL * per_sm * num_sms());
+    per_cta = per_cta < 1 ? 1 : (per_cta > S4_CAUCHY_FAR_TILES ? S4_CAUCHY_FAR_TILES : per_cta);
+  }
+  dim3 grid(H, (unsigned)((tiles + per_cta - 1) / per_cta));
   TimedLaunch tl("cauchy", s);
   int logM = 0;
   while ((1 << logM) < M) ++logM;
   // A programmatic launch lets this grid's CTAs become resident while the
   // previous kernel drains; that pays when the grid fits in one wave.  A larger
   // grid's first wave would only sit on the SMs beside the previous kernel's tail.
-  static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
-  if (pdl && per_sm < 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, T, 0) !=
-          cudaSuccess)
-    per_sm = 0;
   pdl = pdl && (long long)grid.x * grid.y <= (long long)per_sm * num_sms();
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

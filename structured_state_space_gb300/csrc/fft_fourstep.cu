@@ -45,6 +45,19 @@
 //                    2M transform: with R = 16 for its two columns t2 and t2 + M/16,
 //                    with R = 32 for its column t2 (whose nonzero inputs are exactly
 //                    these 16 values) -> X[h][k1][.]
+// When L = M the 2M-point spectrum needs only half of that: its even bins are the
+// root values themselves (K^[2j] = sum_{t<M} K[t] w_M^{jt} = Khat[j], K being the
+// whole inverse transform), and its odd bins are the M-point transform of the
+// twisted kernel, K^[2j+1] = sum_t (K[t] w_2M^t) w_M^{jt}.  With the root values in
+// column order of C = R/2 ([k1][k2], k = k1 + C k2 of the M-point grid):
+//   the row inverse-transform kernel: the C H columns of M/C points, 1/(M/C)
+//   ks_cross_half_kernel per (channel, t2 < M/C): the radix-C inverse -> K (written
+//                    out), the twist w_2M^t and the radix-C forward across-column
+//                    step of its M-point transform -> X[h][k1][t2]
+//   the row spectrum kernel on the C H columns -> T = K^[odd] in column order of C.
+// The column kernel then reads the spectrum's bin k = k1 + R k2 of its column from
+// the root values (k1 even) or from T (k1 odd), at j = k div 2 = k1/2 + C k2: one
+// contiguous column of either array.
 #include "s4_fft.cuh"
 #include "s4_internal.h"
 
@@ -215,6 +228,51 @@ __global__ void __launch_bounds__(kFsThreads) ks_cross_kernel(const float2* __re
   }
 }
 
+// Layer path with L = M: K from the column inverse transforms G[h][k1][t2] (M/C
+// points each, scaled 1/(M/C); C = R/2 for the 2M split's radix R), and the forward
+// across-column step of the M-point transform of K[t] w_2M^t, whose bins are the
+// odd bins of K's 2M-point spectrum.  A thread owns t2 < M/C and K[(M/C) t1 + t2]
+// for all t1 < C; w_2M^t = w_{2C}^{t1} w_2M^{t2}, the second factor applied after
+// the DFT over t1 together with the across-column twiddle w_M^{t2 k1}.
+template <int LOGM>
+__global__ void __launch_bounds__(kFsThreads) ks_cross_half_kernel(const float2* __restrict__ G,
+                                                                   float2* __restrict__ K,
+                                                                   float2* __restrict__ X, int H, int L,
+                                                                   St status) {
+  constexpr int C = 1 << (s4impl::fs_log_radix(LOGM + 1) - 1);
+  constexpr int M = 1 << LOGM, mi = M / C, n = 2 * M;
+  const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
+  const int h = (int)(gid / mi), t2 = (int)(gid % mi);
+  if (h >= H) return;
+  const bool zero = st_bad(status);
+  float2 g[C];
+  const float2* gp = G + (size_t)h * M + t2;
+#pragma unroll
+  for (int k1 = 0; k1 < C; ++k1)
+    g[k1] = S4_IN((long long)h * M + (long long)k1 * mi + t2, (long long)H * M) ? __ldcs(gp + (size_t)k1 * mi)
+                                                                              : make_float2(0.f, 0.f);
+  float2 w = fs_twiddle(t2, M);
+  w.y = -w.y;
+  apply_twiddles<C>(g, w);
+  dft<C, true>(g);
+#pragma unroll
+  for (int t1 = 0; t1 < C; ++t1) {
+    const int t = mi * t1 + t2;
+    g[t1] = (zero || t >= L) ? make_float2(0.f, 0.f) : cscale(g[t1], 1.f / C);
+    if (t < L) st_chk(K, (long long)h * L + t, (long long)H * L, g[t1]);
+    // w_{2C}^{t1} = exp(-2 pi i t1 / (2C)), in 32nds of a turn
+    if (t1 > 0) g[t1] = cmul(g[t1], make_float2(cos32(t1 * (16 / C)), -sin32(t1 * (16 / C))));
+  }
+  dft<C, false>(g);
+  // times w_2M^{t2 (2 k1 + 1)}: v = w_2M^{t2} on every output, then (v^2)^{k1}
+  const float2 v = fs_twiddle(t2, n);
+#pragma unroll
+  for (int k1 = 0; k1 < C; ++k1) g[k1] = cmul(g[k1], v);
+  apply_twiddles<C>(g, fs_twiddle(t2, M));
+#pragma unroll
+  for (int k1 = 0; k1 < C; ++k1) st_chk(X, (long long)h * M + (long long)k1 * mi + t2, (long long)H * M, g[k1]);
+}
+
 // Stores y_b[t] = (Re a_t, Re c_t) and y_{b+1}[t] = (Im a_t, Im c_t) for t < L.
 __device__ __forceinline__ void fs_store_y(float2* __restrict__ y, const FsPair& q, int t, int L, long long ny,
                                            bool zero, float2 a, float2 c) {
@@ -332,10 +390,14 @@ __device__ __forceinline__ float2 fs_spec(const float2* __restrict__ K2h, int k,
 }
 
 // 512 threads per SM at 128 registers (one CTA for m = 8192, more for shorter columns)
+// K2o != nullptr: the spectrum in two halves, even bins from K2 and odd bins from
+// K2o (each H x n/2, in the blocked order of 2^logC over n/2 bins), stored as the
+// spectrum times n kscale and n kscale_o respectively.
 template <int LOGM, int LOGR>
 __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>::THREADS) fs_column_kernel(
     float2* __restrict__ X, float2* __restrict__ Ci, const float2* __restrict__ K2,
-    const float* __restrict__ D, int H, int pb, int logC, float kscale, St status) {
+    const float2* __restrict__ K2o, const float* __restrict__ D, int H, int pb, int logC, float kscale,
+    float kscale_o, St status) {
   using C = FsColCfg<LOGM>;
   constexpr int m = C::m, T = C::T, NP = C::NP, RA = C::RA, RB = C::RB;
   constexpr int R = 1 << LOGR, n = m * R;
@@ -362,7 +424,9 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
     const int h = p / pb;
     float2* xc = X + (size_t)p * n + (size_t)k1 * m;        // this column: X in, a out
     float2* cc = Ci + (size_t)p * n + (size_t)k1 * m;       // c out
-    const float2* K2h = K2 + (size_t)h * n;
+    const bool split = K2o != nullptr, odd = split && (k1 & 1);
+    const float2* K2h = split ? (odd ? K2o : K2) + (size_t)h * (n / 2) : K2 + (size_t)h * n;
+    const float ksc = odd ? kscale_o : kscale;
     const float dv = act ? D[h] : 0.f;
     // forward pass 0: global -> shared
 #pragma unroll
@@ -395,11 +459,13 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
       for (int qq = 0; qq < RB; ++qq) {
         const int k2 = i + qq * NBL;
         const int k = k1 + R * k2;
-        const float2 kv = fs_spec(K2h, k, n, logC);
-        const float2 km = fs_spec(K2h, (n - k) & (n - 1), n, logC);
-        // (K^r + D)/n and K^i/n, the stored spectrum being K^ n kscale
-        const float2 kr = make_float2(fmaf(0.5f * kscale, kv.x + km.x, dv * sc), 0.5f * kscale * (kv.y - km.y));
-        const float2 ki = make_float2(0.5f * kscale * (kv.y + km.y), 0.5f * kscale * (km.x - kv.x));
+        // K^[k] and K^[-k] (the same parity: the same half when split)
+        const int kmir = (n - k) & (n - 1);
+        const float2 kv = split ? fs_spec(K2h, k >> 1, n / 2, logC) : fs_spec(K2h, k, n, logC);
+        const float2 km = split ? fs_spec(K2h, kmir >> 1, n / 2, logC) : fs_spec(K2h, kmir, n, logC);
+        // (K^r + D)/n and K^i/n, the stored spectrum being K^ n ksc
+        const float2 kr = make_float2(fmaf(0.5f * ksc, kv.x + km.x, dv * sc), 0.5f * ksc * (kv.y - km.y));
+        const float2 ki = make_float2(0.5f * ksc * (kv.y + km.y), 0.5f * ksc * (km.x - kv.x));
         pa[s][qq] = cmul(z[qq], kr);
         pc[s][qq] = cmul(z[qq], ki);
       }
@@ -462,7 +528,8 @@ size_t fs_scratch_bytes(int logn, int batch, int H) {
 
 template <int LOGN>
 static cudaError_t fs_launch(const float* u, const float2* K2, int k2_logC, float k2_scale, const float* D,
-                             float2* y, int batch, int H, int L, float2* scratch, St st, cudaStream_t s) {
+                             float2* y, int batch, int H, int L, float2* scratch, St st, cudaStream_t s,
+                             const float2* K2o, float k2o_scale) {
   constexpr int LOGR = fs_log_radix(LOGN), R = 1 << LOGR, n = 1 << LOGN, m = n / R, LOGM = LOGN - LOGR;
   using C = FsColCfg<LOGM>;
   const int pb = (batch + 1) / 2;
@@ -490,7 +557,7 @@ static cudaError_t fs_launch(const float* u, const float2* K2, int k2_logC, floa
   const int grid = (int)(need < (long long)per_sm * num_sms() ? need : (long long)per_sm * num_sms());
   {
     TimedLaunch tl("conv_col", s);
-    k<<<grid, C::THREADS, smem, s>>>(X, Ci, K2, D, H, pb, k2_logC, k2_scale, st);
+    k<<<grid, C::THREADS, smem, s>>>(X, Ci, K2, K2o, D, H, pb, k2_logC, k2_scale, k2o_scale, st);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -505,12 +572,13 @@ static cudaError_t fs_launch(const float* u, const float2* K2, int k2_logC, floa
 
 cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, int k2_logC, float k2_scale,
                                  const float* D, float2* y, int batch, int H, int L, float2* scratch, St st,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const float2* K2o, float k2o_scale) {
   switch (logn) {
-    case 14: return fs_launch<14>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
-    case 15: return fs_launch<15>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
-    case 16: return fs_launch<16>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
-    case 17: return fs_launch<17>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s);
+#define S4_CASE(X) \
+  case X:          \
+    return fs_launch<X>(u, K2, k2_logC, k2_scale, D, y, batch, H, L, scratch, st, s, K2o, k2o_scale);
+    S4_CASE(14) S4_CASE(15) S4_CASE(16) S4_CASE(17)
+#undef S4_CASE
     default: return cudaErrorInvalidValue;
   }
 }
@@ -573,6 +641,37 @@ cudaError_t launch_kspec_fourstep(int logM, const float2* Khat, float2* K, float
     case 14: return ks_fs_launch<14>(Khat, K, K2, H, L, G, X, st, s);
     case 15: return ks_fs_launch<15>(Khat, K, K2, H, L, G, X, st, s);
     case 16: return ks_fs_launch<16>(Khat, K, K2, H, L, G, X, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Layer path, L = M: root values in column order of C = R/2 -> K (out) and the
+// odd bins of its 2M spectrum, T, in column order of C, scaled 8/(2M).  G and X:
+// scratch of H M complex values each.
+template <int LOGM>
+static cudaError_t ks_half_launch(const float2* Khat, float2* K, float2* T, int H, int L, float2* G, float2* X,
+                                  St st, cudaStream_t s) {
+  constexpr int LC = fs_log_radix(LOGM + 1) - 1, C = 1 << LC;
+  constexpr int M = 1 << LOGM, mi = M / C, n = 2 * M;
+  cudaError_t e = launch_ifft_rows(LOGM - LC, Khat, G, H * C, mi, st, s);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)(((long long)H * mi + kFsThreads - 1) / kFsThreads);
+  {
+    TimedLaunch tl("kspec_cross", s);
+    ks_cross_half_kernel<LOGM><<<blocks, kFsThreads, 0, s>>>(G, K, X, H, L, st);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_spectrum_rows_full(LOGM - LC, X, T, H * C, 8.f / n, st, s);
+}
+
+cudaError_t launch_kspec_fourstep_half(int logM, const float2* Khat, float2* K, float2* T, int H, int L,
+                                       float2* G, float2* X, St st, cudaStream_t s) {
+  switch (logM) {
+    case 13: return ks_half_launch<13>(Khat, K, T, H, L, G, X, st, s);
+    case 14: return ks_half_launch<14>(Khat, K, T, H, L, G, X, st, s);
+    case 15: return ks_half_launch<15>(Khat, K, T, H, L, G, X, st, s);
+    case 16: return ks_half_launch<16>(Khat, K, T, H, L, G, X, st, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -13,6 +13,12 @@
 #include "s4_dev.cuh"
 #include "s4_internal.h"
 
+// Build-time tuning: on long rows with L = M, form only the odd half of the
+// kernel spectrum (1) or all of it (0).
+#ifndef S4_HALF_SPECTRUM
+#define S4_HALF_SPECTRUM 1
+#endif
+
 namespace {
 
 constexpr int kMaxL = 65536;
@@ -381,12 +387,27 @@ s4_status s4_layer_fwd(const s4_c32* Lambda, const s4_c32* P, const s4_c32* Q, c
     // long rows: root values in column order -> column inverse transforms -> K
     // (out) and the across-column step of its spectrum -> column spectra ->
     // four-step convolution.  The spectrum's scratch (H M + 2 H M values) lies
-    // in the convolution's, which is written only after it is consumed.
+    // in the convolution's, which is written only after it is consumed; the root
+    // values stay in their own region until the convolution has read them.
     const Layout lay = layout_for(H, L, batch);
     char* w = static_cast<char*>(ws);
     float2* khat = reinterpret_cast<float2*>(w + lay.khat);
     float2* k2 = reinterpret_cast<float2*>(w + lay.k2);
     float2* fs = reinterpret_cast<float2*>(w + lay.fs);
+    if (S4_HALF_SPECTRUM && L == (1 << logM)) {
+      // L = M: the spectrum's even bins are the root values; only its odd bins are
+      // formed (into the spectrum's region), and the convolution reads both halves
+      const int logC = s4impl::fs_log_radix(logM + 1) - 1;
+      cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s, logC);
+      if (e == cudaSuccess)
+        e = s4impl::launch_kspec_fourstep_half(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, fs,
+                                               fs + ((size_t)H << logM), st, s);
+      if (e == cudaSuccess)
+        e = s4impl::launch_conv_fourstep(logM + 1, u, khat, logC, 1.f / (float)(2 << logM), D,
+                                         reinterpret_cast<float2*>(y), batch, H, L, fs, st, s, k2,
+                                         s4impl::kFsSpecScale);
+      return cuda_status(e);
+    }
     cudaError_t e = cauchy_impl(Lambda, P, Q, B, Ctilde, dt, H, N, r, L, ws, st, chain, s, /*logC=*/4);
     if (e == cudaSuccess)
       e = s4impl::launch_kspec_fourstep(logM, khat, reinterpret_cast<float2*>(K), k2, H, L, fs,

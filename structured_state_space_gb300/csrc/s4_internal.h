@@ -119,9 +119,12 @@ constexpr int fs_log_radix(int logn) { return logn >= 17 ? 5 : 4; }
 // the four-step spectrum; cluster_log(logn): from the cluster spectrum
 // kernels), stored as the spectrum times n k2_scale.
 size_t fs_scratch_bytes(int logn, int batch, int H);
+// K2o != nullptr: the spectrum in two halves (see launch_kspec_fourstep_half),
+// the even bins in K2 and the odd bins in K2o (stored as the spectrum times n
+// k2o_scale), each H x n/2 in the blocked order of 2^k2_logC over n/2 bins.
 cudaError_t launch_conv_fourstep(int logn, const float* u, const float2* K2, int k2_logC, float k2_scale,
                                  const float* D, float2* y, int batch, int H, int L, float2* scratch, St st,
-                                 cudaStream_t s);
+                                 cudaStream_t s, const float2* K2o = nullptr, float k2o_scale = 0.f);
 // The four-step kernel spectrum (2M = 2^logn, 2^14..2^17) of K [H][L], in
 // column order (k2_logC = fs_log_radix(logn)) scaled 8/(2M) (k2_scale = 1/8);
 // scratch of fs_spec_scratch_bytes(logn, H) bytes.  Records the call's generation.
@@ -134,6 +137,14 @@ cudaError_t launch_spectrum_fourstep(int logn, const float2* K, float2* K2, int 
 // H 2M complex scratch.
 cudaError_t launch_kspec_fourstep(int logM, const float2* Khat, float2* K, float2* K2, int H, int L, float2* G,
                                   float2* X, St st, cudaStream_t s);
+// Layer path with L = M (M = 2^13 .. 2^16): the 2M spectrum's even bins are the
+// root values themselves, so only its odd bins T (H x M, scaled 8/(2M)) are
+// formed, from the root values in column order of C = 2^(fs_log_radix(logM + 1) - 1)
+// (the root-value kernel with logC = log C); K written out; G and X: H M complex
+// scratch each.  The convolution then takes (K2 = root values, scale 1/(2M);
+// K2o = T, scale 1/8; k2_logC = log C).
+cudaError_t launch_kspec_fourstep_half(int logM, const float2* Khat, float2* K, float2* T, int H, int L,
+                                       float2* G, float2* X, St st, cudaStream_t s);
 
 // Cluster row transforms for longer rows (rows split over C = 2..8 CTAs).
 cudaError_t launch_ifft_cluster(int logM, const float2* Khat, float2* K, int H, int L,

@@ -92,6 +92,8 @@ def test_layer_matches_oracle(wi, nch, full_rows):
     (7, 3, 2, 33, 2), (4, 4, 2, 64, 1), (300, 1, 2, 200, 2), (16, 1, 9, 1000, 3),
     (16, 2, 3, 5000, 2), (4, 1, 3, 6000, 3), (4, 1, 3, 3001, 3), (4, 1, 3, 4000, 3), (12, 1, 2, 16384, 1), (8, 1, 2, 20000, 2),
     (8, 2, 2, 40000, 1),
+    # L = M on long rows: the spectrum's even bins taken from the root values
+    (8, 1, 3, 8192, 3), (6, 2, 2, 32768, 1), (4, 1, 2, 65536, 1),
     # M = 32 and 512 (kspec with staged twiddle tables), M = 2048 (unstaged)
     (6, 1, 3, 20, 3), (8, 1, 3, 300, 2), (8, 2, 2, 2048, 3),
 ])
