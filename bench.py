@@ -61,20 +61,21 @@ FAR_TERMS = 42  # the far-root series' largest number of terms (the library's kF
 
 def cauchy_work(p, w, sms):
     """The root-value kernel's algorithmic flop for one call, as it splits the
-    roots: a CTA of consecutive roots with any root near its channel's poles
-    (|s - c| < 1.5 R) sums directly over the N poles (cauchy_flop per pole and
-    root, for every root of the CTA); the other roots evaluate the series,
-    (r+1)^2 (P - 1) complex multiply-adds of 8 flop plus ~24 flop of set-up
-    each, P the terms their warp takes.  The split is replayed here in float64 from the parameters
-    (the kernel decides in fp32; the two can differ only at a CTA on the
-    boundary).  Returns (flop, fraction of roots summed directly)."""
+    roots: a warp's 32 RPT consecutive roots (RPT roots per thread) with any root
+    near the channel's poles (|s - c| < 1.5 R) sum directly over the N poles
+    (cauchy_flop per pole and root, for every root of the warp); the other roots
+    evaluate the series, (r+1)^2 (P - 1) complex multiply-adds of 8 flop plus ~24
+    flop of set-up each, P the terms their warp takes.  The split is replayed here
+    in float64 from the parameters (the kernel decides in fp32; the two can
+    differ only at a warp on the boundary).  Returns (flop, fraction of roots
+    summed directly)."""
     import numpy as np
     H, N, r, M = w.H, w.N, w.r, w.M
     nw = (r + 1) ** 2
     if M < 8192 or N < 48:  # the library takes the series only on rows of M >= 8192 roots, N >= 48 poles
         return H * M * N * cauchy_flop(r), 1.0
     big = H * M >= 512 * 5 * 2 * sms
-    cta = 128 * (4 if (big and r <= 2) else (2 if r <= 2 else 1))
+    cta = 32 * (4 if (big and r <= 2) else (2 if r <= 2 else 1))  # roots per warp
     k = np.arange(M)
     t = np.tan(np.pi * k / M)
     direct_roots = 0
@@ -100,7 +101,7 @@ def cauchy_work(p, w, sms):
         need = np.clip(np.nan_to_num(need, nan=1.0), 1, FAR_TERMS).astype(int)
         padn = np.ones(nb * cta, int)
         padn[:M] = need
-        warp = padn.reshape(-1, 32).max(axis=1).repeat(32).reshape(nb, cta)
+        warp = padn.reshape(nb, cta).max(axis=1, keepdims=True).repeat(cta, axis=1)
         far_terms += int(warp[blk_far].sum())
     direct_roots = min(direct_roots, H * M)
     far_roots = H * M - direct_roots

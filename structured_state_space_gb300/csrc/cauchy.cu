@@ -298,9 +298,11 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   if (!far_on) st_record_gen(status);  // (else the moments kernel, this call's first, did)
   pdl_launch_dependents();  // the next kernel may start; it waits for this grid before reading
   const int h = blockIdx.x;
-  if (far_on)
+  if (far_on) {
     for (int i = threadIdx.x; i < 2 + NW * FP; i += T)
       mus[i] = ld_chk(mom, (long long)h * kFarStride + i, (long long)gridDim.x * kFarStride);
+    __syncthreads();  // every warp reads c and R below (far_on is uniform)
+  }
   const int M = 1 << logM;
   const float delta = dt[h];
   const bool bad = !(delta > 0.f) || !(delta <= FLT_MAX);
@@ -310,7 +312,9 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   const float a_lo = bad ? 0.f : __fdiv_rn(fmaf(-a_hi, delta, 2.f), delta);
 
   // A tile is RPT T consecutive roots k (so that near and far roots fall in
-  // separate tiles); root k is stored at position (k mod C) M/C + k div C.  The
+  // separate tiles); root k is stored at position (k mod C) M/C + k div C.  With
+  // the far-root series a warp owns 32 RPT consecutive roots of the tile (lane l
+  // takes l, l + 32, ...), so that near and far roots also fall in separate warps.  The
   // CTA takes the tiles of its channel numbered v = blockIdx.y, blockIdx.y +
   // gridDim.y, ..., tile v/2 for even v and tiles - 1 - v/2 for odd v: the roots
   // near the poles lie at the two ends of the range (s = i a tan(pi k/M) small),
@@ -318,8 +322,12 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   // The next tile's tan values are loaded while the current one is computed.
   const int tiles = (M + RPT * T - 1) / (RPT * T);
   auto tile_of = [&](int v) { return (v & 1) ? tiles - 1 - (v >> 1) : (v >> 1); };
+  auto root_of = [&](int tile, int rr) {
+    return FAR ? tile * RPT * T + (int)(threadIdx.x >> 5) * 32 * RPT + rr * 32 + (int)(threadIdx.x & 31)
+               : (tile * RPT + rr) * T + (int)threadIdx.x;
+  };
   auto tan_of = [&](int tile, int rr) {
-    const int kr = (tile * RPT + rr) * T + threadIdx.x;
+    const int kr = root_of(tile, rr);
     return (kr < M && S4_IN(kr << (16 - logM), 65536)) ? __ldg(g_tan + (kr << (16 - logM)))
                                                       : make_float2(0.f, 0.f);
   };
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   float shi[RPT], slo[RPT], th[RPT];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
-    const int kr = (tile * RPT + rr) * T + threadIdx.x;
+    const int kr = root_of(tile, rr);
     const bool valid = kr < M;
     const int k = valid ? kr : 0;
     pos[rr] = valid ? (k & ((1 << logC) - 1)) * Mc + (k >> logC) : M;
@@ -356,20 +364,23 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     for (int rr = 0; rr < RPT; ++rr) tnext[FAR ? rr : 0] = tan_of(tile_of(v + gridDim.y), rr);
   }
   // far roots: |s - c|^2 >= 2.25 R^2 with u = s - c (s = i (shi + slo)); the z = -1
-  // root and positions past M need no sums.  A CTA takes the series only when all
-  // its roots are far; otherwise every root takes the direct sum.
+  // root and positions past M need no sums.  A warp takes the series only when all
+  // its roots are far; otherwise each of its roots takes the direct sum.  The CTA
+  // stages the poles unless all its warps are far.
   const float2 fc = far_on ? mus[0] : make_float2(0.f, 0.f);
   const float fR = far_on ? mus[1].x : 0.f;
   float2 fu[RPT];
-  bool all_far = far_on != 0;
+  bool warp_far = false, cta_far = false;
   if constexpr (FAR) {
+    bool mine = far_on != 0;
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) {
       fu[rr] = make_float2(-fc.x, (shi[rr] - fc.y) + slo[rr]);
       const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
-      all_far = all_far && (pos[rr] >= M || zm1[rr] || (n2u >= kFarRadius2 * fR * fR && n2u > 0.f));
+      mine = mine && (pos[rr] >= M || zm1[rr] || (n2u >= kFarRadius2 * fR * fR && n2u > 0.f));
     }
-    all_far = __syncthreads_and(all_far) != 0;  // (also orders the far constants' loads)
+    warp_far = __all_sync(0xffffffffu, mine);
+    cta_far = __syncthreads_and(warp_far) != 0;
   }
 
   float2 acc[RPT][NW];
@@ -393,7 +404,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     }
   }
 
-  for (int j0 = 0; j0 < (all_far ? 0 : N); j0 += JT) {
+  for (int j0 = 0; j0 < (cta_far ? 0 : N); j0 += JT) {
     const int jn = min(JT, N - j0);
     __syncthreads();
     for (int jj = threadIdx.x; jj < jn; jj += T) {
@@ -440,6 +451,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
       }
     }
     __syncthreads();
+    if (warp_far) continue;  // (a far warp only helps stage the poles)
     if constexpr (PACKED) {
 #pragma unroll kCauchyUnroll
       for (int jj = 0; jj < jn; ++jj) {
@@ -519,7 +531,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   // far roots: the series by Horner's rule, x = R/u, S_w = (1/u) sum_m mu[w][m] x^m,
   // with the terms this warp's roots need: P >= 23 / -log2|x| (one more for the
   // approximate logarithm), at most FP
-  if (FAR && all_far) {
+  if (FAR && warp_far) {
     float2 iu[RPT], xx[RPT];
     int pneed = 1;
 #pragma unroll
@@ -547,33 +559,40 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
         x2y[pr] = make_float2(xx[2 * pr].y, xx[2 * pr + 1].y);
         n2y[pr] = make_float2(-x2y[pr].x, -x2y[pr].y);
       }
+      // all weights' chains advance together: NW NPR independent chains per step
+      // (one weight after another measured 2 % slower on N=256 H=1024 M=65536)
+      float2 hx[NW][NPR], hy[NW][NPR];
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        float2 hx[NPR], hy[NPR];
         const float2 top = mus[2 + w * FP + P - 1];
 #pragma unroll
         for (int pr = 0; pr < NPR; ++pr) {
-          hx[pr] = make_float2(top.x, top.x);
-          hy[pr] = make_float2(top.y, top.y);
+          hx[w][pr] = make_float2(top.x, top.x);
+          hy[w][pr] = make_float2(top.y, top.y);
         }
-#pragma unroll 4
-        for (int m = P - 2; m >= 0; --m) {
+      }
+#pragma unroll 2
+      for (int m = P - 2; m >= 0; --m) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
           const float2 mu = mus[2 + w * FP + m];
           const float2 mx = make_float2(mu.x, mu.x), my = make_float2(mu.y, mu.y);
 #pragma unroll
           for (int pr = 0; pr < NPR; ++pr) {
-            const float2 nx = __ffma2_rn(hx[pr], x2x[pr], __ffma2_rn(hy[pr], n2y[pr], mx));
-            const float2 ny = __ffma2_rn(hx[pr], x2y[pr], __ffma2_rn(hy[pr], x2x[pr], my));
-            hx[pr] = nx;
-            hy[pr] = ny;
+            const float2 nx = __ffma2_rn(hx[w][pr], x2x[pr], __ffma2_rn(hy[w][pr], n2y[pr], mx));
+            const float2 ny = __ffma2_rn(hx[w][pr], x2y[pr], __ffma2_rn(hy[w][pr], x2x[pr], my));
+            hx[w][pr] = nx;
+            hy[w][pr] = ny;
           }
         }
+      }
+#pragma unroll
+      for (int w = 0; w < NW; ++w)
 #pragma unroll
         for (int pr = 0; pr < NPR; ++pr) {
-          acc[2 * pr][w] = cmul(make_float2(hx[pr].x, hy[pr].x), iu[2 * pr]);
-          acc[2 * pr + 1][w] = cmul(make_float2(hx[pr].y, hy[pr].y), iu[2 * pr + 1]);
+          acc[2 * pr][w] = cmul(make_float2(hx[w][pr].x, hy[w][pr].x), iu[2 * pr]);
+          acc[2 * pr + 1][w] = cmul(make_float2(hx[w][pr].y, hy[w][pr].y), iu[2 * pr + 1]);
         }
-      }
     } else {
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
@@ -596,7 +615,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
   // when the pole loop was skipped, else the loop's sum
   float2 cb_all;
-  if (FAR && all_far) {
+  if (FAR && cta_far) {
     cb_all = mus[2];
   } else {
 #pragma unroll
@@ -625,7 +644,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
       } else {
         // (far tiles cannot meet a resonance: a non-finite value there shows in Hk)
         bool fin = true;
-        if (!(FAR && all_far)) {
+        if (!(FAR && warp_far)) {
 #pragma unroll
           for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
         }
