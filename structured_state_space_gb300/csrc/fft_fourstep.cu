@@ -58,10 +58,21 @@
 // The column kernel then reads the spectrum's bin k = k1 + R k2 of its column from
 // the root values (k1 even) or from T (k1 odd), at j = k div 2 = k1/2 + C k2: one
 // contiguous column of either array.
+// (light twiddle loads only in the passes of P >= 256 here; see s4_fft.cuh)
+#ifndef S4_TW_LIGHT_MINP
+#define S4_TW_LIGHT_MINP 256
+#endif
 #include "s4_fft.cuh"
 #include "s4_internal.h"
 
 namespace s4dev {
+
+// Build-time tuning: the column kernel reads its input cached in L2 only (1), which
+// keeps L1 for the twiddle tables (1140 -> 1098 us with the light loads on N=256
+// H=1024 L=65536), or as streaming data (0).
+#ifndef S4_FS_XCG
+#define S4_FS_XCG 1
+#endif
 
 constexpr int kFsThreads = 256;  // threads per CTA of the across-column kernels
 constexpr int kKsRadix = 16;     // across-column radix of the layer path's M-point inverse
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
 #pragma unroll
       for (int qq = 0; qq < RA; ++qq)
         a[qq] = (act && S4_IN((long long)p * n + (long long)k1 * m + i + qq * NB0, (long long)pb * H * n))
-                    ? __ldcs(xc + i + qq * NB0) : make_float2(0.f, 0.f);
+                    ? (S4_FS_XCG ? __ldcg(xc + i + qq * NB0) : __ldcs(xc + i + qq * NB0)) : make_float2(0.f, 0.f);
       dft<RA, false>(a);
 #pragma unroll
       for (int qq = 0; qq < RA; ++qq) st_chk(bufA, IXF0::wr(i, qq), C::PADM, a[qq]);

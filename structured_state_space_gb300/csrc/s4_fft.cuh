@@ -29,6 +29,21 @@ struct PassIdx {
   }
 };
 
+// Build-time tuning: read only the first two powers of a butterfly's factors
+// from the "rows" tables and form the others by products (1), or read all (0),
+// for passes with at least S4_TW_LIGHT_MINP butterfly indices P.  A quarter of
+// the table's bytes stays hot in L1 at the price of R - 3 complex products; on
+// GB300 the row kernels gained 3-8 % from it (inverse transforms of 4096
+// points 185.8 -> 175.0 us on N=256 H=1024 L=65536), the 4096-point column
+// kernel only for its P = 256 passes (1140 -> 1115 us; with every pass light the
+// 2048-point columns lost 4 %).
+#ifndef S4_TW_LIGHT
+#define S4_TW_LIGHT 1
+#endif
+#ifndef S4_TW_LIGHT_MINP
+#define S4_TW_LIGHT_MINP 1
+#endif
+
 // Twiddle factors of pass IDX for butterfly k, applied to a[1..R-1]
 // (conjugated for an inverse pass).  `w` is filled from the table first so
 // several rows that share the butterfly index can reuse it.  With SMEM the
@@ -46,7 +61,17 @@ struct PassTw {
   // w[q] = w^(k q) for q = 1..R-1
   template <bool SMEM = false>
   __device__ __forceinline__ static void load(float2 (&w)[R], int k, const float2* sm = nullptr) {
-    if constexpr (ROWS) {
+    if constexpr (ROWS && S4_TW_LIGHT && !SMEM && R > 4 && P >= S4_TW_LIGHT_MINP) {
+      // the first word of butterfly k's entry (w^k, w^2k), the other powers by products
+      const float4 t = __ldg(reinterpret_cast<const float4*>(table()) + k);
+      w[1] = make_float2(t.x, t.y);
+      w[2] = make_float2(t.z, t.w);
+#pragma unroll
+      for (int q = 3; q < R; ++q) {
+        const int hb = highbit(q);
+        w[q] = (hb == q) ? cmul(w[q / 2], w[q / 2]) : cmul(w[hb], w[q - hb]);
+      }
+    } else if constexpr (ROWS) {
       const float4* col = reinterpret_cast<const float4*>(SMEM ? sm : table()) + k;
 #pragma unroll
       for (int v = 0; v < R / 2; ++v) {
