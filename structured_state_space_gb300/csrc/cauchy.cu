@@ -117,7 +117,11 @@ __device__ __forceinline__ bool solve_small(float2 (&W)[R][R], float2 (&v)[R]) {
 
 // ---- far-field constants of a channel ---------------------------------------------
 using s4impl::kFarTerms;   // series terms kept at most
-using s4impl::kFarStride;  // float2 entries per channel: [c, (R, 0), mu[w][m]]
+using s4impl::kFarStride;  // float2 entries of the whole set: [c, (R, 0), mu[w][m]]
+using s4impl::kFarChannel;  // float2 entries per channel: whole set, groups, permutation
+using s4impl::kFarGroups;
+using s4impl::kFarGStride;
+using s4impl::kFarPermMax;
 constexpr float kFarRadius2 = 2.25f;  // far: |s - c|^2 >= (1.5 R)^2
 
 __device__ __forceinline__ float2 far_weight(int widx, int RANKv, float2 c, float2 b, const float2* p,
@@ -232,15 +236,308 @@ __global__ void __launch_bounds__(256) cauchy_moments_kernel(
       }
     }
   }
-  float2* out = mom + (size_t)h * kFarStride;
+  float2* out = mom + (size_t)h * kFarChannel;
+  const long long nout = (long long)gridDim.x * kFarChannel;
   if (tid == 0) {
-    out[0] = c;
-    out[1] = make_float2(R, 0.f);
+    st_chk(out, 0, nout - (long long)h * kFarChannel, c);
+    st_chk(out, 1, nout - (long long)h * kFarChannel, make_float2(R, 0.f));
   }
 #pragma unroll
   for (int o = 0; o < OWN; ++o) {
     const int t = tid + o * T;
-    if (t < NW * P) out[2 + t] = acc[o];
+    if (t < NW * P) st_chk(out, 2 + t, nout - (long long)h * kFarChannel, acc[o]);
+  }
+}
+
+// Rank 1 with the series' second level (N <= kFarPermMax poles): one CTA per
+// channel.  The poles fall into kFarGroups groups of equal width in imaginary part
+// (between the smallest and largest), numbered in that order and, within a group,
+// by pole index; the rank is a pole's position in that order.  The CTA writes the
+// whole set's constants, each group's centre, radius (its start rank in the
+// imaginary slot) and moments, and the poles by rank.  The five sets' moments
+// accumulate over the poles in rank order, one thread per (set, m) with the 4
+// weights in registers.
+__global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
+    const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
+    const float2* __restrict__ Bv, const float2* __restrict__ Ct, int N, float2* __restrict__ mom, St status) {
+  constexpr int NW = 4, P = kFarTerms, T = 256, G = kFarGroups, NS = 1 + G, JC = 32, PPT = kFarPermMax / T;
+  __shared__ float2 sl[kFarPermMax];       // poles by rank
+  __shared__ float4 sw[kFarPermMax][2];    // their 4 weights by rank
+  __shared__ unsigned char sgid[kFarPermMax];
+  __shared__ short sloc[kFarPermMax];      // place within the group (by pole index)
+  __shared__ int sperm[kFarPermMax];
+  __shared__ int sstart[G + 1];
+  __shared__ float scr[NS][3];             // centre and radius of each set (0: all poles)
+  __shared__ float sred[T / 32][4];
+  __shared__ float2 pw0[JC][P], pwg[JC][P];  // powers of a chunk's poles about the whole set / their group
+  __shared__ int sgrp[JC];
+  pdl_wait();
+  st_record_gen(status);
+  pdl_launch_dependents();
+  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  const long long nj = (long long)gridDim.x * N;
+  // this thread's poles j = tid + q T in registers; the whole set's bounding box
+  float2 lr[PPT], wr[PPT][NW];
+  float b0 = INFINITY, b1 = -INFINITY, b2 = INFINITY, b3 = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < PPT; ++q) {
+    const int j = tid + q * T;
+    if (j >= N) continue;
+    const long long jg = (long long)h * N + j;
+    lr[q] = ld_chk(Lambda, jg, nj);
+    float2 pp[1] = {ld_chk(Pm, jg, nj)}, qq[1] = {ld_chk(Qm, jg, nj)};
+    const float2 bj = ld_chk(Bv, jg, nj), cj = ld_chk(Ct, jg, nj);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) wr[q][w] = far_weight(w, 1, cj, bj, pp, qq);
+    b0 = fminf(b0, lr[q].x); b1 = fmaxf(b1, lr[q].x); b2 = fminf(b2, lr[q].y); b3 = fmaxf(b3, lr[q].y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    b0 = fminf(b0, __shfl_xor_sync(0xffffffffu, b0, o));
+    b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, o));
+    b2 = fminf(b2, __shfl_xor_sync(0xffffffffu, b2, o));
+    b3 = fmaxf(b3, __shfl_xor_sync(0xffffffffu, b3, o));
+  }
+  if (lane == 0) { sred[wp][0] = b0; sred[wp][1] = b1; sred[wp][2] = b2; sred[wp][3] = b3; }
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 1; i < T / 32; ++i) {
+      b0 = fminf(b0, sred[i][0]); b1 = fmaxf(b1, sred[i][1]); b2 = fminf(b2, sred[i][2]); b3 = fmaxf(b3, sred[i][3]);
+    }
+    sred[0][0] = b0; sred[0][1] = b1; sred[0][2] = b2; sred[0][3] = b3;
+  }
+  __syncthreads();
+  const float ylo = sred[0][2], yhi = sred[0][3];
+  const float gscale = yhi > ylo ? (float)G / (yhi - ylo) : 0.f;
+#pragma unroll
+  for (int q = 0; q < PPT; ++q) {
+    const int j = tid + q * T;
+    if (j >= N) continue;
+    const float gf = (lr[q].y - ylo) * gscale;  // (NaN: group 0)
+    sgid[j] = (unsigned char)(gf >= 1.f ? min((int)gf, G - 1) : 0);
+  }
+  __syncthreads();
+  if (wp == 0) {  // stable counting by group: place of each pole within its group, group starts
+    int cnt[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) cnt[g] = 0;
+    for (int j0 = 0; j0 < N; j0 += 32) {
+      const int j = j0 + lane;
+      const int g = j < N ? sgid[j] : -1;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        const unsigned b = __ballot_sync(0xffffffffu, g == gg);
+        if (g == gg) sloc[j] = (short)(cnt[gg] + __popc(b & ((1u << lane) - 1u)));
+        cnt[gg] += __popc(b);
+      }
+    }
+    if (lane == 0) {
+      int acc = 0;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sstart[g] = acc;
+        acc += cnt[g];
+      }
+      sstart[G] = acc;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < PPT; ++q) {
+    const int j = tid + q * T;
+    if (j >= N) continue;
+    const int rk = sstart[sgid[j]] + sloc[j];
+    if (!S4_IN(rk, kFarPermMax)) continue;
+    sperm[rk] = j;
+    sl[rk] = lr[q];
+    sw[rk][0] = make_float4(wr[q][0].x, wr[q][0].y, wr[q][1].x, wr[q][1].y);
+    sw[rk][1] = make_float4(wr[q][2].x, wr[q][2].y, wr[q][3].x, wr[q][3].y);
+  }
+  __syncthreads();
+  // warp 0: the whole set's centre and radius; warps 1..G: group wp - 1
+  if (wp <= G) {
+    const int lo = wp == 0 ? 0 : sstart[wp - 1], hi = wp == 0 ? N : sstart[wp];
+    float a0 = INFINITY, a1 = -INFINITY, a2 = INFINITY, a3 = -INFINITY;
+    for (int rk = lo + lane; rk < hi; rk += 32) {
+      const float2 l = sl[rk];
+      a0 = fminf(a0, l.x); a1 = fmaxf(a1, l.x); a2 = fminf(a2, l.y); a3 = fmaxf(a3, l.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a0 = fminf(a0, __shfl_xor_sync(0xffffffffu, a0, o));
+      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, o));
+      a2 = fminf(a2, __shfl_xor_sync(0xffffffffu, a2, o));
+      a3 = fmaxf(a3, __shfl_xor_sync(0xffffffffu, a3, o));
+    }
+    const float c0 = hi > lo ? 0.5f * (a0 + a1) : 0.f, c1 = hi > lo ? 0.5f * (a2 + a3) : 0.f;
+    float q2 = 0.f;
+    for (int rk = lo + lane; rk < hi; rk += 32) {
+      const float2 l = sl[rk];
+      const float dx = l.x - c0, dy = l.y - c1;
+      q2 = fmaxf(q2, fmaf(dx, dx, dy * dy));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q2 = fmaxf(q2, __shfl_xor_sync(0xffffffffu, q2, o));
+    if (lane == 0) {
+      const float Rq = sqrtf(q2);
+      scr[wp][0] = c0;
+      scr[wp][1] = c1;
+      scr[wp][2] = (Rq > 0.f && Rq <= FLT_MAX) ? Rq : 1.f;
+    }
+  }
+  __syncthreads();
+  // moments: thread (set, m) for set < NS, m < P, the 4 weights at once
+  const int set = tid / P, m = tid % P;
+  const bool mine = set < NS;
+  const int lo = set == 0 ? 0 : (mine ? sstart[set - 1] : 0), hi = set == 0 ? N : (mine ? sstart[set] : 0);
+  float2 acc[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) acc[w] = make_float2(0.f, 0.f);
+  for (int r0 = 0; r0 < N; r0 += JC) {
+    const int jn = min(JC, N - r0);
+    __syncthreads();
+    if (tid < 2 * jn) {  // powers of chunk pole c about the whole set (first half) or its group
+      const int c = tid < jn ? tid : tid - jn, rk = r0 + c;
+      int g = 0;
+      while (g + 1 < G && sstart[g + 1] <= rk) ++g;
+      const int st = tid < jn ? 0 : 1 + g;
+      const float2 l = sl[rk];
+      const float ir = 1.f / scr[st][2];
+      const float2 rho = make_float2((l.x - scr[st][0]) * ir, (l.y - scr[st][1]) * ir);
+      float2* dst = tid < jn ? pw0[c] : pwg[c];
+      float2 pwr = make_float2(1.f, 0.f);
+#pragma unroll
+      for (int mm = 0; mm < P; ++mm) {
+        dst[mm] = pwr;
+        pwr = cmul(pwr, rho);
+      }
+    }
+    __syncthreads();
+    if (!mine) continue;
+    const int jlo = max(lo - r0, 0), jhi = min(hi - r0, jn);
+    for (int jj = jlo; jj < jhi; ++jj) {
+      const float2 y = set == 0 ? pw0[jj][m] : pwg[jj][m];
+      const float4 x01 = sw[r0 + jj][0], x23 = sw[r0 + jj][1];
+      const float2 x[NW] = {make_float2(x01.x, x01.y), make_float2(x01.z, x01.w), make_float2(x23.x, x23.y),
+                            make_float2(x23.z, x23.w)};
+#pragma unroll
+      for (int w = 0; w < NW; ++w)
+        acc[w] = make_float2(fmaf(x[w].x, y.x, fmaf(-x[w].y, y.y, acc[w].x)),
+                             fmaf(x[w].x, y.y, fmaf(x[w].y, y.x, acc[w].y)));
+    }
+  }
+  // [whole set: c, (R, 0), mu[w][m] (room for rank 4)] [group g: c, (R, start), mu[w][m]] [poles by rank]
+  float2* out = mom + (size_t)h * kFarChannel;
+  const long long nout = (long long)kFarChannel;
+  if (tid < NS) {
+    const long long base = tid == 0 ? 0 : kFarStride + (long long)(tid - 1) * kFarGStride;
+    st_chk(out, base, nout, make_float2(scr[tid][0], scr[tid][1]));
+    st_chk(out, base + 1, nout, make_float2(scr[tid][2], tid == 0 ? 0.f : (float)sstart[tid - 1]));
+  }
+  if (mine) {
+    const long long base = set == 0 ? 0 : kFarStride + (long long)(set - 1) * kFarGStride;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) st_chk(out, base + 2 + w * P + m, nout, acc[w]);
+  }
+  int* outp = reinterpret_cast<int*>(out + kFarStride + G * kFarGStride);
+  for (int rk = tid; rk < N; rk += T)
+    if (S4_IN(kFarStride + G * kFarGStride + rk / 2, kFarChannel)) outp[rk] = sperm[rk];
+}
+
+// The far-field series of the weight sums at this thread's roots s = i (shi + slo):
+// with u = s - cen and x = Rr/u, S_w = (1/u) sum_m mu[w FP + m] x^m by Horner's rule,
+// with the terms the warp's roots need (P >= 23 / -log2|x|, one more for the
+// approximate logarithm, at most FP; roots with live[rr] false do not count).
+// Written into acc (ADD false) or added to it.  Called by whole warps.
+template <int NW, int RPT, bool PACKED, int FP, bool ADD>
+__device__ __forceinline__ void far_series(const float2* __restrict__ mu, float2 cen, float Rr,
+                                           const float (&shi)[RPT], const float (&slo)[RPT],
+                                           const bool (&live)[RPT], float2 (&acc)[RPT][NW]) {
+  float2 iu[RPT], xx[RPT];
+  int pneed = 1;
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    const float2 u = make_float2(-cen.x, (shi[rr] - cen.y) + slo[rr]);
+    const float n2u = fmaf(u.x, u.x, u.y * u.y);
+    // 1/|u|^2 to within an ulp or two (the approximate reciprocal), which the
+    // series inherits as a relative error of the same size
+    const float r = n2u > 0.f ? rcp_approx(n2u) : 0.f;
+    iu[rr] = make_float2(u.x * r, -u.y * r);
+    xx[rr] = cscale(iu[rr], Rr);
+    const float ax2 = Rr * Rr * r;  // |x|^2 <= 1/2.25 on a far root
+    if (live[rr] && ax2 > 0.f) {
+      const float p = 23.f * rcp_approx(-0.5f * __log2f(ax2));
+      pneed = max(pneed, min(FP, (int)p + 2));
+    }
+  }
+  const int P = __reduce_max_sync(0xffffffffu, (unsigned)pneed);
+  if constexpr (PACKED) {
+    constexpr int NPR = RPT / 2;
+    // root pairs in packed fp32x2: hx = {Re h of root 2pr, of root 2pr+1}, hy likewise;
+    // each step is the scalar step below, operation for operation
+    float2 x2x[NPR], x2y[NPR], n2y[NPR];
+#pragma unroll
+    for (int pr = 0; pr < NPR; ++pr) {
+      x2x[pr] = make_float2(xx[2 * pr].x, xx[2 * pr + 1].x);
+      x2y[pr] = make_float2(xx[2 * pr].y, xx[2 * pr + 1].y);
+      n2y[pr] = make_float2(-x2y[pr].x, -x2y[pr].y);
+    }
+    // all weights' chains advance together: NW NPR independent chains per step
+    // (one weight after another measured 2 % slower on N=256 H=1024 M=65536)
+    float2 hx[NW][NPR], hy[NW][NPR];
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float2 top = mu[w * FP + P - 1];
+#pragma unroll
+      for (int pr = 0; pr < NPR; ++pr) {
+        hx[w][pr] = make_float2(top.x, top.x);
+        hy[w][pr] = make_float2(top.y, top.y);
+      }
+    }
+#pragma unroll 2
+    for (int m = P - 2; m >= 0; --m) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float2 mv = mu[w * FP + m];
+        const float2 mx = make_float2(mv.x, mv.x), my = make_float2(mv.y, mv.y);
+#pragma unroll
+        for (int pr = 0; pr < NPR; ++pr) {
+          const float2 nx = __ffma2_rn(hx[w][pr], x2x[pr], __ffma2_rn(hy[w][pr], n2y[pr], mx));
+          const float2 ny = __ffma2_rn(hx[w][pr], x2y[pr], __ffma2_rn(hy[w][pr], x2x[pr], my));
+          hx[w][pr] = nx;
+          hy[w][pr] = ny;
+        }
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+#pragma unroll
+      for (int pr = 0; pr < NPR; ++pr) {
+        const float2 v0 = cmul(make_float2(hx[w][pr].x, hy[w][pr].x), iu[2 * pr]);
+        const float2 v1 = cmul(make_float2(hx[w][pr].y, hy[w][pr].y), iu[2 * pr + 1]);
+        acc[2 * pr][w] = ADD ? cadd(acc[2 * pr][w], v0) : v0;
+        acc[2 * pr + 1][w] = ADD ? cadd(acc[2 * pr + 1][w], v1) : v1;
+      }
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      float2 hw[RPT];
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) hw[rr] = mu[w * FP + P - 1];
+#pragma unroll 4
+      for (int m = P - 2; m >= 0; --m) {
+        const float2 mv = mu[w * FP + m];
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr)
+          hw[rr] = make_float2(fmaf(hw[rr].x, xx[rr].x, fmaf(-hw[rr].y, xx[rr].y, mv.x)),
+                               fmaf(hw[rr].x, xx[rr].y, fmaf(hw[rr].y, xx[rr].x, mv.y)));
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) {
+        const float2 v = cmul(hw[rr], iu[rr]);
+        acc[rr][w] = ADD ? cadd(acc[rr][w], v) : v;
+      }
+    }
   }
 }
 
@@ -277,13 +574,15 @@ struct CauchyLayout {
 #endif
 // FAR: the far-root series is compiled in (it is used when `far_on` and the
 // constants are given); without it the kernel is the direct sum alone.
-template <int RANK, int RPT, int T, bool PACKED = false, bool FAR = false>
+// GRP: the second level of the series is compiled in (used when `grouped`: the
+// moments kernel formed the groups and the permutation for this call).
+template <int RANK, int RPT, int T, bool PACKED = false, bool FAR = false, bool GRP = false>
 __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MINB_FAR2 : S4_CAUCHY_MINB) : 0)
     cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
-    float2* __restrict__ Khat, const float2* __restrict__ mom, int far_on, int N, int logM, int logC,
-    St status) {
+    float2* __restrict__ Khat, const float2* __restrict__ mom, int far_on, int grouped, int N, int logM,
+    int logC, St status) {
   using Lay = CauchyLayout<RANK, PACKED>;
   constexpr int NW = Lay::NW, PS = Lay::PS, JT = Lay::JT;
   static_assert(!PACKED || RPT % 2 == 0, "packed roots come in pairs");
@@ -292,15 +591,20 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   __shared__ __align__(16) float par[JT * PS];
   __shared__ float2 mus[2 + NW * FP];  // c, (R, 0), mu[w][m] of this channel
   __shared__ float2 red[T / 32 + 1];
+  // the groups' constants [c_g, (R_g, 0), mu_g[w][m]], loaded at the first near tile
+  __shared__ float2 musg[GRP ? kFarGroups * kFarGStride : 1];
+  static_assert(!GRP || (FAR && RANK == 1), "groups: rank 1 with the series");
 
   if constexpr (!FAR) far_on = 0;
+  if constexpr (!GRP) grouped = 0;
+  grouped = far_on ? grouped : 0;
   pdl_wait();  // the moments kernel (and whatever ran before it) is done
   if (!far_on) st_record_gen(status);  // (else the moments kernel, this call's first, did)
   pdl_launch_dependents();  // the next kernel may start; it waits for this grid before reading
   const int h = blockIdx.x;
   if (far_on) {
     for (int i = threadIdx.x; i < 2 + NW * FP; i += T)
-      mus[i] = ld_chk(mom, (long long)h * kFarStride + i, (long long)gridDim.x * kFarStride);
+      mus[i] = ld_chk(mom, (long long)h * kFarChannel + i, (long long)gridDim.x * kFarChannel);
     __syncthreads();  // every warp reads c and R below (far_on is uniform)
   }
   const int M = 1 << logM;
@@ -337,6 +641,9 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     for (int rr = 0; rr < RPT; ++rr) tnext[rr] = tan_of(tile_of(blockIdx.y), rr);
   }
   unsigned flags = bad ? ST_BAD_STEP : 0u;
+  bool groups_loaded = false;
+  const int* permh = reinterpret_cast<const int*>(mom + (size_t)h * kFarChannel + kFarStride +
+                                                  kFarGroups * kFarGStride);
   for (int v = blockIdx.y; v < tiles; v += gridDim.y) {
   const int tile = tile_of(v);
   int pos[RPT];
@@ -382,6 +689,34 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     warp_far = __all_sync(0xffffffffu, mine);
     cta_far = __syncthreads_and(warp_far) != 0;
   }
+  // a near warp of a grouped channel: bit g of gnear when some root of the warp is
+  // near group g (|s - c_g| < 1.5 R_g); it sums directly over those groups' poles only
+  unsigned gnear = 0u;
+  if constexpr (GRP) {
+    if (grouped && !cta_far) {
+      if (!groups_loaded) {  // (uniform)
+        for (int i = threadIdx.x; i < kFarGroups * kFarGStride; i += T)
+          musg[i] = ld_chk(mom, (long long)h * kFarChannel + kFarStride + i, (long long)gridDim.x * kFarChannel);
+        groups_loaded = true;
+        __syncthreads();
+      }
+      if (!warp_far) {
+#pragma unroll
+        for (int g = 0; g < kFarGroups; ++g) {
+          const float2 cg = musg[g * kFarGStride];
+          const float Rg = musg[g * kFarGStride + 1].x;
+          bool gfar = true;
+#pragma unroll
+          for (int rr = 0; rr < RPT; ++rr) {
+            const float2 u = make_float2(-cg.x, (shi[rr] - cg.y) + slo[rr]);
+            const float n2 = fmaf(u.x, u.x, u.y * u.y);
+            gfar = gfar && (pos[rr] >= M || zm1[rr] || (n2 >= kFarRadius2 * Rg * Rg && n2 > 0.f));
+          }
+          if (!__all_sync(0xffffffffu, gfar)) gnear |= 1u << g;
+        }
+      }
+    }
+  }
 
   float2 acc[RPT][NW];
 #pragma unroll
@@ -408,7 +743,13 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     const int jn = min(JT, N - j0);
     __syncthreads();
     for (int jj = threadIdx.x; jj < jn; jj += T) {
-      const size_t j = (size_t)h * N + j0 + jj;
+      // (grouped: the poles in rank order, so that each group is one range)
+      const int jp = (GRP && grouped && S4_IN((long long)h * kFarChannel + kFarStride + kFarGroups * kFarGStride +
+                                                  (j0 + jj) / 2,
+                                              (long long)gridDim.x * kFarChannel))
+                         ? __ldg(permh + j0 + jj)
+                         : j0 + jj;
+      const size_t j = (size_t)h * N + jp;
       const long long nj = (long long)gridDim.x * N;  // H N
       if (!S4_IN(j, nj) || !S4_IN((long long)j * RANK + RANK - 1, nj * RANK) || !S4_IN(jj * PS + PS - 1, JT * PS))
         continue;
@@ -453,8 +794,16 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
     __syncthreads();
     if (warp_far) continue;  // (a far warp only helps stage the poles)
     if constexpr (PACKED) {
+      // the staged poles this warp sums over: all, or the ranges of its near groups
+      for (int g = 0; g < (GRP && grouped ? kFarGroups : 1); ++g) {
+      int jlo = 0, jhi = jn;
+      if (GRP && grouped) {
+        if (!((gnear >> g) & 1u)) continue;
+        jlo = max((int)musg[g * kFarGStride + 1].y - j0, 0);
+        jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * kFarGStride + 1].y : N) - j0, jn);
+      }
 #pragma unroll kCauchyUnroll
-      for (int jj = 0; jj < jn; ++jj) {
+      for (int jj = jlo; jj < jhi; ++jj) {
         const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
         const float4 pl = p4[0];
         const float2 nim = make_float2(pl.x, pl.y), re2 = make_float2(pl.z, pl.w);
@@ -487,6 +836,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
           }
         }
       }
+      }  // groups
       continue;
     }
 #pragma unroll kCauchyUnroll
@@ -528,88 +878,20 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
       }
   }
 
-  // far roots: the series by Horner's rule, x = R/u, S_w = (1/u) sum_m mu[w][m] x^m,
-  // with the terms this warp's roots need: P >= 23 / -log2|x| (one more for the
-  // approximate logarithm), at most FP
-  if (FAR && warp_far) {
-    float2 iu[RPT], xx[RPT];
-    int pneed = 1;
+  // far warps: the series of the whole set; near warps of a grouped channel: the
+  // series of each group they are far from, added to the direct sums of the others
+  if (FAR && (warp_far || (GRP && grouped))) {
+    bool live[RPT];
 #pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) {
-      const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
-      // 1/|u|^2 to within an ulp or two (the approximate reciprocal), which the
-      // series inherits as a relative error of the same size
-      const float r = n2u > 0.f ? rcp_approx(n2u) : 0.f;
-      iu[rr] = make_float2(fu[rr].x * r, -fu[rr].y * r);
-      xx[rr] = cscale(iu[rr], fR);
-      const float ax2 = fR * fR * r;  // |x|^2 <= 1/2.25 on a far root
-      if (pos[rr] < M && !zm1[rr] && ax2 > 0.f) {
-        const float p = 23.f * rcp_approx(-0.5f * __log2f(ax2));
-        pneed = max(pneed, min(FP, (int)p + 2));
-      }
-    }
-    const int P = __reduce_max_sync(0xffffffffu, (unsigned)pneed);
-    if constexpr (PACKED) {
-      // root pairs in packed fp32x2: hx = {Re h of root 2pr, of root 2pr+1}, hy likewise;
-      // each step is the scalar step below, operation for operation
-      float2 x2x[NPR], x2y[NPR], n2y[NPR];
+    for (int rr = 0; rr < RPT; ++rr) live[rr] = pos[rr] < M && !zm1[rr];
+    if (warp_far) {
+      far_series<NW, RPT, PACKED, FP, false>(mus + 2, fc, fR, shi, slo, live, acc);
+    } else if constexpr (GRP) {
 #pragma unroll
-      for (int pr = 0; pr < NPR; ++pr) {
-        x2x[pr] = make_float2(xx[2 * pr].x, xx[2 * pr + 1].x);
-        x2y[pr] = make_float2(xx[2 * pr].y, xx[2 * pr + 1].y);
-        n2y[pr] = make_float2(-x2y[pr].x, -x2y[pr].y);
-      }
-      // all weights' chains advance together: NW NPR independent chains per step
-      // (one weight after another measured 2 % slower on N=256 H=1024 M=65536)
-      float2 hx[NW][NPR], hy[NW][NPR];
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float2 top = mus[2 + w * FP + P - 1];
-#pragma unroll
-        for (int pr = 0; pr < NPR; ++pr) {
-          hx[w][pr] = make_float2(top.x, top.x);
-          hy[w][pr] = make_float2(top.y, top.y);
-        }
-      }
-#pragma unroll 2
-      for (int m = P - 2; m >= 0; --m) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float2 mu = mus[2 + w * FP + m];
-          const float2 mx = make_float2(mu.x, mu.x), my = make_float2(mu.y, mu.y);
-#pragma unroll
-          for (int pr = 0; pr < NPR; ++pr) {
-            const float2 nx = __ffma2_rn(hx[w][pr], x2x[pr], __ffma2_rn(hy[w][pr], n2y[pr], mx));
-            const float2 ny = __ffma2_rn(hx[w][pr], x2y[pr], __ffma2_rn(hy[w][pr], x2x[pr], my));
-            hx[w][pr] = nx;
-            hy[w][pr] = ny;
-          }
-        }
-      }
-#pragma unroll
-      for (int w = 0; w < NW; ++w)
-#pragma unroll
-        for (int pr = 0; pr < NPR; ++pr) {
-          acc[2 * pr][w] = cmul(make_float2(hx[w][pr].x, hy[w][pr].x), iu[2 * pr]);
-          acc[2 * pr + 1][w] = cmul(make_float2(hx[w][pr].y, hy[w][pr].y), iu[2 * pr + 1]);
-        }
-    } else {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        float2 hw[RPT];
-#pragma unroll
-        for (int rr = 0; rr < RPT; ++rr) hw[rr] = mus[2 + w * FP + P - 1];
-#pragma unroll 4
-        for (int m = P - 2; m >= 0; --m) {
-          const float2 mu = mus[2 + w * FP + m];
-#pragma unroll
-          for (int rr = 0; rr < RPT; ++rr)
-            hw[rr] = make_float2(fmaf(hw[rr].x, xx[rr].x, fmaf(-hw[rr].y, xx[rr].y, mu.x)),
-                                 fmaf(hw[rr].x, xx[rr].y, fmaf(hw[rr].y, xx[rr].x, mu.y)));
-        }
-#pragma unroll
-        for (int rr = 0; rr < RPT; ++rr) acc[rr][w] = cmul(hw[rr], iu[rr]);
-      }
+      for (int g = 0; g < kFarGroups; ++g)
+        if (!((gnear >> g) & 1u))
+          far_series<NW, RPT, PACKED, FP, true>(musg + g * kFarGStride + 2, musg[g * kFarGStride],
+                                                musg[g * kFarGStride + 1].x, shi, slo, live, acc);
     }
   }
   // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
@@ -729,9 +1011,13 @@ S4_OOB_COUNTER(oob_cauchy)
 #ifndef S4_CAUCHY_FAR_TILES
 #define S4_CAUCHY_FAR_TILES 4
 #endif
+// The far series' second level (pole groups) for near warps (1) or none (0).
+#ifndef S4_CAUCHY_GROUPS
+#define S4_CAUCHY_GROUPS 1
+#endif
 
 
-template <int RANK, int RPT, bool PACKED, bool FAR>
+template <int RANK, int RPT, bool PACKED, bool FAR, bool GRP = false>
 static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, const float2* Q,
                                      const float2* B, const float2* Ct, const float* dt,
                                      float2* Khat, const float2* mom, int H, int N, int M, int logC, St status,
@@ -740,8 +1026,8 @@ static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, cons
   const int tiles = (M + T * RPT - 1) / (T * RPT);
   static int per_sm = -1;  // resident CTAs per SM (queried once per instantiation)
   if (per_sm < 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, T, 0) !=
-          cudaSuccess)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_kernel<RANK, RPT, T, PACKED, FAR, GRP>, T,
+                                                    0) != cudaSuccess)
     per_sm = 0;
   // With the far-root series, a CTA loops over up to S4_CAUCHY_FAR_TILES tiles of
   // its channel (most of them cheap series tiles, which would otherwise each pay a
@@ -772,16 +1058,22 @@ static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, cons
   cfg.stream = s;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T, PACKED, FAR>, Lambda, P, Q, B, Ct, dt, Khat, mom,
-                            mom ? 1 : 0, N, logM, logC, status);
+  return cudaLaunchKernelEx(&cfg, cauchy_kernel<RANK, RPT, T, PACKED, FAR, GRP>, Lambda, P, Q, B, Ct, dt, Khat,
+                            mom, mom ? 1 : 0, GRP ? 1 : 0, N, logM, logC, status);
 }
 
-// the far-root series compiled in only where its constants are given
+// the far-root series compiled in only where its constants are given, and its
+// second level where the groups were formed (`grouped`)
 template <int RANK, int RPT, bool PACKED = false>
 static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const float2* Q,
                                  const float2* B, const float2* Ct, const float* dt,
                                  float2* Khat, const float2* mom, int H, int N, int M, int logC, St status,
-                                 cudaStream_t s, bool pdl) {
+                                 cudaStream_t s, bool pdl, bool grouped = false) {
+  if constexpr (RANK == 1 && PACKED) {
+    if (mom != nullptr && grouped)
+      return cauchy_launch_far<RANK, RPT, PACKED, true, true>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC,
+                                                              status, s, pdl);
+  }
   if (mom != nullptr)
     return cauchy_launch_far<RANK, RPT, PACKED, true>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s,
                                                       pdl);
@@ -789,14 +1081,15 @@ static cudaError_t cauchy_launch(const float2* Lambda, const float2* P, const fl
                                                      pdl);
 }
 
-template <int RANK>
+template <int RANK, bool GROUPS = false>
 static cudaError_t moments_launch(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
                                   const float2* Ct, float2* mom, int H, int N, St status, cudaStream_t s,
                                   bool pdl) {
+  static_assert(!GROUPS || RANK == 1, "groups at rank 1");
   TimedLaunch tl("moments", s);
+  auto kern = GROUPS ? cauchy_moments_grouped_kernel : cauchy_moments_kernel<RANK>;
   static int per_sm = -1;
-  if (pdl && per_sm < 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cauchy_moments_kernel<RANK>, 256, 0) != cudaSuccess)
+  if (pdl && per_sm < 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess)
     per_sm = 0;
   pdl = pdl && (long long)H <= (long long)per_sm * num_sms();
   cudaLaunchConfig_t cfg = {};
@@ -808,7 +1101,7 @@ static cudaError_t moments_launch(const float2* Lambda, const float2* P, const f
   cfg.stream = s;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, cauchy_moments_kernel<RANK>, Lambda, P, Q, B, Ct, N, mom, status);
+  return cudaLaunchKernelEx(&cfg, kern, Lambda, P, Q, B, Ct, N, mom, status);
 }
 
 cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q, const float2* B,
@@ -820,10 +1113,19 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
   // with few poles the series is not shorter than the sum, so the extra launch
   // would not pay (measured slower on N=64 M=1024 and M=4096).
   if (M < 8192 || N < 48) mom = nullptr;
+  // roots per thread: rank 1 takes 2 on every grid (S4_CAUCHY_RPT1_BIG); rank 2
+  // takes 4 (512 per CTA) once the grid holds at least two waves of such CTAs
+  // and 2 below that, to keep enough warps resident
+  const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
+  // the series' second level (pole groups) for the packed rank-1 kernel, N <= kFarPermMax
+  const bool grouped = S4_CAUCHY_GROUPS && S4_CAUCHY_PACKED && r == 1 && !small && N <= kFarPermMax;
   if (mom != nullptr) {
     cudaError_t e;
     switch (r) {
-      case 1: e = moments_launch<1>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
+      case 1:
+        e = grouped ? moments_launch<1, true>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl)
+                    : moments_launch<1>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl);
+        break;
       case 2: e = moments_launch<2>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
       case 3: e = moments_launch<3>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
       case 4: e = moments_launch<4>(Lambda, P, Q, B, Ct, mom, H, N, status, s, pdl); break;
@@ -832,16 +1134,12 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
     if (e != cudaSuccess) return e;
     pdl = true;
   }
-  // roots per thread: rank 1 takes 2 on every grid (S4_CAUCHY_RPT1_BIG); rank 2
-  // takes 4 (512 per CTA) once the grid holds at least two waves of such CTAs
-  // and 2 below that, to keep enough warps resident
-  const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
   switch (r) {
     case 1:
 #if S4_CAUCHY_PACKED
       return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl)
                    : cauchy_launch<1, S4_CAUCHY_PRPT1_BIG, true>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s,
-                                                               pdl);
+                                                               pdl, grouped);
 #else
       return small ? cauchy_launch<1, S4_CAUCHY_RPT1>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl)
                    : cauchy_launch<1, S4_CAUCHY_RPT1_BIG>(Lambda, P, Q, B, Ct, dt, Khat, mom, H, N, M, logC, status, s, pdl);

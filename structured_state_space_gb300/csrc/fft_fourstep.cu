@@ -253,8 +253,10 @@ __global__ void __launch_bounds__(kFsThreads) ks_cross_half_kernel(const float2*
   constexpr int C = 1 << (s4impl::fs_log_radix(LOGM + 1) - 1);
   constexpr int M = 1 << LOGM, mi = M / C, n = 2 * M;
   const long long gid = (long long)blockIdx.x * kFsThreads + threadIdx.x;
-  const int h = (int)(gid / mi), t2 = (int)(gid % mi);
-  if (h >= H) return;
+  if (gid / mi >= H) return;
+  // channels in reverse order: the first read are the inverse transforms' last
+  // writes (still in L2), the last written are the column spectra's first reads
+  const int h = H - 1 - (int)(gid / mi), t2 = (int)(gid % mi);
   const bool zero = st_bad(status);
   float2 g[C];
   const float2* gp = G + (size_t)h * M + t2;
@@ -429,8 +431,10 @@ __global__ void __launch_bounds__(FsColCfg<LOGM>::THREADS, 512 / FsColCfg<LOGM>:
   const int cols = pb * H * R;
   const float sc = 1.f / n;
   for (int c0 = blockIdx.x * C::ROWS; c0 < cols; c0 += gridDim.x * C::ROWS) {
-    const int col = c0 + slot;
-    const bool act = col < cols;
+    // columns in reverse order: the first ones read are the across-column step's
+    // last writes, still in L2, and the last ones written are the inverse step's first reads
+    const bool act = c0 + slot < cols;
+    const int col = act ? cols - 1 - (c0 + slot) : 0;
     const int p = act ? col / R : 0, k1 = col % R;
     const int h = p / pb;
     float2* xc = X + (size_t)p * n + (size_t)k1 * m;        // this column: X in, a out

@@ -34,7 +34,7 @@ int ilog2_ceil(int v) {
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Workspace: [status word | far-field constants of the root values (H
-// kFarStride) | root values (H M) | kernel spectra (H 2M) | long-row convolution
+// kFarChannel) | root values (H M) | kernel spectra (H 2M) | long-row convolution
 // scratch (two rows of 2M points per pair of batch rows, only when 2M >= 2^14)].
 // `gen_total` is what kernel generation alone needs.
 struct Layout {
@@ -45,7 +45,7 @@ Layout layout_for(int H, int L, int batch) {
   const size_t M = (size_t)1 << ilog2_ceil(L);
   Layout l;
   l.mom = 256;
-  l.khat = l.mom + round256(sizeof(float2) * (size_t)s4impl::kFarStride * (size_t)H);
+  l.khat = l.mom + round256(sizeof(float2) * (size_t)s4impl::kFarChannel * (size_t)H);
   l.k2 = l.khat + round256(sizeof(float2) * M * (size_t)H);
   l.fs = l.k2 + round256(sizeof(float2) * 2 * M * (size_t)H);
   l.gen_total = l.fs;

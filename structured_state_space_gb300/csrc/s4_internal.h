@@ -70,6 +70,15 @@ __host__ __device__ constexpr int khat_cluster_log(int logM) {
 // of each; kFarStride complex values per channel (room for rank 4).
 constexpr int kFarTerms = 42;
 constexpr int kFarStride = 2 + 25 * kFarTerms;
+// Second level (rank 1, N <= kFarPermMax): the poles ranked by imaginary part and
+// split into kFarGroups groups of consecutive ranks, each with its own centre,
+// radius and kFarTerms moments of the 4 weight vectors (kFarGStride complex values),
+// then the permutation (pole index by rank, 32-bit).  Per channel: kFarChannel
+// complex values in all.
+constexpr int kFarGroups = 4;
+constexpr int kFarGStride = 2 + 4 * kFarTerms;
+constexpr int kFarPermMax = 512;
+constexpr int kFarChannel = kFarStride + kFarGroups * kFarGStride + kFarPermMax / 2;
 
 // Root values Khat[h][p] for every channel, in the blocked root order
 // (position p -> root (p mod M/C) C + p div M/C, C = 2^logC), after the far-field

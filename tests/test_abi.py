@@ -35,10 +35,10 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_workspace_bytes(lib):
-    # [256 status | H x 1052 far-field constants | H M root values | H 2M spectra
+    # [256 status | H x 1988 far-field constants | H M root values | H 2M spectra
     # | long rows only: 2 x 2M per pair of batch rows], each 256-aligned
     r256 = lambda b: (b + 255) // 256 * 256
-    far = lambda H: r256(8 * 1052 * H)
+    far = lambda H: r256(8 * 1988 * H)
     H, L = 256, 1024
     M = 1024
     assert s4.s4_workspace_bytes(H, 64, 1, L, 16) == 256 + far(H) + 8 * H * M + 16 * H * M
