@@ -65,9 +65,12 @@ def cauchy_work(p, w, sms):
     near the channel's poles (|s - c| < 1.5 R) sum directly over the N poles
     (cauchy_flop per pole and root, for every root of the warp); the other roots
     evaluate the series, (r+1)^2 (P - 1) complex multiply-adds of 8 flop plus ~24
-    flop of set-up each, P the terms their warp takes.  The split is replayed here
-    in float64 from the parameters (the kernel decides in fp32; the two can
-    differ only at a warp on the boundary).  Returns (flop, fraction of roots
+    flop of set-up each, P the terms their warp takes.  With the series' second
+    level (rank 1, packed kernel, N <= 512) a near warp instead sums directly over
+    the poles of each of the 4 groups (equal widths in imaginary part) it is near
+    and takes the group series of the others.  The split is replayed here in
+    float64 from the parameters (the kernel decides in fp32; the two can differ
+    only at a warp on the boundary).  Returns (flop, fraction of root-pole terms
     summed directly)."""
     import numpy as np
     H, N, r, M = w.H, w.N, w.r, w.M
@@ -76,10 +79,15 @@ def cauchy_work(p, w, sms):
         return H * M * N * cauchy_flop(r), 1.0
     big = H * M >= 512 * 5 * 2 * sms
     cta = 32 * (4 if (big and r <= 2) else (2 if r <= 2 else 1))  # roots per warp
+    grouped = r == 1 and big and N <= 512
+    G = 4
     k = np.arange(M)
     t = np.tan(np.pi * k / M)
     direct_roots = 0
     far_terms = 0
+    grp_flop = 0.0  # near warps of grouped channels: direct over near groups, series for the others
+    grp_terms = 0   # (root, pole) terms those warps sum directly
+    far_roots = 0
     for h in range(H):
         lam = p["Lambda"][h].astype(np.complex128)
         c = 0.5 * (lam.real.min() + lam.real.max()) + 0.5j * (lam.imag.min() + lam.imag.max())
@@ -93,7 +101,34 @@ def cauchy_work(p, w, sms):
         pad = np.ones(nb * cta, bool)
         pad[:M] = far
         blk_far = pad.reshape(nb, cta).all(axis=1)
-        direct_roots += int((~blk_far).sum()) * cta
+        if grouped:
+            lo, hi = lam.imag.min(), lam.imag.max()
+            gid = np.minimum(np.where(hi > lo, (lam.imag - lo) * G / max(hi - lo, 1e-300), 0).astype(int), G - 1)
+            gsets = [lam[gid == g] for g in range(G)]
+            gpar = []
+            for gl in gsets:
+                if len(gl) == 0:
+                    gpar.append((0j, 1.0, 0))
+                    continue
+                cg = 0.5 * (gl.real.min() + gl.real.max()) + 0.5j * (gl.imag.min() + gl.imag.max())
+                gpar.append((cg, np.abs(gl - cg).max() or 1.0, len(gl)))
+            padu = np.full(nb * cta, 1e300 + 0j)
+            padu[:M] = 1j * a * t
+            for wi in np.where(~blk_far)[0]:
+                sw = padu[wi * cta:(wi + 1) * cta]
+                sw = sw[np.abs(sw) < 1e299]
+                for cg, Rg, ng in gpar:
+                    ug = sw - cg
+                    if np.all(np.abs(ug) >= 1.5 * Rg):
+                        axg = np.abs(Rg / ug).max()
+                        P = int(np.clip(23 / -np.log2(max(axg, 1e-300)) + 2, 1, FAR_TERMS))
+                        grp_flop += cta * (nw * 8 * (P - 1) + 24)
+                    else:
+                        grp_flop += cta * ng * cauchy_flop(r)
+                        grp_terms += cta * ng
+            # the warps' roots are counted by grp_flop instead of the full direct sum
+        else:
+            direct_roots += int((~blk_far).sum()) * cta
         # terms of the series per root, as the kernel takes them (the warp's largest)
         with np.errstate(divide="ignore", invalid="ignore"):
             ax = np.abs(R / u)
@@ -103,10 +138,11 @@ def cauchy_work(p, w, sms):
         padn[:M] = need
         warp = padn.reshape(nb, cta).max(axis=1, keepdims=True).repeat(cta, axis=1)
         far_terms += int(warp[blk_far].sum())
-    direct_roots = min(direct_roots, H * M)
-    far_roots = H * M - direct_roots
-    flop = direct_roots * N * cauchy_flop(r) + nw * 8 * max(far_terms - far_roots, 0) + 24 * far_roots
-    return flop, direct_roots / (H * M)
+        far_roots += int(blk_far.sum()) * cta
+    # far_terms counts, per far root, the terms P its warp takes: P - 1 Horner steps each
+    flop = (direct_roots * N * cauchy_flop(r) + grp_flop + nw * 8 * max(far_terms - far_roots, 0)
+            + 24 * far_roots)
+    return flop, (direct_roots * N + grp_terms) / (H * M * N)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -550,7 +586,7 @@ def run_ours(args):
     cflop, direct_frac = cauchy_work(p, w, sms)
     work = {
         "cauchy": ("alu", cflop,
-                   f"{cauchy_flop(r)} flop per (channel, root, pole) on the {100 * direct_frac:.1f} % of roots summed "
+                   f"{cauchy_flop(r)} flop per (channel, root, pole) on the {100 * direct_frac:.2f} % of root-pole terms summed "
                    f"directly, 8 (r+1)^2 (P - 1) + 24 flop per far root (series of P <= {FAR_TERMS} terms)"),
         "conv": ("hbm", Bsz * H * L * (4 + 8) + H * 2 * M * 8,
                  "u 4 B + y 8 B per channel-sample, kernel spectrum 16 B per channel-root once"),
