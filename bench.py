@@ -225,10 +225,11 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-_FFT_FILES = ["fft_rows.cu", "s4_fft.cuh", "s4_kspec.cuh", "s4_dev.cuh", "s4_plan.cuh", "../gen_twiddles.py"]
+_FFT_FILES = ["fft_rows.cu", "fft_fourstep.cu", "s4_fft.cuh", "s4_kspec.cuh", "s4_dev.cuh", "s4_plan.cuh",
+              "../gen_twiddles.py"]
 KERNEL_FILES = {
     "conv": _FFT_FILES,
-    "cauchy": ["cauchy.cu", "s4_dev.cuh", "../gen_twiddles.py"],
+    "cauchy": ["cauchy.cu", "s4_dev.cuh", "s4_internal.h", "../gen_twiddles.py"],
     "spectrum": _FFT_FILES,
     "kspec": _FFT_FILES,
     "ifft": _FFT_FILES,
@@ -236,8 +237,9 @@ KERNEL_FILES = {
 
 
 def profiled_traffic(kernel, workload):
-    """DRAM bytes per launch on `workload` from the committed ncu summary, if
-    they were taken on the current source of that kernel; else None."""
+    """DRAM bytes per step of a part (the sum over its launches) on `workload`
+    from the committed ncu summary, if they were taken on the current source of
+    that part's kernels; else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)

@@ -487,3 +487,19 @@ def test_far_root_series_against_the_definition(r, dt):
     K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L).cpu().numpy()
     K_ref = O.s4_kernel_channels(p, w.L, [0, 3])
     assert rel_l2(K[[0, 3]], K_ref) <= 1e-5, rel_l2(K[[0, 3]], K_ref)
+
+
+@pytest.mark.parametrize("dt", [1e-3, 1e-4])
+def test_pole_group_series_against_the_definition(dt):
+    # Rank 1 on a grid large enough for the packed kernel (H M >= 2^19.6), N = 256
+    # poles: the far-field series' second level is on.  With a = 2/Delta = 2e3
+    # about 15 % of the roots lie within 1.5 R of the poles' centre; their warps sum
+    # directly only over the pole groups they are near and take the group series
+    # for the others.  K must match the definition to 1e-5 here too.
+    w = W.custom(256, 1, 16, 65536, 1, seed=91, dt_lo=dt, dt_hi=dt)
+    p = W.make_params(w)
+    d = dev(p, keys=("Lambda", "P", "Q", "B", "Ctilde", "dt"))
+    K = s4.s4_kernel_gen(d["Lambda"], d["P"], d["Q"], d["B"], d["Ctilde"], d["dt"], w.L).cpu().numpy()
+    K_ref = O.s4_kernel_channels(p, w.L, [0, 11])
+    assert rel_l2(K[[0, 11]], K_ref) <= 1e-5, rel_l2(K[[0, 11]], K_ref)
+    assert np.all(np.isfinite(K))
