@@ -66,7 +66,7 @@ def cauchy_work(p, w, sms):
     (cauchy_flop per pole and root, for every root of the warp); the other roots
     evaluate the series, (r+1)^2 (P - 1) complex multiply-adds of 8 flop plus ~24
     flop of set-up each, P the terms their warp takes.  With the series' second
-    level (rank 1, packed kernel, N <= 512) a near warp instead sums directly over
+    level (rank 1, large grids, 128 <= N <= 512) a near warp instead sums directly over
     the poles of each of the 4 groups (equal widths in imaginary part) it is near
     and takes the group series of the others.  The split is replayed here in
     float64 from the parameters (the kernel decides in fp32; the two can differ
@@ -79,7 +79,7 @@ def cauchy_work(p, w, sms):
         return H * M * N * cauchy_flop(r), 1.0
     big = H * M >= 512 * 5 * 2 * sms
     cta = 32 * (4 if (big and r <= 2) else (2 if r <= 2 else 1))  # roots per warp
-    grouped = r == 1 and big and N <= 512
+    grouped = r == 1 and big and 128 <= N <= 512
     G = 4
     k = np.arange(M)
     t = np.tan(np.pi * k / M)

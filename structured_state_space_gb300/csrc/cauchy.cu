@@ -255,20 +255,23 @@ __global__ void __launch_bounds__(256) cauchy_moments_kernel(
   }
 }
 
-// Rank 1 with the series' second level (N <= kFarPermMax poles): one CTA per
+// The series' second level (N <= kFarPermMax poles; launched at rank 1): one CTA per
 // channel.  The poles fall into kFarGroups groups of equal width in imaginary part
 // (between the smallest and largest), numbered in that order and, within a group,
 // by pole index; the rank is a pole's position in that order.  The CTA writes the
 // whole set's constants, each group's centre, radius (its start rank in the
 // imaginary slot) and moments, and the poles by rank.  The five sets' moments
-// accumulate over the poles in rank order, one thread per (set, m) with the 4
-// weights in registers.
+// accumulate over the poles in rank order, one thread per (set, m) with the
+// (r+1)^2 weights in registers.
+template <int RANK>
 __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, int N, float2* __restrict__ mom, St status) {
-  constexpr int NW = 4, P = kFarTerms, T = 256, G = kFarGroups, NS = 1 + G, JC = 32, PPT = kFarPermMax / T;
-  __shared__ float2 sl[kFarPermMax];       // poles by rank
-  __shared__ float4 sw[kFarPermMax][2];    // their 4 weights by rank
+  constexpr int NW = (RANK + 1) * (RANK + 1), P = kFarTerms, T = 256, G = kFarGroups, NS = 1 + G, JC = 32;
+  constexpr int PPT = kFarPermMax / T;
+  static_assert(2 + NW * P <= kFarGStride, "group stride");
+  __shared__ float2 sl[kFarPermMax];                    // poles by rank
+  __shared__ __align__(16) float2 sw[kFarPermMax][NW];  // their weights by rank
   __shared__ unsigned char sgid[kFarPermMax];
   __shared__ short sloc[kFarPermMax];      // place within the group (by pole index)
   __shared__ int sperm[kFarPermMax];
@@ -291,10 +294,15 @@ __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
     if (j >= N) continue;
     const long long jg = (long long)h * N + j;
     lr[q] = ld_chk(Lambda, jg, nj);
-    float2 pp[1] = {ld_chk(Pm, jg, nj)}, qq[1] = {ld_chk(Qm, jg, nj)};
+    float2 pp[RANK], qq[RANK];
+#pragma unroll
+    for (int i = 0; i < RANK; ++i) {
+      pp[i] = ld_chk(Pm, jg * RANK + i, nj * RANK);
+      qq[i] = ld_chk(Qm, jg * RANK + i, nj * RANK);
+    }
     const float2 bj = ld_chk(Bv, jg, nj), cj = ld_chk(Ct, jg, nj);
 #pragma unroll
-    for (int w = 0; w < NW; ++w) wr[q][w] = far_weight(w, 1, cj, bj, pp, qq);
+    for (int w = 0; w < NW; ++w) wr[q][w] = far_weight(w, RANK, cj, bj, pp, qq);
     b0 = fminf(b0, lr[q].x); b1 = fmaxf(b1, lr[q].x); b2 = fminf(b2, lr[q].y); b3 = fmaxf(b3, lr[q].y);
   }
 #pragma unroll
@@ -356,8 +364,8 @@ __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
     if (!S4_IN(rk, kFarPermMax)) continue;
     sperm[rk] = j;
     sl[rk] = lr[q];
-    sw[rk][0] = make_float4(wr[q][0].x, wr[q][0].y, wr[q][1].x, wr[q][1].y);
-    sw[rk][1] = make_float4(wr[q][2].x, wr[q][2].y, wr[q][3].x, wr[q][3].y);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) sw[rk][w] = wr[q][w];
   }
   __syncthreads();
   // warp 0: the whole set's centre and radius; warps 1..G: group wp - 1
@@ -423,9 +431,19 @@ __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
     const int jlo = max(lo - r0, 0), jhi = min(hi - r0, jn);
     for (int jj = jlo; jj < jhi; ++jj) {
       const float2 y = set == 0 ? pw0[jj][m] : pwg[jj][m];
-      const float4 x01 = sw[r0 + jj][0], x23 = sw[r0 + jj][1];
-      const float2 x[NW] = {make_float2(x01.x, x01.y), make_float2(x01.z, x01.w), make_float2(x23.x, x23.y),
-                            make_float2(x23.z, x23.w)};
+      float2 x[NW];
+      if constexpr (NW % 2 == 0) {  // 16-byte loads of weight pairs
+        const float4* x4 = reinterpret_cast<const float4*>(sw[r0 + jj]);
+#pragma unroll
+        for (int w = 0; w < NW / 2; ++w) {
+          const float4 t = x4[w];
+          x[2 * w] = make_float2(t.x, t.y);
+          x[2 * w + 1] = make_float2(t.z, t.w);
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) x[w] = sw[r0 + jj][w];
+      }
 #pragma unroll
       for (int w = 0; w < NW; ++w)
         acc[w] = make_float2(fmaf(x[w].x, y.x, fmaf(-x[w].y, y.y, acc[w].x)),
@@ -574,7 +592,7 @@ struct CauchyLayout {
 #ifndef S4_CAUCHY_MINB
 #define S4_CAUCHY_MINB 4
 #endif
-// (rank >= 2 with the far-root series compiled in: resident CTAs per SM)
+// (rank >= 2: resident CTAs per SM; 4 spills at 128 registers)
 #ifndef S4_CAUCHY_MINB_FAR2
 #define S4_CAUCHY_MINB_FAR2 3
 #endif
@@ -583,7 +601,7 @@ struct CauchyLayout {
 // GRP: the second level of the series is compiled in (used when `grouped`: the
 // moments kernel formed the groups and the permutation for this call).
 template <int RANK, int RPT, int T, bool PACKED = false, bool FAR = false, bool GRP = false>
-__global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MINB_FAR2 : S4_CAUCHY_MINB) : 0)
+__global__ void __launch_bounds__(T, RPT >= 4 ? (RANK >= 2 ? S4_CAUCHY_MINB_FAR2 : S4_CAUCHY_MINB) : 0)
     cauchy_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, const float* __restrict__ dt,
@@ -598,8 +616,9 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   __shared__ float2 mus[2 + NW * FP];  // c, (R, 0), mu[w][m] of this channel
   __shared__ float2 red[T / 32 + 1];
   // the groups' constants [c_g, (R_g, 0), mu_g[w][m]], loaded at the first near tile
-  __shared__ float2 musg[GRP ? kFarGroups * kFarGStride : 1];
-  static_assert(!GRP || (FAR && RANK == 1), "groups: rank 1 with the series");
+  constexpr int GSL = 2 + NW * FP;  // a group's constants in shared memory
+  __shared__ float2 musg[GRP ? kFarGroups * GSL : 1];
+  static_assert(!GRP || (FAR && 2 + NW * FP <= kFarGStride), "groups: the series, the group stride");
 
   if constexpr (!FAR) far_on = 0;
   if constexpr (!GRP) grouped = 0;
@@ -701,16 +720,17 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
   if constexpr (GRP) {
     if (grouped && !cta_far) {
       if (!groups_loaded) {  // (uniform)
-        for (int i = threadIdx.x; i < kFarGroups * kFarGStride; i += T)
-          musg[i] = ld_chk(mom, (long long)h * kFarChannel + kFarStride + i, (long long)gridDim.x * kFarChannel);
+        for (int i = threadIdx.x; i < kFarGroups * GSL; i += T)
+          musg[i] = ld_chk(mom, (long long)h * kFarChannel + kFarStride + (i / GSL) * kFarGStride + i % GSL,
+                           (long long)gridDim.x * kFarChannel);
         groups_loaded = true;
         __syncthreads();
       }
       if (!warp_far) {
 #pragma unroll
         for (int g = 0; g < kFarGroups; ++g) {
-          const float2 cg = musg[g * kFarGStride];
-          const float Rg = musg[g * kFarGStride + 1].x;
+          const float2 cg = musg[g * GSL];
+          const float Rg = musg[g * GSL + 1].x;
           bool gfar = true;
 #pragma unroll
           for (int rr = 0; rr < RPT; ++rr) {
@@ -805,8 +825,8 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
       int jlo = 0, jhi = jn;
       if (GRP && grouped) {
         if (!((gnear >> g) & 1u)) continue;
-        jlo = max((int)musg[g * kFarGStride + 1].y - j0, 0);
-        jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * kFarGStride + 1].y : N) - j0, jn);
+        jlo = max((int)musg[g * GSL + 1].y - j0, 0);
+        jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * GSL + 1].y : N) - j0, jn);
       }
 #pragma unroll kCauchyUnroll
       for (int jj = jlo; jj < jhi; ++jj) {
@@ -845,8 +865,15 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
       }  // groups
       continue;
     }
+    for (int g = 0; g < (GRP && grouped ? kFarGroups : 1); ++g) {
+    int jlo = 0, jhi = jn;
+    if (GRP && grouped) {
+      if (!((gnear >> g) & 1u)) continue;
+      jlo = max((int)musg[g * GSL + 1].y - j0, 0);
+      jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * GSL + 1].y : N) - j0, jn);
+    }
 #pragma unroll kCauchyUnroll
-    for (int jj = 0; jj < jn; ++jj) {
+    for (int jj = jlo; jj < jhi; ++jj) {
       float pr[PS];
       const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
 #pragma unroll
@@ -872,6 +899,7 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
         }
       }
     }
+    }  // groups
   }
 
   if constexpr (PACKED) {
@@ -896,8 +924,8 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (FAR && RANK >= 2 ? S4_CAUCHY_MI
 #pragma unroll
       for (int g = 0; g < kFarGroups; ++g)
         if (!((gnear >> g) & 1u))
-          far_series<NW, RPT, PACKED, FP, true>(musg + g * kFarGStride + 2, musg[g * kFarGStride],
-                                                musg[g * kFarGStride + 1].x, shi, slo, live, acc);
+          far_series<NW, RPT, PACKED, FP, true>(musg + g * GSL + 2, musg[g * GSL], musg[g * GSL + 1].x, shi, slo,
+                                                live, acc);
     }
   }
   // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
@@ -1093,7 +1121,9 @@ static cudaError_t moments_launch(const float2* Lambda, const float2* P, const f
                                   bool pdl) {
   static_assert(!GROUPS || RANK == 1, "groups at rank 1");
   TimedLaunch tl("moments", s);
-  auto kern = GROUPS ? cauchy_moments_grouped_kernel : cauchy_moments_kernel<RANK>;
+  using Kern = void (*)(const float2*, const float2*, const float2*, const float2*, const float2*, int, float2*, St);
+  Kern kern = cauchy_moments_kernel<RANK>;
+  if constexpr (GROUPS) kern = cauchy_moments_grouped_kernel<RANK>;
   static int per_sm = -1;
   if (pdl && per_sm < 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess)
     per_sm = 0;
@@ -1123,8 +1153,13 @@ cudaError_t launch_cauchy(const float2* Lambda, const float2* P, const float2* Q
   // takes 4 (512 per CTA) once the grid holds at least two waves of such CTAs
   // and 2 below that, to keep enough warps resident
   const bool small = (long long)H * M < 512LL * 5 * 2 * num_sms();
-  // the series' second level (pole groups) for the packed rank-1 kernel, N <= kFarPermMax
-  const bool grouped = S4_CAUCHY_GROUPS && S4_CAUCHY_PACKED && r == 1 && !small && N <= kFarPermMax;
+  // the series' second level (pole groups) for the packed rank-1 kernel of large
+  // grids, 128 <= N <= kFarPermMax: groups of 32 poles or more, where a group's
+  // series (<= 41 steps of 4 complex multiply-adds) costs less than its direct sum.
+  // (At rank 2 with N = 64, groups of 16 poles, the root values measured slower:
+  // 160 -> 245 us on N=64 r=2 H=256 M=16384.  The kernels are templated on the
+  // rank; only rank 1 is launched, and the group stride holds its 4 weight vectors.)
+  const bool grouped = S4_CAUCHY_GROUPS && S4_CAUCHY_PACKED && r == 1 && !small && N >= 128 && N <= kFarPermMax;
   if (mom != nullptr) {
     cudaError_t e;
     switch (r) {

@@ -72,9 +72,9 @@ constexpr int kFarTerms = 42;
 constexpr int kFarStride = 2 + 25 * kFarTerms;
 // Second level (rank 1, N <= kFarPermMax): the poles ranked by imaginary part and
 // split into kFarGroups groups of consecutive ranks, each with its own centre,
-// radius and kFarTerms moments of the 4 weight vectors (kFarGStride complex values),
-// then the permutation (pole index by rank, 32-bit).  Per channel: kFarChannel
-// complex values in all.
+// radius and kFarTerms moments of the 4 weight vectors (kFarGStride complex
+// values), then the permutation (pole index by rank, 32-bit).  Per channel:
+// kFarChannel complex values in all.
 constexpr int kFarGroups = 4;
 constexpr int kFarGStride = 2 + 4 * kFarTerms;
 constexpr int kFarPermMax = 512;
