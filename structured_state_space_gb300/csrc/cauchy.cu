@@ -51,6 +51,13 @@
 #define S4_CAUCHY_SCALAR_DEN 0
 #endif
 
+// Poles per chunk of the grouped moments kernel's accumulation (its shared-memory
+// power tables hold 2 x chunk x kFarTerms complex values; 16 and 8 measured
+// slower: 57 -> 61 and 76 us on N=256 H=1024).
+#ifndef S4_CAUCHY_MOM_CHUNK
+#define S4_CAUCHY_MOM_CHUNK 32
+#endif
+
 namespace s4dev {
 
 constexpr int kCauchyUnroll = S4_CAUCHY_UNROLL;  // poles per unrolled step of the pole loop
@@ -267,8 +274,8 @@ template <int RANK>
 __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
     const float2* __restrict__ Lambda, const float2* __restrict__ Pm, const float2* __restrict__ Qm,
     const float2* __restrict__ Bv, const float2* __restrict__ Ct, int N, float2* __restrict__ mom, St status) {
-  constexpr int NW = (RANK + 1) * (RANK + 1), P = kFarTerms, T = 256, G = kFarGroups, NS = 1 + G, JC = 32;
-  constexpr int PPT = kFarPermMax / T;
+  constexpr int NW = (RANK + 1) * (RANK + 1), P = kFarTerms, T = 256, G = kFarGroups, NS = 1 + G;
+  constexpr int JC = S4_CAUCHY_MOM_CHUNK, PPT = kFarPermMax / T;
   static_assert(2 + NW * P <= kFarGStride, "group stride");
   __shared__ float2 sl[kFarPermMax];                    // poles by rank
   __shared__ __align__(16) float2 sw[kFarPermMax][NW];  // their weights by rank
@@ -1043,7 +1050,7 @@ S4_OOB_COUNTER(oob_cauchy)
 #define S4_CAUCHY_PRPT1_BIG 4
 #endif
 #ifndef S4_CAUCHY_FAR_TILES
-#define S4_CAUCHY_FAR_TILES 4
+#define S4_CAUCHY_FAR_TILES 8
 #endif
 // The far series' second level (pole groups) for near warps (1) or none (0).
 #ifndef S4_CAUCHY_GROUPS
@@ -1066,10 +1073,11 @@ static cudaError_t cauchy_launch_far(const float2* Lambda, const float2* P, cons
   // With the far-root series, a CTA loops over up to S4_CAUCHY_FAR_TILES tiles of
   // its channel (most of them cheap series tiles, which would otherwise each pay a
   // CTA's set-up), as long as the grid keeps 16 CTAs per resident slot for the
-  // balance of the costly direct tiles (measured: 1511 -> 1394 us on N=256 H=1024
-  // M=65536 at 4 tiles, where 8 was no faster; 184 -> 198 us on N=64 H=256
-  // M=16384 at 4, whose grid is 16 times smaller).  The direct sum alone keeps one
-  // tile per CTA.
+  // balance of the costly direct tiles (measured on N=256 H=1024 M=65536: 1511 ->
+  // 1394 us at 4 tiles when the series was introduced; with the later far path 8
+  // tiles 969 -> 957 us and 2 tiles 1001 us; on N=64 H=256 M=16384, whose grid is
+  // 16 times smaller, 4 tiles were slower: 184 -> 198 us).  The direct sum alone
+  // keeps one tile per CTA.
   long long per_cta = 1;
   if (FAR && per_sm > 0) {
     per_cta = (long long)H * tiles / (16LL * per_sm * num_sms());
