@@ -677,157 +677,201 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (RANK >= 2 ? S4_CAUCHY_MINB_FAR2
   const int* permh = reinterpret_cast<const int*>(mom + (size_t)h * kFarChannel + kFarStride +
                                                   kFarGroups * kFarGStride);
   for (int v = blockIdx.y; v < tiles; v += gridDim.y) {
-  const int tile = tile_of(v);
-  int pos[RPT];
-  bool zm1[RPT];
-  float shi[RPT], slo[RPT], th[RPT];
-#pragma unroll
-  for (int rr = 0; rr < RPT; ++rr) {
-    const int kr = root_of(tile, rr);
-    const bool valid = kr < M;
-    const int k = valid ? kr : 0;
-    pos[rr] = valid ? (k & ((1 << logC) - 1)) * Mc + (k >> logC) : M;
-    float2 tt;
-    if constexpr (FAR) tt = tnext[rr];
-    else tt = tan_of(tile, rr);
-    zm1[rr] = valid && M >= 2 && 2 * k == M;
-    const float p = a_hi * tt.x;
-    const float perr = fmaf(a_hi, tt.x, -p);
-    const float lo = perr + fmaf(a_hi, tt.y, a_lo * tt.x);
-    shi[rr] = zm1[rr] ? 0.f : p;
-    slo[rr] = zm1[rr] ? 0.f : lo;
-    th[rr] = tt.x;
-  }
-  if (FAR && v + (int)gridDim.y < tiles) {
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) tnext[FAR ? rr : 0] = tan_of(tile_of(v + gridDim.y), rr);
-  }
-  // far roots: |s - c|^2 >= 2.25 R^2 with u = s - c (s = i (shi + slo)); the z = -1
-  // root and positions past M need no sums.  A warp takes the series only when all
-  // its roots are far; otherwise each of its roots takes the direct sum.  The CTA
-  // stages the poles unless all its warps are far.
-  const float2 fc = far_on ? mus[0] : make_float2(0.f, 0.f);
-  const float fR = far_on ? mus[1].x : 0.f;
-  float2 fu[RPT];
-  bool warp_far = false, cta_far = false;
-  if constexpr (FAR) {
-    bool mine = far_on != 0;
+    const int tile = tile_of(v);
+    int pos[RPT];
+    bool zm1[RPT];
+    float shi[RPT], slo[RPT], th[RPT];
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) {
-      fu[rr] = make_float2(-fc.x, (shi[rr] - fc.y) + slo[rr]);
-      const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
-      mine = mine && (pos[rr] >= M || zm1[rr] || (n2u >= kFarRadius2 * fR * fR && n2u > 0.f));
+      const int kr = root_of(tile, rr);
+      const bool valid = kr < M;
+      const int k = valid ? kr : 0;
+      pos[rr] = valid ? (k & ((1 << logC) - 1)) * Mc + (k >> logC) : M;
+      float2 tt;
+      if constexpr (FAR) tt = tnext[rr];
+      else tt = tan_of(tile, rr);
+      zm1[rr] = valid && M >= 2 && 2 * k == M;
+      const float p = a_hi * tt.x;
+      const float perr = fmaf(a_hi, tt.x, -p);
+      const float lo = perr + fmaf(a_hi, tt.y, a_lo * tt.x);
+      shi[rr] = zm1[rr] ? 0.f : p;
+      slo[rr] = zm1[rr] ? 0.f : lo;
+      th[rr] = tt.x;
     }
-    warp_far = __all_sync(0xffffffffu, mine);
-    cta_far = __syncthreads_and(warp_far) != 0;
-  }
-  // a near warp of a grouped channel: bit g of gnear when some root of the warp is
-  // near group g (|s - c_g| < 1.5 R_g); it sums directly over those groups' poles only
-  unsigned gnear = 0u;
-  if constexpr (GRP) {
-    if (grouped && !cta_far) {
-      if (!groups_loaded) {  // (uniform)
-        for (int i = threadIdx.x; i < kFarGroups * GSL; i += T)
-          musg[i] = ld_chk(mom, (long long)h * kFarChannel + kFarStride + (i / GSL) * kFarGStride + i % GSL,
-                           (long long)gridDim.x * kFarChannel);
-        groups_loaded = true;
-        __syncthreads();
+    if (FAR && v + (int)gridDim.y < tiles) {
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) tnext[FAR ? rr : 0] = tan_of(tile_of(v + gridDim.y), rr);
+    }
+    // far roots: |s - c|^2 >= 2.25 R^2 with u = s - c (s = i (shi + slo)); the z = -1
+    // root and positions past M need no sums.  A warp takes the series only when all
+    // its roots are far; otherwise each of its roots takes the direct sum.  The CTA
+    // stages the poles unless all its warps are far.
+    const float2 fc = far_on ? mus[0] : make_float2(0.f, 0.f);
+    const float fR = far_on ? mus[1].x : 0.f;
+    float2 fu[RPT];
+    bool warp_far = false, cta_far = false;
+    if constexpr (FAR) {
+      bool mine = far_on != 0;
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) {
+        fu[rr] = make_float2(-fc.x, (shi[rr] - fc.y) + slo[rr]);
+        const float n2u = fmaf(fu[rr].x, fu[rr].x, fu[rr].y * fu[rr].y);
+        mine = mine && (pos[rr] >= M || zm1[rr] || (n2u >= kFarRadius2 * fR * fR && n2u > 0.f));
       }
-      if (!warp_far) {
+      warp_far = __all_sync(0xffffffffu, mine);
+      cta_far = __syncthreads_and(warp_far) != 0;
+    }
+    // a near warp of a grouped channel: bit g of gnear when some root of the warp is
+    // near group g (|s - c_g| < 1.5 R_g); it sums directly over those groups' poles only
+    unsigned gnear = 0u;
+    if constexpr (GRP) {
+      if (grouped && !cta_far) {
+        if (!groups_loaded) {  // (uniform)
+          for (int i = threadIdx.x; i < kFarGroups * GSL; i += T)
+            musg[i] = ld_chk(mom, (long long)h * kFarChannel + kFarStride + (i / GSL) * kFarGStride + i % GSL,
+                             (long long)gridDim.x * kFarChannel);
+          groups_loaded = true;
+          __syncthreads();
+        }
+        if (!warp_far) {
 #pragma unroll
-        for (int g = 0; g < kFarGroups; ++g) {
-          const float2 cg = musg[g * GSL];
-          const float Rg = musg[g * GSL + 1].x;
-          bool gfar = true;
+          for (int g = 0; g < kFarGroups; ++g) {
+            const float2 cg = musg[g * GSL];
+            const float Rg = musg[g * GSL + 1].x;
+            bool gfar = true;
 #pragma unroll
-          for (int rr = 0; rr < RPT; ++rr) {
-            const float2 u = make_float2(-cg.x, (shi[rr] - cg.y) + slo[rr]);
-            const float n2 = fmaf(u.x, u.x, u.y * u.y);
-            gfar = gfar && (pos[rr] >= M || zm1[rr] || (n2 >= kFarRadius2 * Rg * Rg && n2 > 0.f));
+            for (int rr = 0; rr < RPT; ++rr) {
+              const float2 u = make_float2(-cg.x, (shi[rr] - cg.y) + slo[rr]);
+              const float n2 = fmaf(u.x, u.x, u.y * u.y);
+              gfar = gfar && (pos[rr] >= M || zm1[rr] || (n2 >= kFarRadius2 * Rg * Rg && n2 > 0.f));
+            }
+            if (!__all_sync(0xffffffffu, gfar)) gnear |= 1u << g;
           }
-          if (!__all_sync(0xffffffffu, gfar)) gnear |= 1u << g;
         }
       }
     }
-  }
 
-  float2 acc[RPT][NW];
+    float2 acc[RPT][NW];
 #pragma unroll
-  for (int rr = 0; rr < RPT; ++rr)
+    for (int rr = 0; rr < RPT; ++rr)
 #pragma unroll
-    for (int w = 0; w < NW; ++w) acc[rr][w] = make_float2(0.f, 0.f);
-  float2 cb = make_float2(0.f, 0.f);  // this thread's part of C~^* B (pole loop)
-  // (PACKED) the accumulators of root pair pr: ax = {acc[2pr][w].x, acc[2pr+1][w].x}, ay likewise
-  float2 ax[PACKED ? NPR : 1][NW], ay[PACKED ? NPR : 1][NW], sh2[PACKED ? NPR : 1], sl2[PACKED ? NPR : 1];
-  if constexpr (PACKED) {
-#pragma unroll
-    for (int pr = 0; pr < NPR; ++pr) {
-      sh2[pr] = make_float2(shi[2 * pr], shi[2 * pr + 1]);
-      sl2[pr] = make_float2(slo[2 * pr], slo[2 * pr + 1]);
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        ax[pr][w] = make_float2(0.f, 0.f);
-        ay[pr][w] = make_float2(0.f, 0.f);
-      }
-    }
-  }
-
-  for (int j0 = 0; j0 < (cta_far ? 0 : N); j0 += JT) {
-    const int jn = min(JT, N - j0);
-    __syncthreads();
-    for (int jj = threadIdx.x; jj < jn; jj += T) {
-      // (grouped: the poles in rank order, so that each group is one range)
-      const int jp = (GRP && grouped && S4_IN((long long)h * kFarChannel + kFarStride + kFarGroups * kFarGStride +
-                                                  (j0 + jj) / 2,
-                                              (long long)gridDim.x * kFarChannel))
-                         ? __ldg(permh + j0 + jj)
-                         : j0 + jj;
-      const size_t j = (size_t)h * N + jp;
-      const long long nj = (long long)gridDim.x * N;  // H N
-      if (!S4_IN(j, nj) || !S4_IN((long long)j * RANK + RANK - 1, nj * RANK) || !S4_IN(jj * PS + PS - 1, JT * PS))
-        continue;
-      const float2 lam = Lambda[j], b = Bv[j], c = Ct[j];
-      float* pp = par + jj * PS;
-      const float nre = -lam.x;
-      if constexpr (PACKED) {
-        reinterpret_cast<float4*>(pp)[0] = make_float4(-lam.y, -lam.y, lam.x * lam.x, lam.x * lam.x);
-      } else {
-        pp[0] = lam.y;
-        pp[1] = lam.x * lam.x;
-      }
-      auto put = [&](int widx, float2 w) {
-        if constexpr (PACKED) {
-          float4* p4 = reinterpret_cast<float4*>(pp) + 1 + 2 * widx;
-          p4[0] = make_float4(w.y, w.y, w.x * nre, w.x * nre);
-          p4[1] = make_float4(-w.x, -w.x, w.y * nre, w.y * nre);
-        } else {
-          pp[2 + 4 * widx] = w.x;
-          pp[3 + 4 * widx] = w.y;
-          pp[4 + 4 * widx] = w.x * nre;
-          pp[5 + 4 * widx] = w.y * nre;
-        }
-      };
-      const float2 w0 = conj_mul(c, b);
-      cb = cadd(cb, w0);
-      put(0, w0);
-#pragma unroll
-      for (int l = 0; l < RANK; ++l) put(1 + l, conj_mul(c, Pm[j * RANK + l]));
-#pragma unroll
-      for (int i = 0; i < RANK; ++i) {
-        const float2 qi = Qm[j * RANK + i];
-        put(1 + RANK + i, conj_mul(qi, b));
-#pragma unroll
-        for (int l = 0; l < RANK; ++l) put(1 + 2 * RANK + i * RANK + l, conj_mul(qi, Pm[j * RANK + l]));
-      }
-      if constexpr (!PACKED) {
-#pragma unroll
-        for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
-      }
-    }
-    __syncthreads();
-    if (warp_far) continue;  // (a far warp only helps stage the poles)
+      for (int w = 0; w < NW; ++w) acc[rr][w] = make_float2(0.f, 0.f);
+    float2 cb = make_float2(0.f, 0.f);  // this thread's part of C~^* B (pole loop)
+    // (PACKED) the accumulators of root pair pr: ax = {acc[2pr][w].x, acc[2pr+1][w].x}, ay likewise
+    float2 ax[PACKED ? NPR : 1][NW], ay[PACKED ? NPR : 1][NW], sh2[PACKED ? NPR : 1], sl2[PACKED ? NPR : 1];
     if constexpr (PACKED) {
-      // the staged poles this warp sums over: all, or the ranges of its near groups
+#pragma unroll
+      for (int pr = 0; pr < NPR; ++pr) {
+        sh2[pr] = make_float2(shi[2 * pr], shi[2 * pr + 1]);
+        sl2[pr] = make_float2(slo[2 * pr], slo[2 * pr + 1]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          ax[pr][w] = make_float2(0.f, 0.f);
+          ay[pr][w] = make_float2(0.f, 0.f);
+        }
+      }
+    }
+
+    for (int j0 = 0; j0 < (cta_far ? 0 : N); j0 += JT) {
+      const int jn = min(JT, N - j0);
+      __syncthreads();
+      for (int jj = threadIdx.x; jj < jn; jj += T) {
+        // (grouped: the poles in rank order, so that each group is one range)
+        const int jp = (GRP && grouped && S4_IN((long long)h * kFarChannel + kFarStride + kFarGroups * kFarGStride +
+                                                    (j0 + jj) / 2,
+                                                (long long)gridDim.x * kFarChannel))
+                           ? __ldg(permh + j0 + jj)
+                           : j0 + jj;
+        const size_t j = (size_t)h * N + jp;
+        const long long nj = (long long)gridDim.x * N;  // H N
+        if (!S4_IN(j, nj) || !S4_IN((long long)j * RANK + RANK - 1, nj * RANK) || !S4_IN(jj * PS + PS - 1, JT * PS))
+          continue;
+        const float2 lam = Lambda[j], b = Bv[j], c = Ct[j];
+        float* pp = par + jj * PS;
+        const float nre = -lam.x;
+        if constexpr (PACKED) {
+          reinterpret_cast<float4*>(pp)[0] = make_float4(-lam.y, -lam.y, lam.x * lam.x, lam.x * lam.x);
+        } else {
+          pp[0] = lam.y;
+          pp[1] = lam.x * lam.x;
+        }
+        auto put = [&](int widx, float2 w) {
+          if constexpr (PACKED) {
+            float4* p4 = reinterpret_cast<float4*>(pp) + 1 + 2 * widx;
+            p4[0] = make_float4(w.y, w.y, w.x * nre, w.x * nre);
+            p4[1] = make_float4(-w.x, -w.x, w.y * nre, w.y * nre);
+          } else {
+            pp[2 + 4 * widx] = w.x;
+            pp[3 + 4 * widx] = w.y;
+            pp[4 + 4 * widx] = w.x * nre;
+            pp[5 + 4 * widx] = w.y * nre;
+          }
+        };
+        const float2 w0 = conj_mul(c, b);
+        cb = cadd(cb, w0);
+        put(0, w0);
+#pragma unroll
+        for (int l = 0; l < RANK; ++l) put(1 + l, conj_mul(c, Pm[j * RANK + l]));
+#pragma unroll
+        for (int i = 0; i < RANK; ++i) {
+          const float2 qi = Qm[j * RANK + i];
+          put(1 + RANK + i, conj_mul(qi, b));
+#pragma unroll
+          for (int l = 0; l < RANK; ++l) put(1 + 2 * RANK + i * RANK + l, conj_mul(qi, Pm[j * RANK + l]));
+        }
+        if constexpr (!PACKED) {
+#pragma unroll
+          for (int f = 2 + 4 * NW; f < PS; ++f) pp[f] = 0.f;
+        }
+      }
+      __syncthreads();
+      if (warp_far) continue;  // (a far warp only helps stage the poles)
+      if constexpr (PACKED) {
+        // the staged poles this warp sums over: all, or the ranges of its near groups
+        for (int g = 0; g < (GRP && grouped ? kFarGroups : 1); ++g) {
+        int jlo = 0, jhi = jn;
+        if (GRP && grouped) {
+          if (!((gnear >> g) & 1u)) continue;
+          jlo = max((int)musg[g * GSL + 1].y - j0, 0);
+          jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * GSL + 1].y : N) - j0, jn);
+        }
+#pragma unroll kCauchyUnroll
+        for (int jj = jlo; jj < jhi; ++jj) {
+          const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
+          const float4 pl = p4[0];
+          const float2 nim = make_float2(pl.x, pl.y), re2 = make_float2(pl.z, pl.w);
+          float2 dim[NPR], rn[NPR];
+#pragma unroll
+          for (int pr = 0; pr < NPR; ++pr) {
+#if S4_CAUCHY_SCALAR_DEN
+            // the denominators in scalar instructions, which may issue to the FMA
+            // pipe's other half while the packed products keep the first busy
+            dim[pr] = make_float2((sh2[pr].x + nim.x) + sl2[pr].x, (sh2[pr].y + nim.y) + sl2[pr].y);
+            rn[pr] = make_float2(rcp_approx(fmaf(dim[pr].x, dim[pr].x, re2.x)),
+                                 rcp_approx(fmaf(dim[pr].y, dim[pr].y, re2.y)));
+#else
+            dim[pr] = __fadd2_rn(__fadd2_rn(sh2[pr], nim), sl2[pr]);
+            const float2 n2 = __ffma2_rn(dim[pr], dim[pr], re2);
+            rn[pr] = make_float2(rcp_approx(n2.x), rcp_approx(n2.y));
+#endif
+          }
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float4 b4 = p4[1 + 2 * w], c4 = p4[2 + 2 * w];
+            const float2 wy = make_float2(b4.x, b4.y), wax = make_float2(b4.z, b4.w);
+            const float2 nwx = make_float2(c4.x, c4.y), way = make_float2(c4.z, c4.w);
+#pragma unroll
+            for (int pr = 0; pr < NPR; ++pr) {
+              const float2 tx = __ffma2_rn(dim[pr], wy, wax);
+              const float2 ty = __ffma2_rn(dim[pr], nwx, way);
+              ax[pr][w] = __ffma2_rn(rn[pr], tx, ax[pr][w]);
+              ay[pr][w] = __ffma2_rn(rn[pr], ty, ay[pr][w]);
+            }
+          }
+        }
+        }  // groups
+        continue;
+      }
       for (int g = 0; g < (GRP && grouped ? kFarGroups : 1); ++g) {
       int jlo = 0, jhi = jn;
       if (GRP && grouped) {
@@ -837,179 +881,135 @@ __global__ void __launch_bounds__(T, RPT >= 4 ? (RANK >= 2 ? S4_CAUCHY_MINB_FAR2
       }
 #pragma unroll kCauchyUnroll
       for (int jj = jlo; jj < jhi; ++jj) {
+        float pr[PS];
         const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
-        const float4 pl = p4[0];
-        const float2 nim = make_float2(pl.x, pl.y), re2 = make_float2(pl.z, pl.w);
-        float2 dim[NPR], rn[NPR];
 #pragma unroll
-        for (int pr = 0; pr < NPR; ++pr) {
-#if S4_CAUCHY_SCALAR_DEN
-          // the denominators in scalar instructions, which may issue to the FMA
-          // pipe's other half while the packed products keep the first busy
-          dim[pr] = make_float2((sh2[pr].x + nim.x) + sl2[pr].x, (sh2[pr].y + nim.y) + sl2[pr].y);
-          rn[pr] = make_float2(rcp_approx(fmaf(dim[pr].x, dim[pr].x, re2.x)),
-                               rcp_approx(fmaf(dim[pr].y, dim[pr].y, re2.y)));
-#else
-          dim[pr] = __fadd2_rn(__fadd2_rn(sh2[pr], nim), sl2[pr]);
-          const float2 n2 = __ffma2_rn(dim[pr], dim[pr], re2);
-          rn[pr] = make_float2(rcp_approx(n2.x), rcp_approx(n2.y));
-#endif
+        for (int v = 0; v < PS / 4; ++v) {
+          const float4 t = p4[v];
+          pr[4 * v] = t.x;
+          pr[4 * v + 1] = t.y;
+          pr[4 * v + 2] = t.z;
+          pr[4 * v + 3] = t.w;
         }
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float4 b4 = p4[1 + 2 * w], c4 = p4[2 + 2 * w];
-          const float2 wy = make_float2(b4.x, b4.y), wax = make_float2(b4.z, b4.w);
-          const float2 nwx = make_float2(c4.x, c4.y), way = make_float2(c4.z, c4.w);
+        for (int rr = 0; rr < RPT; ++rr) {
+          const float dim = (shi[rr] - pr[0]) + slo[rr];
+          const float n2 = fmaf(dim, dim, pr[1]);
+          const float rn = rcp_approx(n2);
 #pragma unroll
-          for (int pr = 0; pr < NPR; ++pr) {
-            const float2 tx = __ffma2_rn(dim[pr], wy, wax);
-            const float2 ty = __ffma2_rn(dim[pr], nwx, way);
-            ax[pr][w] = __ffma2_rn(rn[pr], tx, ax[pr][w]);
-            ay[pr][w] = __ffma2_rn(rn[pr], ty, ay[pr][w]);
+          for (int w = 0; w < NW; ++w) {
+            const float wx = pr[2 + 4 * w], wy = pr[3 + 4 * w];
+            const float tx = fmaf(dim, wy, pr[4 + 4 * w]);
+            const float ty = fmaf(-dim, wx, pr[5 + 4 * w]);
+            acc[rr][w].x = fmaf(rn, tx, acc[rr][w].x);
+            acc[rr][w].y = fmaf(rn, ty, acc[rr][w].y);
           }
         }
       }
       }  // groups
-      continue;
     }
-    for (int g = 0; g < (GRP && grouped ? kFarGroups : 1); ++g) {
-    int jlo = 0, jhi = jn;
-    if (GRP && grouped) {
-      if (!((gnear >> g) & 1u)) continue;
-      jlo = max((int)musg[g * GSL + 1].y - j0, 0);
-      jhi = min((g + 1 < kFarGroups ? (int)musg[(g + 1) * GSL + 1].y : N) - j0, jn);
-    }
-#pragma unroll kCauchyUnroll
-    for (int jj = jlo; jj < jhi; ++jj) {
-      float pr[PS];
-      const float4* p4 = reinterpret_cast<const float4*>(par + jj * PS);
+
+    if constexpr (PACKED) {
 #pragma unroll
-      for (int v = 0; v < PS / 4; ++v) {
-        const float4 t = p4[v];
-        pr[4 * v] = t.x;
-        pr[4 * v + 1] = t.y;
-        pr[4 * v + 2] = t.z;
-        pr[4 * v + 3] = t.w;
-      }
-#pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) {
-        const float dim = (shi[rr] - pr[0]) + slo[rr];
-        const float n2 = fmaf(dim, dim, pr[1]);
-        const float rn = rcp_approx(n2);
+      for (int pr = 0; pr < NPR; ++pr)
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float wx = pr[2 + 4 * w], wy = pr[3 + 4 * w];
-          const float tx = fmaf(dim, wy, pr[4 + 4 * w]);
-          const float ty = fmaf(-dim, wx, pr[5 + 4 * w]);
-          acc[rr][w].x = fmaf(rn, tx, acc[rr][w].x);
-          acc[rr][w].y = fmaf(rn, ty, acc[rr][w].y);
+          acc[2 * pr][w] = make_float2(ax[pr][w].x, ay[pr][w].x);
+          acc[2 * pr + 1][w] = make_float2(ax[pr][w].y, ay[pr][w].y);
         }
+    }
+
+    // far warps: the series of the whole set; near warps of a grouped channel: the
+    // series of each group they are far from, added to the direct sums of the others
+    if (FAR && (warp_far || (GRP && grouped))) {
+      bool live[RPT];
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) live[rr] = pos[rr] < M && !zm1[rr];
+      if (warp_far) {
+        far_series<NW, RPT, PACKED, FP, false>(mus + 2, fc, fR, shi, slo, live, acc);
+      } else if constexpr (GRP) {
+#pragma unroll
+        for (int g = 0; g < kFarGroups; ++g)
+          if (!((gnear >> g) & 1u))
+            far_series<NW, RPT, PACKED, FP, true>(musg + g * GSL + 2, musg[g * GSL], musg[g * GSL + 1].x, shi, slo,
+                                                  live, acc);
       }
     }
-    }  // groups
-  }
-
-  if constexpr (PACKED) {
+    // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
+    // when the pole loop was skipped, else the loop's sum
+    float2 cb_all;
+    if (FAR && cta_far) {
+      cb_all = mus[2];
+    } else {
 #pragma unroll
-    for (int pr = 0; pr < NPR; ++pr)
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        acc[2 * pr][w] = make_float2(ax[pr][w].x, ay[pr][w].x);
-        acc[2 * pr + 1][w] = make_float2(ax[pr][w].y, ay[pr][w].y);
+      for (int o = 16; o > 0; o >>= 1) {
+        cb.x += __shfl_xor_sync(0xffffffffu, cb.x, o);
+        cb.y += __shfl_xor_sync(0xffffffffu, cb.y, o);
       }
-  }
-
-  // far warps: the series of the whole set; near warps of a grouped channel: the
-  // series of each group they are far from, added to the direct sums of the others
-  if (FAR && (warp_far || (GRP && grouped))) {
-    bool live[RPT];
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) live[rr] = pos[rr] < M && !zm1[rr];
-    if (warp_far) {
-      far_series<NW, RPT, PACKED, FP, false>(mus + 2, fc, fR, shi, slo, live, acc);
-    } else if constexpr (GRP) {
-#pragma unroll
-      for (int g = 0; g < kFarGroups; ++g)
-        if (!((gnear >> g) & 1u))
-          far_series<NW, RPT, PACKED, FP, true>(musg + g * GSL + 2, musg[g * GSL], musg[g * GSL + 1].x, shi, slo,
-                                                live, acc);
+      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cb;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float2 t = make_float2(0.f, 0.f);
+        for (int i = 0; i < T / 32; ++i) t = cadd(t, red[i]);
+        red[T / 32] = t;
+      }
+      __syncthreads();
+      cb_all = red[T / 32];
     }
-  }
-  // C~^* B over all poles, for the root z = -1: the zeroth moment of that weight
-  // when the pole loop was skipped, else the loop's sum
-  float2 cb_all;
-  if (FAR && cta_far) {
-    cb_all = mus[2];
-  } else {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      cb.x += __shfl_xor_sync(0xffffffffu, cb.x, o);
-      cb.y += __shfl_xor_sync(0xffffffffu, cb.y, o);
-    }
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cb;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float2 t = make_float2(0.f, 0.f);
-      for (int i = 0; i < T / 32; ++i) t = cadd(t, red[i]);
-      red[T / 32] = t;
-    }
-    __syncthreads();
-    cb_all = red[T / 32];
-  }
 
 #pragma unroll
-  for (int rr = 0; rr < RPT; ++rr) {
-    if (pos[rr] >= M) continue;
-    float2 Hk = make_float2(0.f, 0.f);
-    if (!bad) {
-      if (zm1[rr]) {
-        Hk = cscale(cb_all, 0.5f * delta);
-      } else {
-        // (far tiles cannot meet a resonance: a non-finite value there shows in Hk)
-        bool fin = true;
-        if (!(FAR && warp_far)) {
-#pragma unroll
-          for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
-        }
-        if (!fin) {
-          // an exactly zero denominator gives inf/nan; tell it apart from overflow
-          bool res = false;
-          for (int j = 0; j < N; ++j) {
-            const float2 lam = Lambda[(size_t)h * N + j];
-            const float dim = (shi[rr] - lam.y) + slo[rr];
-            res = res || (fmaf(dim, dim, lam.x * lam.x) == 0.f);
-          }
-          flags |= res ? ST_RES_DIAG : ST_NONFINITE;
-          st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
-          continue;
-        }
-        float2 Wm[RANK][RANK], z[RANK];
-#pragma unroll
-        for (int i = 0; i < RANK; ++i) {
-          z[i] = acc[rr][1 + RANK + i];
-#pragma unroll
-          for (int l = 0; l < RANK; ++l) {
-            Wm[i][l] = acc[rr][1 + 2 * RANK + i * RANK + l];
-            if (i == l) Wm[i][l].x += 1.f;
-          }
-        }
-        if (!solve_small<RANK>(Wm, z)) {
-          flags |= ST_RES_CORR;
+    for (int rr = 0; rr < RPT; ++rr) {
+      if (pos[rr] >= M) continue;
+      float2 Hk = make_float2(0.f, 0.f);
+      if (!bad) {
+        if (zm1[rr]) {
+          Hk = cscale(cb_all, 0.5f * delta);
         } else {
-          float2 g = acc[rr][0];
+          // (far tiles cannot meet a resonance: a non-finite value there shows in Hk)
+          bool fin = true;
+          if (!(FAR && warp_far)) {
 #pragma unroll
-          for (int l = 0; l < RANK; ++l) g = csub(g, cmul(acc[rr][1 + l], z[l]));
-          Hk = make_float2(fmaf(-th[rr], g.y, g.x), fmaf(th[rr], g.x, g.y));
-          if (!cfinite(Hk)) {
-            flags |= ST_NONFINITE;
-            Hk = make_float2(0.f, 0.f);
+            for (int w = 0; w < NW; ++w) fin = fin && cfinite(acc[rr][w]);
+          }
+          if (!fin) {
+            // an exactly zero denominator gives inf/nan; tell it apart from overflow
+            bool res = false;
+            for (int j = 0; j < N; ++j) {
+              const float2 lam = Lambda[(size_t)h * N + j];
+              const float dim = (shi[rr] - lam.y) + slo[rr];
+              res = res || (fmaf(dim, dim, lam.x * lam.x) == 0.f);
+            }
+            flags |= res ? ST_RES_DIAG : ST_NONFINITE;
+            st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
+            continue;
+          }
+          float2 Wm[RANK][RANK], z[RANK];
+#pragma unroll
+          for (int i = 0; i < RANK; ++i) {
+            z[i] = acc[rr][1 + RANK + i];
+#pragma unroll
+            for (int l = 0; l < RANK; ++l) {
+              Wm[i][l] = acc[rr][1 + 2 * RANK + i * RANK + l];
+              if (i == l) Wm[i][l].x += 1.f;
+            }
+          }
+          if (!solve_small<RANK>(Wm, z)) {
+            flags |= ST_RES_CORR;
+          } else {
+            float2 g = acc[rr][0];
+#pragma unroll
+            for (int l = 0; l < RANK; ++l) g = csub(g, cmul(acc[rr][1 + l], z[l]));
+            Hk = make_float2(fmaf(-th[rr], g.y, g.x), fmaf(th[rr], g.x, g.y));
+            if (!cfinite(Hk)) {
+              flags |= ST_NONFINITE;
+              Hk = make_float2(0.f, 0.f);
+            }
           }
         }
       }
+      st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
     }
-    st_chk(Khat, (long long)h * M + pos[rr], (long long)gridDim.x * M, Hk);
-  }
-  if constexpr (!FAR) break;  // one tile per CTA
+    if constexpr (!FAR) break;  // one tile per CTA
   }  // tiles
   if (flags) st_flag(status, flags);
 }
