@@ -94,6 +94,9 @@ def test_layer_matches_oracle(wi, nch, full_rows):
     (8, 2, 2, 40000, 1),
     # L = M on long rows: the spectrum's even bins taken from the root values
     (8, 1, 3, 8192, 3), (6, 2, 2, 32768, 1), (4, 1, 2, 65536, 1),
+    # N = 256 at rank 1 on grids of H M >= 2^19.6: far-field series with pole groups,
+    # with the half spectrum at radix 16 (L = M = 16384) and the full one (L < M)
+    (256, 1, 48, 16384, 2), (256, 1, 16, 40000, 1),
     # M = 32 and 512 (kspec with staged twiddle tables), M = 2048 (unstaged)
     (6, 1, 3, 20, 3), (8, 1, 3, 300, 2), (8, 2, 2, 2048, 3),
 ])
@@ -102,6 +105,15 @@ def test_edge_sizes(N, r, H, L, batch):
     p = W.make_params(w)
     u = W.make_u(w, p)
     K_gpu, y_gpu = run_layer(p, u)
+    if N * N * L * H > 2e10:  # the oracle's kernel on a sample of channels
+        chans = [0, H // 2, H - 1]
+        K_ref = O.s4_kernel_channels(p, L, chans)
+        assert rel_l2(K_gpu[chans], K_ref) <= REL_K, rel_l2(K_gpu[chans], K_ref)
+        ts = [0, 1, L // 3, L // 2, L - 2, L - 1]
+        y_ref = np.array([[O.causal_conv_at(K_ref[ci], u[b, h], p["D"][h], ts) for ci, h in enumerate(chans)]
+                          for b in range(batch)])
+        check_y(y_gpu[:, chans][:, :, ts], y_ref, f"edge N{N} r{r} L{L}")
+        return
     K_ref = O.s4_kernel_channels(p, L)
     assert rel_l2(K_gpu, K_ref) <= REL_K, rel_l2(K_gpu, K_ref)
     if L <= 20000:
