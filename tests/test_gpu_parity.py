@@ -142,6 +142,25 @@ def test_kernel_gen_and_conv_separately():
     check_y(np.stack([y[b, h] for b, h in rows]), y_ref, "conv only")
 
 
+@pytest.mark.parametrize("batch,H,L", [(2, 30, 32768), (3, 26, 65536)])
+def test_long_row_conv_many_pairs(batch, H, L):
+    # the four-step convolution alone on 30 and 52 pairs of rows (2M = 2^16 with
+    # radix-16 columns, 2^17 with radix 32; the odd batch leaves each channel's
+    # last pair with one row), rows across the whole scratch
+    rng = np.random.default_rng(H * L + batch)
+    u = rng.standard_normal((batch, H, L)).astype(np.float32)
+    Kin = ((rng.standard_normal((H, L)) + 1j * rng.standard_normal((H, L))) * 0.01).astype(np.complex64)
+    D = rng.standard_normal(H).astype(np.float32)
+    ut, Kt, Dt = torch.from_numpy(u).cuda(), torch.from_numpy(Kin).cuda(), torch.from_numpy(D).cuda()
+    y = s4.s4_conv_fwd(ut, Kt, Dt).cpu().numpy()
+    assert np.array_equal(y, s4.s4_conv_fwd(ut, Kt, Dt).cpu().numpy())
+    pb = (batch + 1) // 2
+    # pair p = h pb + b // 2: the first pairs, the middle, the last pair
+    rows = [(0, 0), (batch - 1, H - 1), (0, 24 // pb), (batch - 1, 25 // pb), (batch // 2, H // 2), (1, H - 2)]
+    y_ref = np.stack([O.causal_conv(Kin[h], u[b, h], D[h]) for b, h in rows])
+    check_y(np.stack([y[b, h] for b, h in rows]), y_ref, f"conv L{L} pairs {pb * H}")
+
+
 def test_scalar_example_conv_gives_prefix_sums():
     # Page example: K = (1, ..., 1), D = 0  =>  y_t = sum_{s<=t} u_s.
     L = 8
