@@ -286,7 +286,6 @@ __global__ void __launch_bounds__(256) cauchy_moments_grouped_kernel(
   __shared__ float scr[NS][3];             // centre and radius of each set (0: all poles)
   __shared__ float sred[T / 32][4];
   __shared__ float2 pw0[JC][P], pwg[JC][P];  // powers of a chunk's poles about the whole set / their group
-  __shared__ int sgrp[JC];
   pdl_wait();
   st_record_gen(status);
   pdl_launch_dependents();
