@@ -97,6 +97,8 @@ def test_layer_matches_oracle(wi, nch, full_rows):
     # N = 256 at rank 1 on grids of H M >= 2^19.6: far-field series with pole groups,
     # with the half spectrum at radix 16 (L = M = 16384) and the full one (L < M)
     (256, 1, 48, 16384, 2), (256, 1, 16, 40000, 1),
+    # the far-field series at ranks 3 and 4 (N >= 48 poles, M >= 8192 roots), long rows
+    (64, 3, 2, 8192, 2), (48, 4, 2, 16384, 1),
     # M = 32 and 512 (kspec with staged twiddle tables), M = 2048 (unstaged)
     (6, 1, 3, 20, 3), (8, 1, 3, 300, 2), (8, 2, 2, 2048, 3),
 ])
@@ -504,7 +506,7 @@ def test_packed_root_values_equal_scalar_bitwise():
     assert rel_l2(K1, K_ref) <= REL_K
 
 
-@pytest.mark.parametrize("r,dt", [(1, 1e-4), (1, 1e-2), (2, 1e-3)])
+@pytest.mark.parametrize("r,dt", [(1, 1e-4), (1, 1e-2), (2, 1e-3), (3, 1e-3), (4, 1e-4)])
 def test_far_root_series_against_the_definition(r, dt):
     # Channels whose roots are almost all far from the poles (N = 256 poles spread
     # over 800 along the imaginary axis, a = 2/Delta >= 200): nearly every CTA
